@@ -1,0 +1,225 @@
+/*
+ * strata_moe.h -- C ABI of the GB300 (sm_103a) routed mixture-of-experts FFN
+ * forward: router -> top-K -> int4-block-quantized SwiGLU experts -> weighted
+ * combine with a sigmoid-gated shared expert.
+ *
+ * What the operation is (the pages describe it in engineering notes, never as
+ * a formula; the plain reading taken here is stated with each call):
+ *   Strata, "Qwen3.6-35B-A3B: pictures, several requests at once and speed",
+ *   section "Speed": a 256-expert, top-8 MoE whose router and shared-expert
+ *   gate are one product, SwiGLU experts, router top-k and grouping in one
+ *   launch, the weighted sum of the experts ("the MoE end").  Section
+ *   "Several requests at once": every routed expert two tokens share is read
+ *   once for both.  PolyStrata, "Models and backends", section "What was
+ *   tuned": a launch covers a call's experts together, one launch adds them up.
+ *
+ * Conventions for every call
+ *   - Pointers named *_dev are device pointers; nothing else is.  The caller
+ *     allocates every buffer; the library allocates nothing, frees nothing and
+ *     never synchronises inside a forward call.  It keeps no pointer across
+ *     calls.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) in call order.
+ *   - `ws_dev` is a caller-owned device workspace of at least
+ *     moe_workspace_bytes(dims, max_tokens) bytes, 256-byte aligned, created
+ *     zero-filled once (the library keeps it consistent afterwards).  Two
+ *     calls that may run at the same time (two streams) must not share a
+ *     workspace: the pages report silent corruption from exactly that sharing
+ *     (colibri, "qwen36: CUDA VRAM expert tier", section "Placement").
+ *   - Host-side validation comes first: an unsupported shape, a NULL or
+ *     misaligned pointer, T < 0, T > the workspace's max_tokens or a too-small
+ *     workspace returns STRATA_EINVAL with nothing launched.  T == 0 returns
+ *     STRATA_OK and launches nothing.  A failed launch returns STRATA_ECUDA.
+ *   - Kernels never trap.  A forced expert id outside [0, E) is skipped and
+ *     latches STRATA_EBADROUTE in the workspace's error word; a bounded wait
+ *     that runs out latches STRATA_ETIMEOUT.  moe_get_device_status reads and
+ *     clears the word.
+ *   - Results are deterministic: ids, permutations and every floating sum are
+ *     computed in a fixed order, with no floating-point atomics.
+ *
+ * Supported shapes: group == 32; hidden H a multiple of 256 in [256, 4096];
+ * n_experts E in [1, 1024]; top_k K in [1, min(E, 16)]; inter I and
+ * shared_inter Is each one of 64, 128, 256, 512, 1024.
+ *
+ * Packed-weight layout (16-byte aligned planes; a layer is one caller-owned
+ * allocation or several, any order):
+ *   router      bf16 [E+1][H]: row e < E is expert e's router row, row E is
+ *               the shared-expert gate vector (one more row of the same
+ *               product, as on the Strata page).
+ *   router_bias fp32 [E] added to the logits before selection, or NULL.
+ *   gu_q        uint8 [E][2I][H/2]   gate/up rows interleaved: row 2i is
+ *               gate row i, row 2i+1 is up row i.
+ *   gu_s        fp16  [E][2I][H/32]  one scale per 32 consecutive inputs.
+ *   dn_q        uint8 [E][H][I/2],  dn_s fp16 [E][H][I/32]
+ *   sh_gu_q/s, sh_dn_q/s: the same for the one shared expert with Is.
+ *   int4 nibbles: byte b of a row holds element 2b in bits 0..3 and element
+ *   2b+1 in bits 4..7, offset-binary: weight = scale * (nibble - 8), the
+ *   signed value "one XOR with 0x88888888" yields ("Every Public GGUF of This
+ *   Model Is Missing Its Head", section 5).  Symmetric: no zero point.
+ */
+#ifndef STRATA_MOE_H
+#define STRATA_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define STRATA_API __attribute__((visibility("default")))
+#else
+#define STRATA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    STRATA_OK = 0,
+    STRATA_EINVAL = 1,        /* bad argument; nothing launched            */
+    STRATA_ECUDA = 2,         /* a CUDA launch or query failed             */
+    STRATA_EUNSUPPORTED = 3,  /* valid request this build does not handle  */
+    STRATA_ETIMEOUT = 4,      /* a bounded device wait ran out (latched)   */
+    STRATA_EBADROUTE = 5      /* a forced expert id was out of range (latched) */
+} strata_status;
+
+typedef struct {
+    int32_t hidden;        /* H */
+    int32_t n_experts;     /* E */
+    int32_t top_k;         /* K */
+    int32_t inter;         /* I, routed expert intermediate size */
+    int32_t shared_inter;  /* Is, shared expert intermediate size */
+    int32_t group;         /* scale group along the input axis; must be 32 */
+} strata_moe_dims;
+
+typedef struct {
+    const void* router_dev;          /* bf16 [E+1][H] */
+    const float* router_bias_dev;    /* fp32 [E] or NULL */
+    const uint8_t* gu_q_dev;   const uint16_t* gu_s_dev;
+    const uint8_t* dn_q_dev;   const uint16_t* dn_s_dev;
+    const uint8_t* sh_gu_q_dev; const uint16_t* sh_gu_s_dev;
+    const uint8_t* sh_dn_q_dev; const uint16_t* sh_dn_s_dev;
+} strata_moe_layer;
+
+/* Bytes of workspace the calls below need for up to max_tokens tokens of a
+ * layer of shape *dims; 0 when the shape is unsupported or max_tokens < 1. */
+STRATA_API size_t moe_workspace_bytes(const strata_moe_dims* dims, int32_t max_tokens);
+
+/* The T at and below which the calls take the decode (GEMV) kernels; above
+ * it they take the tcgen05 grouped-GEMM (prefill) kernels. */
+STRATA_API int32_t moe_decode_max_tokens(void);
+
+/* Input RMSNorm, unit weight:  x[t][h] = bf16( r[t][h] / sqrt(mean_h r^2 + eps) ).
+ * Strata "Speed": "add+norm+q8_1 in one launch" is the norm in front of the
+ * MoE; this build keeps bf16 activations.
+ * r_dev fp32 [T][H] (in), x_dev bf16 [T][H] (out). */
+STRATA_API strata_status moe_rmsnorm(const float* r_dev, int32_t T, int32_t H, float eps, void* x_dev,
+                          void* stream);
+
+/* Router product, top-K selection and renormalised softmax, shared gate.
+ *   logits[t][e] = sum_h x[t][h] router[e][h] + bias[e]     (fp32 sums)
+ *   ids[t][.]    the K largest logits, ties to the lower expert id (PolyStrata
+ *                "What was tuned": the first of equal values wins), stored in
+ *                ascending expert id
+ *   weights[t][k] = exp(l_k - m) / sum_k' exp(l_k' - m) over the selected,
+ *                m the largest selected logit (softmax over all E followed by
+ *                renormalisation over the K selected is the same number)
+ *   shared_gate[t] = 1 / (1 + exp(-sum_h x[t][h] router[E][h]))
+ * x_dev bf16 [T][H]; ids_dev int32 [T][K]; weights_dev fp32 [T][K];
+ * shared_gate_dev fp32 [T]; logits_dev fp32 [T][E] or NULL. */
+STRATA_API strata_status moe_route(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                        const void* x_dev, int32_t T, int32_t* ids_dev, float* weights_dev,
+                        float* shared_gate_dev, float* logits_dev, void* ws_dev,
+                        size_t ws_bytes, void* stream);
+
+/* Bucketing of the T*K (token, k) pairs by expert (Strata "Speed": router
+ * top-k and grouping; the one-thread `k_group` the page found slow is a
+ * block-parallel counting sort here):
+ *   counts[e]      number of pairs routed to e
+ *   offsets[0..E]  exclusive prefix sum of counts, offsets[E] = T*K
+ *   perm[slot]     t*K + k, slots of one expert in ascending t (stable)
+ *   inv_perm[t*K+k] = slot
+ * ids_dev int32 [T][K] from any source (forced routing allowed); an id out of
+ * range is skipped and latches STRATA_EBADROUTE. */
+STRATA_API strata_status moe_permute(const strata_moe_dims* dims, const int32_t* ids_dev, int32_t T,
+                          int32_t* counts_dev, int32_t* offsets_dev, int32_t* perm_dev,
+                          int32_t* inv_perm_dev, void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Routed experts' gate/up product and SwiGLU (every expert's weights are read
+ * once for all tokens routed to it: Strata "Several requests at once").
+ * For each slot s of expert e (offsets) and token t = perm[s] / K:
+ *   g_i = sum_h x[t][h] Wg[e][i][h],  u_i = sum_h x[t][h] Wu[e][i][h]
+ *   h[s][i] = g_i / (1 + exp(-g_i)) * u_i
+ * with W = fp16 scale * (nibble - 8).  h_dev fp32 [T*K][I] (out). */
+STRATA_API strata_status moe_expert_gate_up(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                                 const void* x_dev, int32_t T, const int32_t* offsets_dev,
+                                 const int32_t* perm_dev, float* h_dev, void* ws_dev,
+                                 size_t ws_bytes, void* stream);
+
+/* Routed experts' down product: y[s][o] = sum_i h[s][i] Wd[e][o][i] for every
+ * slot s of expert e.  h_dev fp32 [T*K][I] (in), y_dev bf16 [T*K][H] (out). */
+STRATA_API strata_status moe_expert_down(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                              const float* h_dev, int32_t T, const int32_t* offsets_dev,
+                              void* y_dev, void* ws_dev, size_t ws_bytes, void* stream);
+
+/* moe_expert_gate_up followed by moe_expert_down, h kept in the workspace.
+ * y_dev bf16 [T*K][H], permuted (slot) order. */
+STRATA_API strata_status moe_expert_ffn(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                             const void* x_dev, int32_t T, const int32_t* offsets_dev,
+                             const int32_t* perm_dev, void* y_dev, void* ws_dev,
+                             size_t ws_bytes, void* stream);
+
+/* Shared expert and weighted combine ("the MoE end", Strata "Speed"; "one
+ * launch adds up a call's experts", PolyStrata "What was tuned"):
+ *   S[t]        the shared SwiGLU expert on x[t] (same arithmetic, Is)
+ *   out[t][o] = bf16( sum_{k ascending} w[t][k] y[inv[t*K+k]][o]
+ *                     + shared_gate[t] S[t][o] )       (fp32 sum)
+ * y_dev bf16 [T*K][H]; inv_perm_dev int32 [T*K]; weights_dev fp32 [T][K];
+ * shared_gate_dev fp32 [T]; out_dev bf16 [T][H]. */
+STRATA_API strata_status moe_combine(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                          const void* x_dev, int32_t T, const void* y_dev,
+                          const int32_t* inv_perm_dev, const float* weights_dev,
+                          const float* shared_gate_dev, void* out_dev, void* ws_dev,
+                          size_t ws_bytes, void* stream);
+
+/* The whole layer: route, permute, experts, shared expert, combine.  For
+ * T <= moe_decode_max_tokens() it runs three fused decode kernels (router +
+ * shared gate/up + selection + permutation in one; routed gate/up in one;
+ * every down product + combine in one); above, the tcgen05 prefill kernels.
+ * ids_dev / weights_dev / shared_gate_dev receive the routing when non-NULL.
+ * out_dev bf16 [T][H]. */
+STRATA_API strata_status moe_layer_forward(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                                const void* x_dev, int32_t T, int32_t* ids_dev,
+                                float* weights_dev, float* shared_gate_dev, void* out_dev,
+                                void* ws_dev, size_t ws_bytes, void* stream);
+
+/* As moe_layer_forward, but with the routing forced: ids_dev / weights_dev
+ * (in) replace the router's choice; shared_gate is still computed. */
+STRATA_API strata_status moe_layer_forward_routed(const strata_moe_dims* dims,
+                                       const strata_moe_layer* layer, const void* x_dev,
+                                       int32_t T, const int32_t* ids_dev,
+                                       const float* weights_dev, void* out_dev, void* ws_dev,
+                                       size_t ws_bytes, void* stream);
+
+/* One residual MoE block of a layer stack:
+ *   x = bf16(rmsnorm(resid, eps));  out = layer(x);  resid += float(out)
+ * resid_dev fp32 [T][H] (in/out).  ids_dev / weights_dev: NULL to route, or
+ * both non-NULL to force the routing.  x_out_dev / out_dev: optional bf16
+ * [T][H] copies of the block's input and output (NULL: workspace only). */
+STRATA_API strata_status moe_block_forward(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                                float* resid_dev, int32_t T, float eps, const int32_t* ids_dev,
+                                const float* weights_dev, void* x_out_dev, void* out_dev,
+                                void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the status latched in the workspace's error
+ * word (STRATA_OK when none) and clears the word.  For tests and debugging;
+ * it is the one call that synchronises. */
+STRATA_API strata_status moe_get_device_status(void* ws_dev, void* stream);
+
+/* Static, human-readable name of a status. */
+STRATA_API const char* strata_status_str(strata_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STRATA_MOE_H */

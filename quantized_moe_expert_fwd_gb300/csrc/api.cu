@@ -1,0 +1,458 @@
+// api.cu -- the C ABI of strata_moe.h: argument checks, workspace layout and
+// dispatch to the decode (GEMV) or prefill (tcgen05 GEMM) kernels.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace strata {
+
+static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(const strata_moe_dims& d, int T) {
+    const size_t H = d.hidden, E = d.n_experts, K = d.top_k, I = d.inter, Is = d.shared_inter;
+    const size_t t = size_t(T > 0 ? T : 1);
+    WsLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    L.ctl = take(sizeof(Ctl));
+    L.logits = take(t * (E + 1) * 4);
+    L.ids = take(t * K * 4);
+    L.w = take(t * K * 4);
+    L.sig = take(t * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm = take(t * K * 4);
+    L.inv = take(t * K * 4);
+    L.h = take(t * K * I * 4);
+    L.hs = take(t * Is * 4);
+    L.x = take(t * H * 2);
+    L.out = take(t * H * 2);
+    L.tiles = L.xf16 = L.hf16 = L.y = L.shy = 0;
+    L.total = o;
+    return L;
+}
+
+Dev device_info() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    int sms = cache[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0)
+            sms = 1;
+        cache[dev].store(sms, std::memory_order_relaxed);
+    }
+    return Dev{sms};
+}
+
+}  // namespace strata
+
+using namespace strata;
+
+namespace {
+
+bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+bool dims_ok(const strata_moe_dims* d) {
+    if (d == nullptr) return false;
+    if (d->group != 32) return false;
+    if (d->hidden < 256 || d->hidden > 4096 || d->hidden % 256 != 0) return false;
+    if (d->n_experts < 1 || d->n_experts > kMaxExperts) return false;
+    if (d->top_k < 1 || d->top_k > kMaxTopK || d->top_k > d->n_experts) return false;
+    if (!pow2_in(d->inter, 64, 1024) || !pow2_in(d->shared_inter, 64, 1024)) return false;
+    return true;
+}
+
+bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool al4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool opt4(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+enum Need { kRouter = 1, kRouted = 2, kShared = 4 };
+
+bool layer_ok(const strata_moe_layer* L, int need) {
+    if (L == nullptr) return false;
+    if ((need & kRouter) && (!al16(L->router_dev) || !opt4(L->router_bias_dev))) return false;
+    if ((need & kRouted) &&
+        (!al16(L->gu_q_dev) || !al16(L->gu_s_dev) || !al16(L->dn_q_dev) || !al4(L->dn_s_dev)))
+        return false;
+    if ((need & kShared) && (!al16(L->sh_gu_q_dev) || !al16(L->sh_gu_s_dev) ||
+                             !al16(L->sh_dn_q_dev) || !al4(L->sh_dn_s_dev)))
+        return false;
+    return true;
+}
+
+bool ws_ok(const strata_moe_dims* d, int T, const void* ws, size_t bytes) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return false;
+    return bytes >= ws_layout(*d, T).total;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+    return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+strata_status cuda_status(cudaError_t e) { return e == cudaSuccess ? STRATA_OK : STRATA_ECUDA; }
+
+#define STRATA_TRY(expr)                                   \
+    do {                                                   \
+        const cudaError_t _e = (expr);                     \
+        if (_e != cudaSuccess) return STRATA_ECUDA;        \
+    } while (0)
+
+// One layer on the decode kernels.  forced_ids/forced_w: NULL to route.
+strata_status decode_layer(const strata_moe_dims* d, const strata_moe_layer* L, const void* x,
+                           int T, const int32_t* forced_ids, const float* forced_w,
+                           int32_t* ids_user, float* w_user, float* sig_user, void* out,
+                           float* resid, void* ws, cudaStream_t s) {
+    const WsLayout W = ws_layout(*d, T);
+    RouteLaunch r{};
+    r.router = static_cast<const uint16_t*>(L->router_dev);
+    r.bias = L->router_bias_dev;
+    r.x = static_cast<const uint16_t*>(x);
+    r.logits = at<float>(ws, W.logits);
+    r.shq = L->sh_gu_q_dev;
+    r.shs = L->sh_gu_s_dev;
+    r.hs = at<float>(ws, W.hs);
+    r.Is = d->shared_inter;
+    r.do_shared = 1;
+    r.do_select = forced_ids == nullptr ? 1 : 0;
+    r.ids = at<int32_t>(ws, W.ids);
+    r.w = at<float>(ws, W.w);
+    r.sig = at<float>(ws, W.sig);
+    r.ids_user = ids_user;
+    r.w_user = w_user;
+    r.sig_user = sig_user;
+    r.logits_user = nullptr;
+    r.ids_in = forced_ids;
+    r.w_in = forced_w;
+    r.do_permute = 1;
+    r.counts = at<int32_t>(ws, W.counts);
+    r.offsets = at<int32_t>(ws, W.offsets);
+    r.perm = at<int32_t>(ws, W.perm);
+    r.inv = at<int32_t>(ws, W.inv);
+    r.ctl = at<void>(ws, W.ctl);
+    r.T = T;
+    r.H = d->hidden;
+    r.E = d->n_experts;
+    r.K = d->top_k;
+    STRATA_TRY(launch_route_decode(r, s));
+
+    GuLaunch g{};
+    g.q = L->gu_q_dev;
+    g.sc = L->gu_s_dev;
+    g.x = r.x;
+    g.offsets = r.offsets;
+    g.perm = r.perm;
+    g.h = at<float>(ws, W.h);
+    g.err = &at<Ctl>(ws, W.ctl)->err;
+    g.T = T;
+    g.H = d->hidden;
+    g.I = d->inter;
+    g.E = d->n_experts;
+    g.K = d->top_k;
+    g.shared = 0;
+    STRATA_TRY(launch_gate_up_decode(g, s));
+
+    DownLaunch dn{};
+    dn.q = L->dn_q_dev;
+    dn.sc = L->dn_s_dev;
+    dn.shq = L->sh_dn_q_dev;
+    dn.shs = L->sh_dn_s_dev;
+    dn.h = g.h;
+    dn.hs = r.hs;
+    dn.offsets = r.offsets;
+    dn.inv = r.inv;
+    dn.w = r.w;
+    dn.sig = r.sig;
+    dn.out = static_cast<uint16_t*>(out);
+    dn.resid = resid;
+    dn.err = g.err;
+    dn.T = T;
+    dn.H = d->hidden;
+    dn.I = d->inter;
+    dn.Is = d->shared_inter;
+    dn.E = d->n_experts;
+    dn.K = d->top_k;
+    dn.mode = kDownFused;
+    STRATA_TRY(launch_down_decode(dn, s));
+    return STRATA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const strata_moe_dims* dims, int32_t max_tokens) {
+    if (!dims_ok(dims) || max_tokens < 1) return 0;
+    return ws_layout(*dims, max_tokens).total;
+}
+
+int32_t moe_decode_max_tokens(void) { return kDecodeMaxTokens; }
+
+strata_status moe_rmsnorm(const float* r_dev, int32_t T, int32_t H, float eps, void* x_dev,
+                          void* stream) {
+    if (T < 0 || H < 256 || H > 4096 || H % 256 != 0 || !(eps >= 0.0f)) return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(r_dev) || !al16(x_dev)) return STRATA_EINVAL;
+    return cuda_status(launch_rmsnorm(r_dev, T, H, eps, static_cast<uint16_t*>(x_dev),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+strata_status moe_route(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                        const void* x_dev, int32_t T, int32_t* ids_dev, float* weights_dev,
+                        float* shared_gate_dev, float* logits_dev, void* ws_dev,
+                        size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouter)) return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(x_dev) || !al4(ids_dev) || !al4(weights_dev) || !al4(shared_gate_dev) ||
+        !opt4(logits_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
+    const WsLayout W = ws_layout(*dims, T);
+    RouteLaunch r{};
+    r.router = static_cast<const uint16_t*>(layer->router_dev);
+    r.bias = layer->router_bias_dev;
+    r.x = static_cast<const uint16_t*>(x_dev);
+    r.logits = at<float>(ws_dev, W.logits);
+    r.do_shared = 0;
+    r.do_select = 1;
+    r.ids = at<int32_t>(ws_dev, W.ids);
+    r.w = at<float>(ws_dev, W.w);
+    r.sig = at<float>(ws_dev, W.sig);
+    r.ids_user = ids_dev;
+    r.w_user = weights_dev;
+    r.sig_user = shared_gate_dev;
+    r.logits_user = logits_dev;
+    r.do_permute = 0;
+    r.ctl = at<void>(ws_dev, W.ctl);
+    r.T = T;
+    r.H = dims->hidden;
+    r.E = dims->n_experts;
+    r.K = dims->top_k;
+    r.Is = dims->shared_inter;
+    return cuda_status(launch_route_decode(r, static_cast<cudaStream_t>(stream)));
+}
+
+strata_status moe_permute(const strata_moe_dims* dims, const int32_t* ids_dev, int32_t T,
+                          int32_t* counts_dev, int32_t* offsets_dev, int32_t* perm_dev,
+                          int32_t* inv_perm_dev, void* ws_dev, size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0) return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al4(ids_dev) || !al4(counts_dev) || !al4(offsets_dev) || !al4(perm_dev) ||
+        !al4(inv_perm_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
+    const WsLayout W = ws_layout(*dims, T);
+    return cuda_status(launch_permute_small(ids_dev, T, dims->top_k, dims->n_experts, counts_dev,
+                                            offsets_dev, perm_dev, inv_perm_dev,
+                                            &at<Ctl>(ws_dev, W.ctl)->err,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+strata_status moe_expert_gate_up(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                                 const void* x_dev, int32_t T, const int32_t* offsets_dev,
+                                 const int32_t* perm_dev, float* h_dev, void* ws_dev,
+                                 size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouted)) return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(x_dev) || !al4(offsets_dev) || !al4(perm_dev) || !al16(h_dev) ||
+        !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
+    const WsLayout W = ws_layout(*dims, T);
+    GuLaunch g{};
+    g.q = layer->gu_q_dev;
+    g.sc = layer->gu_s_dev;
+    g.x = static_cast<const uint16_t*>(x_dev);
+    g.offsets = offsets_dev;
+    g.perm = perm_dev;
+    g.h = h_dev;
+    g.err = &at<Ctl>(ws_dev, W.ctl)->err;
+    g.T = T;
+    g.H = dims->hidden;
+    g.I = dims->inter;
+    g.E = dims->n_experts;
+    g.K = dims->top_k;
+    g.shared = 0;
+    return cuda_status(launch_gate_up_decode(g, static_cast<cudaStream_t>(stream)));
+}
+
+strata_status moe_expert_down(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                              const float* h_dev, int32_t T, const int32_t* offsets_dev,
+                              void* y_dev, void* ws_dev, size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouted)) return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(h_dev) || !al4(offsets_dev) || !al16(y_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
+    const WsLayout W = ws_layout(*dims, T);
+    DownLaunch dn{};
+    dn.q = layer->dn_q_dev;
+    dn.sc = layer->dn_s_dev;
+    dn.h = h_dev;
+    dn.offsets = offsets_dev;
+    dn.y_out = static_cast<uint16_t*>(y_dev);
+    dn.err = &at<Ctl>(ws_dev, W.ctl)->err;
+    dn.T = T;
+    dn.H = dims->hidden;
+    dn.I = dims->inter;
+    dn.Is = dims->shared_inter;
+    dn.E = dims->n_experts;
+    dn.K = dims->top_k;
+    dn.mode = kDownSlots;
+    return cuda_status(launch_down_decode(dn, static_cast<cudaStream_t>(stream)));
+}
+
+strata_status moe_expert_ffn(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                             const void* x_dev, int32_t T, const int32_t* offsets_dev,
+                             const int32_t* perm_dev, void* y_dev, void* ws_dev,
+                             size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouted)) return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(x_dev) || !al4(offsets_dev) || !al4(perm_dev) || !al16(y_dev) ||
+        !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
+    const WsLayout W = ws_layout(*dims, T);
+    float* h = at<float>(ws_dev, W.h);
+    strata_status st = moe_expert_gate_up(dims, layer, x_dev, T, offsets_dev, perm_dev, h,
+                                          ws_dev, ws_bytes, stream);
+    if (st != STRATA_OK) return st;
+    return moe_expert_down(dims, layer, h, T, offsets_dev, y_dev, ws_dev, ws_bytes, stream);
+}
+
+strata_status moe_combine(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                          const void* x_dev, int32_t T, const void* y_dev,
+                          const int32_t* inv_perm_dev, const float* weights_dev,
+                          const float* shared_gate_dev, void* out_dev, void* ws_dev,
+                          size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kShared)) return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(x_dev) || !al16(y_dev) || !al4(inv_perm_dev) || !al4(weights_dev) ||
+        !al4(shared_gate_dev) || !al16(out_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
+    const WsLayout W = ws_layout(*dims, T);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GuLaunch g{};
+    g.q = layer->sh_gu_q_dev;
+    g.sc = layer->sh_gu_s_dev;
+    g.x = static_cast<const uint16_t*>(x_dev);
+    g.h = at<float>(ws_dev, W.hs);
+    g.err = &at<Ctl>(ws_dev, W.ctl)->err;
+    g.T = T;
+    g.H = dims->hidden;
+    g.I = dims->shared_inter;
+    g.E = 1;
+    g.K = 1;
+    g.shared = 1;
+    STRATA_TRY(launch_gate_up_decode(g, s));
+    DownLaunch dn{};
+    dn.shq = layer->sh_dn_q_dev;
+    dn.shs = layer->sh_dn_s_dev;
+    dn.hs = g.h;
+    dn.inv = inv_perm_dev;
+    dn.w = weights_dev;
+    dn.sig = shared_gate_dev;
+    dn.y_in = static_cast<const uint16_t*>(y_dev);
+    dn.out = static_cast<uint16_t*>(out_dev);
+    dn.err = g.err;
+    dn.T = T;
+    dn.H = dims->hidden;
+    dn.I = dims->inter;
+    dn.Is = dims->shared_inter;
+    dn.E = dims->n_experts;
+    dn.K = dims->top_k;
+    dn.mode = kDownCombine;
+    return cuda_status(launch_down_decode(dn, s));
+}
+
+strata_status moe_layer_forward(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                                const void* x_dev, int32_t T, int32_t* ids_dev,
+                                float* weights_dev, float* shared_gate_dev, void* out_dev,
+                                void* ws_dev, size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouter | kRouted | kShared))
+        return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(x_dev) || !opt4(ids_dev) || !opt4(weights_dev) || !opt4(shared_gate_dev) ||
+        !al16(out_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
+    return decode_layer(dims, layer, x_dev, T, nullptr, nullptr, ids_dev, weights_dev,
+                        shared_gate_dev, out_dev, nullptr, ws_dev,
+                        static_cast<cudaStream_t>(stream));
+}
+
+strata_status moe_layer_forward_routed(const strata_moe_dims* dims,
+                                       const strata_moe_layer* layer, const void* x_dev,
+                                       int32_t T, const int32_t* ids_dev,
+                                       const float* weights_dev, void* out_dev, void* ws_dev,
+                                       size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouter | kRouted | kShared))
+        return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(x_dev) || !al4(ids_dev) || !al4(weights_dev) || !al16(out_dev) ||
+        !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
+    return decode_layer(dims, layer, x_dev, T, ids_dev, weights_dev, nullptr, nullptr, nullptr,
+                        out_dev, nullptr, ws_dev, static_cast<cudaStream_t>(stream));
+}
+
+strata_status moe_block_forward(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                                float* resid_dev, int32_t T, float eps, const int32_t* ids_dev,
+                                const float* weights_dev, void* x_out_dev, void* out_dev,
+                                void* ws_dev, size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouter | kRouted | kShared) ||
+        !(eps >= 0.0f))
+        return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(resid_dev) || (ids_dev == nullptr) != (weights_dev == nullptr) ||
+        !opt4(ids_dev) || !opt4(weights_dev) ||
+        (x_out_dev && !al16(x_out_dev)) || (out_dev && !al16(out_dev)) ||
+        !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
+    const WsLayout W = ws_layout(*dims, T);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* x = x_out_dev ? x_out_dev : at<void>(ws_dev, W.x);
+    void* out = out_dev ? out_dev : at<void>(ws_dev, W.out);
+    STRATA_TRY(launch_rmsnorm(resid_dev, T, dims->hidden, eps, static_cast<uint16_t*>(x), s));
+    return decode_layer(dims, layer, x, T, ids_dev, weights_dev, nullptr, nullptr, nullptr, out,
+                        resid_dev, ws_dev, s);
+}
+
+strata_status moe_get_device_status(void* ws_dev, void* stream) {
+    if (ws_dev == nullptr || (reinterpret_cast<uintptr_t>(ws_dev) & 255u) != 0)
+        return STRATA_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    Ctl* ctl = static_cast<Ctl*>(ws_dev);
+    if (cudaMemcpyAsync(&word, &ctl->err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return STRATA_ECUDA;
+    if (cudaMemsetAsync(&ctl->err, 0, sizeof(uint32_t), s) != cudaSuccess) return STRATA_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return STRATA_ECUDA;
+    return static_cast<strata_status>(word);
+}
+
+const char* strata_status_str(strata_status s) {
+    switch (s) {
+        case STRATA_OK: return "STRATA_OK";
+        case STRATA_EINVAL: return "STRATA_EINVAL: invalid argument";
+        case STRATA_ECUDA: return "STRATA_ECUDA: CUDA launch or query failed";
+        case STRATA_EUNSUPPORTED: return "STRATA_EUNSUPPORTED: not handled by this build";
+        case STRATA_ETIMEOUT: return "STRATA_ETIMEOUT: a bounded device wait ran out";
+        case STRATA_EBADROUTE: return "STRATA_EBADROUTE: expert id out of range";
+    }
+    return "unknown strata_status";
+}
+
+}  // extern "C"

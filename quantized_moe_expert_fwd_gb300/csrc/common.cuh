@@ -1,0 +1,149 @@
+// common.cuh -- device helpers shared by the MoE kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace strata {
+
+constexpr int kWarp = 32;
+
+// Workspace control block (offset 0 of every workspace).
+struct Ctl {
+    uint32_t err;       // latched strata_status (first error wins)
+    uint32_t arrive;    // CTAs of k_route_decode that finished their rows
+    uint32_t pad[62];
+};
+
+__device__ __forceinline__ void latch(uint32_t* err, uint32_t code) {
+    atomicCAS(err, 0u, code);
+}
+
+// ------------------------------------------------------------------ formats
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float f16_to_f32(uint16_t h) {
+    float f;
+    asm("{ .reg .b16 t; mov.b16 t, %1; cvt.f32.f16 %0, t; }" : "=f"(f) : "h"(h));
+    return f;
+}
+
+// fp32 -> bf16 bits, round to nearest even (NaN kept quiet).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+    return r;
+}
+
+// ----------------------------------------------------- packed fp32 (f32x2)
+__device__ __forceinline__ uint64_t pk(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t pku(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 upk(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// ------------------------------------------------------ int4 dot products
+//
+// A 16-byte chunk holds 32 consecutive int4 weights of one row (one scale
+// group): byte b of word w holds element 8w+2b in bits 0..3 and 8w+2b+1 in
+// bits 4..7, offset-binary (weight = scale * (u - 8)).
+//
+// Each nibble u becomes the fp32 value 1 + u/128 without any conversion
+// instruction: OR-ing 0x80 into the byte and placing it under the exponent
+// byte 0x3F gives the bit pattern 0x3F80_0000 | u << 16.  With
+//   A = sum_j (1 + u_j/128) x_j   and   X = sum_j x_j
+// the group's integer dot product is
+//   sum_j (u_j - 8) x_j = 128 (A - X) - 8 X = 128 A - 136 X.
+// Every step is exact except the fp32 sums, whose rounding error relative to
+// the result stays near 1e-5 for |u| <= 15.
+__device__ __forceinline__ uint32_t place_byte(uint32_t bytes, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(bytes), "r"(0x3F000000u), "r"(sel));
+    return r;
+}
+
+// x2[16]: the chunk's 32 activations as pairs (x[2j], x[2j+1]).
+// Returns A = sum_j (1 + u_j/128) x_j.
+__device__ __forceinline__ float dot_chunk(const uint4& q, const uint64_t* x2) {
+    uint64_t acc0 = 0ull, acc1 = 0ull;
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t lo = (words[w] & 0x0F0F0F0Fu) | 0x80808080u;
+        const uint32_t hi = ((words[w] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t sel = 0x7044u | (uint32_t(b) << 8);
+            const uint64_t f = pku(place_byte(lo, sel), place_byte(hi, sel));
+            if (b & 1)
+                acc1 = ffma2(f, x2[4 * w + b], acc1);
+            else
+                acc0 = ffma2(f, x2[4 * w + b], acc0);
+        }
+    }
+    const float2 a0 = upk(acc0), a1 = upk(acc1);
+    return (a0.x + a0.y) + (a1.x + a1.y);
+}
+
+// Scaled group dot product: scale * sum_j (u_j - 8) x_j.
+__device__ __forceinline__ float group_dot(float A, float X, float scale) {
+    return scale * fmaf(128.0f, A, -136.0f * X);
+}
+
+// ------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Sum over aligned groups of `width` lanes (width a power of two <= 32).
+__device__ __forceinline__ float group_sum(float v, int width) {
+    for (int o = width >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return g / (1.0f + expf(-g)) * u;
+}
+
+// ------------------------------------------------------------ global loads
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {   // weights: read once
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint16_t ldg_u16(const uint16_t* p) {
+    uint16_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint4 ldg_keep(const void* p) {     // activations: reused
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ float4 ldcg_f4(const float* p) {    // written by an earlier kernel
+    return __ldcg(reinterpret_cast<const float4*>(p));
+}
+
+// --------------------------------------------- programmatic dependent launch
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+}  // namespace strata
