@@ -1,0 +1,568 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed MoE FFN forward on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl strata|reference]
+
+Workloads (synthetic, seeded; shapes of a Qwen3.6-35B-A3B MoE layer: H=2048,
+256 experts, top-8, I = Is = 512, int4 weights with one fp16 scale per 32
+inputs, bf16 activations):
+  decode1   (default) T=1 decode through 10 distinct layers (seeds 0..9); one
+            step = one token through each of the 10 layers, in order, as one
+            CUDA graph; 16 token variants per layer rotate between steps, so
+            the touched experts change and the 4.56 GB of weights defeat L2.
+  decode16  the same with T=16 (8 requests x 2 MTP tokens, cosine-0.9 pairs)
+            and a Zipf(1.1) router bias.
+  stack     one token (--tokens 1 or 4) through a 40-layer residual MoE stack
+            (moe_block_forward x 40, 18.2 GB resident) as one CUDA graph.
+
+Printed: one JSON line (rank 0).  value = tokens per second through one MoE
+layer (decode1/decode16: layer-tokens / s; stack: tokens / s through all 40
+layers).  The roofline object is for the dominant decode kernel, timed alone
+with CUDA events on its own stream; cpu_baseline is the C oracle on the host.
+--impl reference times that oracle itself on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import gen  # noqa: E402
+
+METRIC = "MoE decode tok/s & expert-weight HBM GB/s vs ~8 TB/s; prefill tok/s, TC util"
+EXPERT_BYTES = None          # filled per dims
+NOMINAL_HBM_GBS = 8000.0
+
+
+def expert_bytes(d) -> int:
+    H, I = d.hidden, d.inter
+    return 2 * I * H // 2 + 2 * I * (H // 32) * 2 + H * I // 2 + H * (I // 32) * 2
+
+
+def shared_bytes(d) -> int:
+    H, Is = d.hidden, d.shared_inter
+    return 2 * Is * H // 2 + 2 * Is * (H // 32) * 2 + H * Is // 2 + H * (Is // 32) * 2
+
+
+def router_bytes(d) -> int:
+    return (d.n_experts + 1) * d.hidden * 2
+
+
+def gu_bytes(d, I) -> int:
+    return 2 * I * d.hidden // 2 + 2 * I * (d.hidden // 32) * 2
+
+
+def dn_bytes(d, I) -> int:
+    return d.hidden * I // 2 + d.hidden * (I // 32) * 2
+
+
+# ------------------------------------------------------------- environment
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class Control:
+    """Host-side control plane of the replicas: barrier and max over ranks
+    (gloo; no data-path collective: every rank runs its own replica)."""
+
+    def __init__(self, world):
+        self.world = world
+        self.pg = None
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.dist = dist
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        if self.world == 1:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            self.dist.destroy_process_group()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "samples": 0}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unparsed"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = j.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "quantized_moe_expert_fwd_gb300", "csrc", ent["source"])
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return ent["bytes_per_launch"] if digest == ent["sha256"] else None
+
+
+# --------------------------------------------------------------- oracle leg
+def oracle_sample(dims, planes_list, xs, budget_s: float):
+    """Layer-tokens per second of the C oracle on the host cores: whole
+    layer-token forwards (one token through one layer) until budget_s has
+    passed (at least one)."""
+    import oracle
+    oracle.build()
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        li = n % len(planes_list)
+        oracle.moe_forward(dims, planes_list[li], xs[li])
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            break
+    return n / dt, n, dt
+
+
+# ------------------------------------------------------------ GPU workloads
+def build_decode(args, dev):
+    import torch
+    import quantized_moe_expert_fwd_gb300 as q
+    cfg = gen.CONFIGS["decode1" if args.workload == "decode1" else "decode16"]
+    dims = cfg.dims
+    T = cfg.tokens
+    nl = args.layers
+    planes, layers = [], []
+    for s in range(nl):
+        p = gen.draw_layer(dims, s, bias=cfg.bias, alpha=cfg.alpha)
+        layers.append(q.DeviceLayer(p, dev))
+        planes.append(p)
+    nvar = args.variants
+    xs = [[None] * nl for _ in range(nvar)]
+    xbufs = []
+    for v in range(nvar):
+        for li in range(nl):
+            r = gen.draw_tokens(dims, T, 1000 * v + li, cfg.token_kind)
+            rt = torch.from_numpy(r).to(dev)
+            x = torch.empty((T, dims.hidden), dtype=torch.int16, device=dev)
+            q.moe_rmsnorm(rt, x)
+            xs[v][li] = x
+    outs = [torch.empty((T, dims.hidden), dtype=torch.int16, device=dev) for _ in range(nl)]
+    return dims, T, planes, layers, xs, outs, cfg
+
+
+def run_strata(args, rank, world, local, ctl):
+    import torch
+    import quantized_moe_expert_fwd_gb300 as q
+    q.build.build()
+    q.load()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    dims, T, planes, layers, xs, outs, cfg = build_decode(args, dev)
+    nl = len(layers)
+    ws = q.make_workspace(dims, T, dev)
+    stream = torch.cuda.Stream(dev)
+    nvar = len(xs)
+
+    def step_calls(v):
+        for li in range(nl):
+            q.moe_layer_forward(dims, layers[li], xs[v][li], outs[li], ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for v in range(nvar):
+            step_calls(v)
+        stream.synchronize()
+        if q.moe_get_device_status(ws, stream) != q.STRATA_OK:
+            raise RuntimeError("device status after first pass")
+        graphs = []
+        for v in range(nvar):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step_calls(v)
+            graphs.append(g)
+        # clocks up and stable before the measured warm-up
+        t_end = time.time() + (0.0 if args.profile else 0.5)
+        i = 0
+        while time.time() < t_end:
+            graphs[i % nvar].replay()
+            i += 1
+            if i % 64 == 0:
+                stream.synchronize()
+        stream.synchronize()
+
+        clocks = ClockSampler(local)
+        clocks.start()
+        for i in range(args.warmup):
+            graphs[i % nvar].replay()
+        stream.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ctl.barrier()
+        torch.cuda.synchronize(dev)
+        clocks.mark_start()
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[(i + args.warmup) % nvar].replay()
+        ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize(dev)
+        clocks.mark_end()
+        ctl.barrier()
+        clocks.stop()
+        ms_total = ev0.elapsed_time(ev1)
+    ms_total = ctl.max(ms_total)
+    st = q.moe_get_device_status(ws, stream)
+    if st != q.STRATA_OK:
+        raise RuntimeError(f"device status {q.strata_status_str(st)}")
+
+    ms_step = ms_total / args.steps
+    layer_tokens = args.steps * nl * T * world
+    value = layer_tokens / (ms_total / 1e3)
+
+    if args.profile:
+        return {"profile": True, "ms_per_step": ms_step, "value": value}, None
+
+    # touched-expert bytes per layer-forward, from the routing of every variant
+    touched = 0
+    ids_buf = torch.empty((T, dims.top_k), dtype=torch.int32, device=dev)
+    for v in range(nvar):
+        for li in range(nl):
+            q.moe_layer_forward(dims, layers[li], xs[v][li], outs[li], ws, ids=ids_buf,
+                                stream=stream)
+            stream.synchronize()
+            touched += len(np.unique(ids_buf.cpu().numpy()))
+    mean_touched = touched / (nvar * nl)
+    layer_bytes = mean_touched * expert_bytes(dims) + shared_bytes(dims) + router_bytes(dims)
+    gbs = layer_bytes * nl / (ms_step / 1e3) / 1e9
+
+    # dominant decode kernel, timed alone: each stage over the 10 layers, with
+    # a workspace per layer so every call sees its own layer's plan
+    wss = [q.make_workspace(dims, T, dev) for _ in range(nl)]
+    v0 = 0
+    with torch.cuda.stream(stream):
+        for li in range(nl):
+            q.moe_decode_route(dims, layers[li], xs[v0][li], wss[li], stream=stream)
+            q.moe_decode_gate_up(dims, layers[li], xs[v0][li], wss[li], stream=stream)
+            q.moe_decode_down_combine(dims, layers[li], T, outs[li], wss[li], stream=stream)
+        stream.synchronize()
+        # touched experts of variant 0 per layer (for per-stage bytes)
+        n_act = []
+        for li in range(nl):
+            q.moe_layer_forward(dims, layers[li], xs[v0][li], outs[li], ws, ids=ids_buf,
+                                stream=stream)
+            stream.synchronize()
+            n_act.append(len(np.unique(ids_buf.cpu().numpy())))
+        stages = {
+            "k_route": (lambda li: q.moe_decode_route(dims, layers[li], xs[v0][li], wss[li],
+                                                      stream=stream),
+                        lambda li: router_bytes(dims) + gu_bytes(dims, dims.shared_inter)),
+            "k_gate_up": (lambda li: q.moe_decode_gate_up(dims, layers[li], xs[v0][li], wss[li],
+                                                          stream=stream),
+                          lambda li: n_act[li] * gu_bytes(dims, dims.inter)),
+            "k_down": (lambda li: q.moe_decode_down_combine(dims, layers[li], T, outs[li],
+                                                            wss[li], stream=stream),
+                       lambda li: n_act[li] * dn_bytes(dims, dims.inter)
+                       + dn_bytes(dims, dims.shared_inter)),
+        }
+        # each stage captured as one graph of reps x 10 launches, so host-side
+        # call overhead does not leak into the per-launch time
+        per_stage = {}
+        reps = 50
+        for name, (fn, nbytes) in stages.items():
+            for li in range(nl):
+                fn(li)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for r in range(reps):
+                    for li in range(nl):
+                        fn(li)
+            g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(4):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (4 * reps * nl)
+            per_stage[name] = (us, sum(nbytes(li) for li in range(nl)) / nl)
+    dom = max(per_stage, key=lambda k: per_stage[k][0])
+    dom_us, dom_bytes = per_stage[dom]
+    hbm_peak, _, peak_src = measured_peaks()
+    achieved = dom_bytes / (dom_us / 1e6) / 1e9
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = [torch.empty((T, dims.hidden), dtype=torch.int16).pin_memory() for _ in range(nl)]
+        oh = [torch.empty((T, dims.hidden), dtype=torch.int16).pin_memory() for _ in range(nl)]
+        xd = [torch.empty((T, dims.hidden), dtype=torch.int16, device=dev) for _ in range(nl)]
+        for li in range(nl):
+            xh[li].copy_(xs[0][li].cpu())
+        k_e2e = max(10, min(args.steps, 500))
+        with torch.cuda.stream(stream):
+            for it in range(3 + k_e2e):
+                if it == 3:
+                    stream.synchronize()
+                    ctl.barrier()
+                    t0 = time.perf_counter()
+                for li in range(nl):
+                    xd[li].copy_(xh[li], non_blocking=True)
+                for li in range(nl):
+                    q.moe_layer_forward(dims, layers[li], xd[li], outs[li], ws, stream=stream)
+                for li in range(nl):
+                    oh[li].copy_(outs[li], non_blocking=True)
+                stream.synchronize()
+            dt = time.perf_counter() - t0
+        dt = ctl.max(dt)
+        e2e = {"value": k_e2e * nl * T * world / dt, "unit": "tok/s",
+               "h2d_bytes_per_step": nl * T * dims.hidden * 2,
+               "d2h_bytes_per_step": nl * T * dims.hidden * 2}
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded random int4 weights and activations of the real shapes)",
+        "config": {
+            "workload": cfg.description,
+            "tokens_per_call": T,
+            "layers_per_step": nl,
+            "value_unit": "layer-tokens per second (one token through one MoE layer)",
+            "l2": f"inputs larger than L2: {nl} layers x 455.8 MB resident, "
+                  f"{len(xs)} token variants per layer rotating between steps",
+            "arithmetic": "int4 weights x bf16 activations, fp32 accumulate",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "expert_weight_gbs": gbs,
+        "expert_weight_frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+        "touched_experts_per_layer": mean_touched,
+        "roofline": {
+            "kernel": dom,
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": hbm_peak,
+            "unit": "GB/s",
+            "frac": achieved / hbm_peak,
+            "peak_source": f"{peak_src} (burst copy, kernel timed alone)",
+            "traffic": kernel_traffic(dom),
+            "us_per_launch": dom_us,
+            "algorithmic_bytes_per_launch": dom_bytes,
+            "stages_us": {k: round(v[0], 3) for k, v in per_stage.items()},
+        },
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "gpu_launches": args.steps * nl * 3,
+    }
+    return result, (dims, planes, xs, nl)
+
+
+def cpu_baseline_block(dims, planes, xs_dev, nl, budget):
+    import torch
+    xs = [xs_dev[0][li].cpu().numpy().view(np.uint16) for li in range(nl)]
+    v, n, dt = oracle_sample(dims, planes, xs, budget)
+    return {"value": v, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} layer-token forwards (T=1, layers cycling over seeds 0..9) "
+                      f"in {dt:.1f} s, OpenMP over experts"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle, as it stands, on the host cores: each step one
+    layer-token forward of the same workload."""
+    import oracle
+    oracle.build()
+    cfg = gen.CONFIGS["decode1" if args.workload == "decode1" else "decode16"]
+    dims = cfg.dims
+    nl = 10
+    planes = [gen.draw_layer(dims, s, bias=cfg.bias, alpha=cfg.alpha) for s in range(nl)]
+    xs = [oracle.rmsnorm(gen.draw_tokens(dims, cfg.tokens, li, cfg.token_kind))
+          for li in range(nl)]
+    # size the steps so the whole run stays within a few minutes
+    t0 = time.perf_counter()
+    oracle.moe_forward(dims, planes[0], xs[0])
+    t_step = time.perf_counter() - t0
+    budget = 150.0
+    k = args.steps
+    if (args.steps + args.warmup) * t_step > budget:
+        k = max(3, int(budget / t_step) - args.warmup)
+    for i in range(args.warmup):
+        oracle.moe_forward(dims, planes[i % nl], xs[i % nl])
+    t0 = time.perf_counter()
+    for i in range(k):
+        oracle.moe_forward(dims, planes[i % nl], xs[i % nl])
+    dt = time.perf_counter() - t0
+    value = k * cfg.tokens / dt
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": k,
+        "steps_requested": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt / k * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded random int4 weights and activations of the real shapes)",
+        "config": {"workload": cfg.description, "tokens_per_call": cfg.tokens,
+                   "value_unit": "layer-tokens per second (one token through one MoE layer)"},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{k} layer-token forwards of the C oracle (fp32, "
+                                   f"OpenMP over experts) in {dt:.1f} s"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["strata", "reference"], default="strata")
+    ap.add_argument("--workload", choices=["decode1", "decode16"], default="decode1")
+    ap.add_argument("--variants", type=int, default=16)
+    ap.add_argument("--layers", type=int, default=10)
+    ap.add_argument("--profile", action="store_true",
+                    help="lean run for ncu: no clock warm loop, stage timing, e2e or oracle")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    ctl = Control(world)
+    try:
+        result, extra = run_strata(args, rank, world, local, ctl)
+        if extra is None:
+            if rank == 0:
+                print(json.dumps(result), flush=True)
+            return
+        dims, planes, xs, nl = extra
+        if rank == 0:
+            if world == 1 and args.cpu_budget > 0:
+                result["cpu_baseline"] = cpu_baseline_block(dims, planes, xs, nl,
+                                                            args.cpu_budget)
+            else:
+                result["cpu_baseline"] = None
+            print(json.dumps(result), flush=True)
+    finally:
+        ctl.close()
+
+
+if __name__ == "__main__":
+    main()

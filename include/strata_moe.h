@@ -182,9 +182,9 @@ STRATA_API strata_status moe_combine(const strata_moe_dims* dims, const strata_m
                           size_t ws_bytes, void* stream);
 
 /* The whole layer: route, permute, experts, shared expert, combine.  For
- * T <= moe_decode_max_tokens() it runs three fused decode kernels (router +
- * shared gate/up + selection + permutation in one; routed gate/up in one;
- * every down product + combine in one); above, the tcgen05 prefill kernels.
+ * T <= moe_decode_max_tokens() it runs three decode kernels (router + shared
+ * gate/up in one; selection, bucketing and routed gate/up in one; every down
+ * product + combine in one); above, the tcgen05 prefill kernels.
  * ids_dev / weights_dev / shared_gate_dev receive the routing when non-NULL.
  * out_dev bf16 [T][H]. */
 STRATA_API strata_status moe_layer_forward(const strata_moe_dims* dims, const strata_moe_layer* layer,
@@ -209,6 +209,38 @@ STRATA_API strata_status moe_block_forward(const strata_moe_dims* dims, const st
                                 float* resid_dev, int32_t T, float eps, const int32_t* ids_dev,
                                 const float* weights_dev, void* x_out_dev, void* out_dev,
                                 void* ws_dev, size_t ws_bytes, void* stream);
+
+/* The three kernels of the decode path (T <= moe_decode_max_tokens()), as
+ * separate calls; moe_layer_forward is the three in a row.  They pass their
+ * state through the workspace (logits, the shared expert's SwiGLU vectors,
+ * the routing, the bucketing and a plan of the touched experts, the routed
+ * SwiGLU vectors), so they take the same workspace and T, in this order.
+ *   moe_decode_route        the router product (all E+1 rows, or with
+ *                           forced != 0 only the shared-gate row) and the
+ *                           shared expert's gate/up + SwiGLU, one kernel.
+ *   moe_decode_gate_up      top-K, softmax and sigmoid gate of every token
+ *                           (or the forced ids/weights: both NULL or both
+ *                           given), the bucketing, then every touched
+ *                           expert's gate/up + SwiGLU, one kernel.
+ *                           ids_dev / weights_dev / shared_gate_dev: optional
+ *                           copies of the routing.
+ *   moe_decode_down_combine every touched expert's down product, the shared
+ *                           expert's, and the weighted combine into out_dev
+ *                           (bf16 [T][H]); resid_dev (fp32 [T][H], optional)
+ *                           gets += the bf16 output. */
+STRATA_API strata_status moe_decode_route(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                                          const void* x_dev, int32_t T, int32_t forced,
+                                          void* ws_dev, size_t ws_bytes, void* stream);
+STRATA_API strata_status moe_decode_gate_up(const strata_moe_dims* dims,
+                                            const strata_moe_layer* layer, const void* x_dev,
+                                            int32_t T, const int32_t* forced_ids_dev,
+                                            const float* forced_weights_dev, int32_t* ids_dev,
+                                            float* weights_dev, float* shared_gate_dev,
+                                            void* ws_dev, size_t ws_bytes, void* stream);
+STRATA_API strata_status moe_decode_down_combine(const strata_moe_dims* dims,
+                                                 const strata_moe_layer* layer, int32_t T,
+                                                 void* out_dev, float* resid_dev, void* ws_dev,
+                                                 size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, returns the status latched in the workspace's error
  * word (STRATA_OK when none) and clears the word.  For tests and debugging;

@@ -29,11 +29,11 @@ WsLayout ws_layout(const strata_moe_dims& d, int T) {
     L.offsets = take((E + 1) * 4);
     L.perm = take(t * K * 4);
     L.inv = take(t * K * 4);
+    L.plan = take((kPlanHeader + 3 * E + t * K) * 4);
     L.h = take(t * K * I * 4);
     L.hs = take(t * Is * 4);
     L.x = take(t * H * 2);
     L.out = take(t * H * 2);
-    L.tiles = L.xf16 = L.hf16 = L.y = L.shy = 0;
     L.total = o;
     return L;
 }
@@ -107,11 +107,12 @@ strata_status cuda_status(cudaError_t e) { return e == cudaSuccess ? STRATA_OK :
         if (_e != cudaSuccess) return STRATA_ECUDA;        \
     } while (0)
 
-// One layer on the decode kernels.  forced_ids/forced_w: NULL to route.
-strata_status decode_layer(const strata_moe_dims* d, const strata_moe_layer* L, const void* x,
-                           int T, const int32_t* forced_ids, const float* forced_w,
-                           int32_t* ids_user, float* w_user, float* sig_user, void* out,
-                           float* resid, void* ws, cudaStream_t s) {
+// The three decode stages.  Stage 1 computes the logits and the shared
+// expert's SwiGLU vectors; stage 2 routes (or takes forced ids), buckets,
+// publishes the routing and the plan, and runs the routed gate/up; stage 3
+// the down products and the combine.
+strata_status stage_route(const strata_moe_dims* d, const strata_moe_layer* L, const void* x,
+                          int T, bool forced, void* ws, cudaStream_t s) {
     const WsLayout W = ws_layout(*d, T);
     RouteLaunch r{};
     r.router = static_cast<const uint16_t*>(L->router_dev);
@@ -123,34 +124,37 @@ strata_status decode_layer(const strata_moe_dims* d, const strata_moe_layer* L, 
     r.hs = at<float>(ws, W.hs);
     r.Is = d->shared_inter;
     r.do_shared = 1;
-    r.do_select = forced_ids == nullptr ? 1 : 0;
-    r.ids = at<int32_t>(ws, W.ids);
-    r.w = at<float>(ws, W.w);
-    r.sig = at<float>(ws, W.sig);
-    r.ids_user = ids_user;
-    r.w_user = w_user;
-    r.sig_user = sig_user;
-    r.logits_user = nullptr;
-    r.ids_in = forced_ids;
-    r.w_in = forced_w;
-    r.do_permute = 1;
-    r.counts = at<int32_t>(ws, W.counts);
-    r.offsets = at<int32_t>(ws, W.offsets);
-    r.perm = at<int32_t>(ws, W.perm);
-    r.inv = at<int32_t>(ws, W.inv);
-    r.ctl = at<void>(ws, W.ctl);
+    r.do_select = forced ? 0 : 1;
     r.T = T;
     r.H = d->hidden;
     r.E = d->n_experts;
     r.K = d->top_k;
-    STRATA_TRY(launch_route_decode(r, s));
+    return cuda_status(launch_route_decode(r, s));
+}
 
+strata_status stage_gate_up(const strata_moe_dims* d, const strata_moe_layer* L, const void* x,
+                            int T, const int32_t* forced_ids, const float* forced_w,
+                            int32_t* ids_user, float* w_user, float* sig_user, void* ws,
+                            cudaStream_t s) {
+    const WsLayout W = ws_layout(*d, T);
     GuLaunch g{};
     g.q = L->gu_q_dev;
     g.sc = L->gu_s_dev;
-    g.x = r.x;
-    g.offsets = r.offsets;
-    g.perm = r.perm;
+    g.x = static_cast<const uint16_t*>(x);
+    g.logits = at<float>(ws, W.logits);
+    g.forced_ids = forced_ids;
+    g.forced_w = forced_w;
+    g.ids = at<int32_t>(ws, W.ids);
+    g.w = at<float>(ws, W.w);
+    g.sig = at<float>(ws, W.sig);
+    g.ids_user = ids_user;
+    g.w_user = w_user;
+    g.sig_user = sig_user;
+    g.counts = at<int32_t>(ws, W.counts);
+    g.offsets = at<int32_t>(ws, W.offsets);
+    g.perm = at<int32_t>(ws, W.perm);
+    g.inv = at<int32_t>(ws, W.inv);
+    g.plan_out = at<int32_t>(ws, W.plan);
     g.h = at<float>(ws, W.h);
     g.err = &at<Ctl>(ws, W.ctl)->err;
     g.T = T;
@@ -158,23 +162,27 @@ strata_status decode_layer(const strata_moe_dims* d, const strata_moe_layer* L, 
     g.I = d->inter;
     g.E = d->n_experts;
     g.K = d->top_k;
-    g.shared = 0;
-    STRATA_TRY(launch_gate_up_decode(g, s));
+    g.mode = kGuRoute;
+    return cuda_status(launch_gate_up_decode(g, s));
+}
 
+strata_status stage_down(const strata_moe_dims* d, const strata_moe_layer* L, int T, void* out,
+                         float* resid, void* ws, cudaStream_t s) {
+    const WsLayout W = ws_layout(*d, T);
     DownLaunch dn{};
     dn.q = L->dn_q_dev;
     dn.sc = L->dn_s_dev;
     dn.shq = L->sh_dn_q_dev;
     dn.shs = L->sh_dn_s_dev;
-    dn.h = g.h;
-    dn.hs = r.hs;
-    dn.offsets = r.offsets;
-    dn.inv = r.inv;
-    dn.w = r.w;
-    dn.sig = r.sig;
+    dn.h = at<float>(ws, W.h);
+    dn.hs = at<float>(ws, W.hs);
+    dn.plan = at<int32_t>(ws, W.plan);
+    dn.inv = at<int32_t>(ws, W.inv);
+    dn.w = at<float>(ws, W.w);
+    dn.sig = at<float>(ws, W.sig);
     dn.out = static_cast<uint16_t*>(out);
     dn.resid = resid;
-    dn.err = g.err;
+    dn.err = &at<Ctl>(ws, W.ctl)->err;
     dn.T = T;
     dn.H = d->hidden;
     dn.I = d->inter;
@@ -182,8 +190,19 @@ strata_status decode_layer(const strata_moe_dims* d, const strata_moe_layer* L, 
     dn.E = d->n_experts;
     dn.K = d->top_k;
     dn.mode = kDownFused;
-    STRATA_TRY(launch_down_decode(dn, s));
-    return STRATA_OK;
+    return cuda_status(launch_down_decode(dn, s));
+}
+
+// One layer on the decode kernels.  forced_ids/forced_w: NULL to route.
+strata_status decode_layer(const strata_moe_dims* d, const strata_moe_layer* L, const void* x,
+                           int T, const int32_t* forced_ids, const float* forced_w,
+                           int32_t* ids_user, float* w_user, float* sig_user, void* out,
+                           float* resid, void* ws, cudaStream_t s) {
+    strata_status st = stage_route(d, L, x, T, forced_ids != nullptr, ws, s);
+    if (st != STRATA_OK) return st;
+    st = stage_gate_up(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, ws, s);
+    if (st != STRATA_OK) return st;
+    return stage_down(d, L, T, out, resid, ws, s);
 }
 
 }  // namespace
@@ -217,6 +236,7 @@ strata_status moe_route(const strata_moe_dims* dims, const strata_moe_layer* lay
         return STRATA_EINVAL;
     if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
     const WsLayout W = ws_layout(*dims, T);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     RouteLaunch r{};
     r.router = static_cast<const uint16_t*>(layer->router_dev);
     r.bias = layer->router_bias_dev;
@@ -224,21 +244,23 @@ strata_status moe_route(const strata_moe_dims* dims, const strata_moe_layer* lay
     r.logits = at<float>(ws_dev, W.logits);
     r.do_shared = 0;
     r.do_select = 1;
-    r.ids = at<int32_t>(ws_dev, W.ids);
-    r.w = at<float>(ws_dev, W.w);
-    r.sig = at<float>(ws_dev, W.sig);
-    r.ids_user = ids_dev;
-    r.w_user = weights_dev;
-    r.sig_user = shared_gate_dev;
-    r.logits_user = logits_dev;
-    r.do_permute = 0;
-    r.ctl = at<void>(ws_dev, W.ctl);
     r.T = T;
     r.H = dims->hidden;
     r.E = dims->n_experts;
     r.K = dims->top_k;
     r.Is = dims->shared_inter;
-    return cuda_status(launch_route_decode(r, static_cast<cudaStream_t>(stream)));
+    STRATA_TRY(launch_route_decode(r, s));
+    SelectLaunch sl{};
+    sl.logits = r.logits;
+    sl.ids = ids_dev;
+    sl.w = weights_dev;
+    sl.sig = shared_gate_dev;
+    sl.logits_out = logits_dev;
+    sl.err = &at<Ctl>(ws_dev, W.ctl)->err;
+    sl.T = T;
+    sl.E = dims->n_experts;
+    sl.K = dims->top_k;
+    return cuda_status(launch_select(sl, s));
 }
 
 strata_status moe_permute(const strata_moe_dims* dims, const int32_t* ids_dev, int32_t T,
@@ -268,12 +290,15 @@ strata_status moe_expert_gate_up(const strata_moe_dims* dims, const strata_moe_l
         return STRATA_EINVAL;
     if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
     const WsLayout W = ws_layout(*dims, T);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* plan = at<int32_t>(ws_dev, W.plan);
+    STRATA_TRY(launch_plan(offsets_dev, perm_dev, T, dims->top_k, dims->n_experts, plan,
+                           &at<Ctl>(ws_dev, W.ctl)->err, s));
     GuLaunch g{};
     g.q = layer->gu_q_dev;
     g.sc = layer->gu_s_dev;
     g.x = static_cast<const uint16_t*>(x_dev);
-    g.offsets = offsets_dev;
-    g.perm = perm_dev;
+    g.plan = plan;
     g.h = h_dev;
     g.err = &at<Ctl>(ws_dev, W.ctl)->err;
     g.T = T;
@@ -281,8 +306,8 @@ strata_status moe_expert_gate_up(const strata_moe_dims* dims, const strata_moe_l
     g.I = dims->inter;
     g.E = dims->n_experts;
     g.K = dims->top_k;
-    g.shared = 0;
-    return cuda_status(launch_gate_up_decode(g, static_cast<cudaStream_t>(stream)));
+    g.mode = kGuPlan;
+    return cuda_status(launch_gate_up_decode(g, s));
 }
 
 strata_status moe_expert_down(const strata_moe_dims* dims, const strata_moe_layer* layer,
@@ -294,11 +319,15 @@ strata_status moe_expert_down(const strata_moe_dims* dims, const strata_moe_laye
         return STRATA_EINVAL;
     if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
     const WsLayout W = ws_layout(*dims, T);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* plan = at<int32_t>(ws_dev, W.plan);
+    STRATA_TRY(launch_plan(offsets_dev, nullptr, T, dims->top_k, dims->n_experts, plan,
+                           &at<Ctl>(ws_dev, W.ctl)->err, s));
     DownLaunch dn{};
     dn.q = layer->dn_q_dev;
     dn.sc = layer->dn_s_dev;
     dn.h = h_dev;
-    dn.offsets = offsets_dev;
+    dn.plan = plan;
     dn.y_out = static_cast<uint16_t*>(y_dev);
     dn.err = &at<Ctl>(ws_dev, W.ctl)->err;
     dn.T = T;
@@ -308,7 +337,7 @@ strata_status moe_expert_down(const strata_moe_dims* dims, const strata_moe_laye
     dn.E = dims->n_experts;
     dn.K = dims->top_k;
     dn.mode = kDownSlots;
-    return cuda_status(launch_down_decode(dn, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_down_decode(dn, s));
 }
 
 strata_status moe_expert_ffn(const strata_moe_dims* dims, const strata_moe_layer* layer,
@@ -353,7 +382,7 @@ strata_status moe_combine(const strata_moe_dims* dims, const strata_moe_layer* l
     g.I = dims->shared_inter;
     g.E = 1;
     g.K = 1;
-    g.shared = 1;
+    g.mode = kGuShared;
     STRATA_TRY(launch_gate_up_decode(g, s));
     DownLaunch dn{};
     dn.shq = layer->sh_dn_q_dev;
@@ -428,6 +457,45 @@ strata_status moe_block_forward(const strata_moe_dims* dims, const strata_moe_la
     STRATA_TRY(launch_rmsnorm(resid_dev, T, dims->hidden, eps, static_cast<uint16_t*>(x), s));
     return decode_layer(dims, layer, x, T, ids_dev, weights_dev, nullptr, nullptr, nullptr, out,
                         resid_dev, ws_dev, s);
+}
+
+strata_status moe_decode_route(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                               const void* x_dev, int32_t T, int32_t forced, void* ws_dev,
+                               size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouter | kShared)) return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (T > kDecodeMaxTokens || !al16(x_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    return stage_route(dims, layer, x_dev, T, forced != 0, ws_dev,
+                       static_cast<cudaStream_t>(stream));
+}
+
+strata_status moe_decode_gate_up(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                                 const void* x_dev, int32_t T, const int32_t* forced_ids_dev,
+                                 const float* forced_weights_dev, int32_t* ids_dev,
+                                 float* weights_dev, float* shared_gate_dev, void* ws_dev,
+                                 size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouted)) return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (T > kDecodeMaxTokens || !al16(x_dev) ||
+        (forced_ids_dev == nullptr) != (forced_weights_dev == nullptr) ||
+        !opt4(forced_ids_dev) || !opt4(forced_weights_dev) || !opt4(ids_dev) ||
+        !opt4(weights_dev) || !opt4(shared_gate_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    return stage_gate_up(dims, layer, x_dev, T, forced_ids_dev, forced_weights_dev, ids_dev,
+                         weights_dev, shared_gate_dev, ws_dev, static_cast<cudaStream_t>(stream));
+}
+
+strata_status moe_decode_down_combine(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                                      int32_t T, void* out_dev, float* resid_dev, void* ws_dev,
+                                      size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouted | kShared)) return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (T > kDecodeMaxTokens || !al16(out_dev) || (resid_dev && !al16(resid_dev)) ||
+        !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    return stage_down(dims, layer, T, out_dev, resid_dev, ws_dev,
+                      static_cast<cudaStream_t>(stream));
 }
 
 strata_status moe_get_device_status(void* ws_dev, void* stream) {

@@ -11,12 +11,28 @@ constexpr int kWarp = 32;
 // Workspace control block (offset 0 of every workspace).
 struct Ctl {
     uint32_t err;       // latched strata_status (first error wins)
-    uint32_t arrive;    // CTAs of k_route_decode that finished their rows
-    uint32_t pad[62];
+    uint32_t where[7];  // first timed-out wait: site, block, warp, slot, round, item, 1
+    uint32_t pad[56];
 };
 
 __device__ __forceinline__ void latch(uint32_t* err, uint32_t code) {
     atomicCAS(err, 0u, code);
+}
+
+// A bounded wait ran out: latch STRATA_ETIMEOUT and record where (the first
+// one only).  `err` points at Ctl::err.
+__device__ __forceinline__ void latch_timeout(uint32_t* err, uint32_t site, uint32_t slot,
+                                              uint32_t round, uint32_t item) {
+    atomicCAS(err, 0u, 4u /* STRATA_ETIMEOUT */);
+    uint32_t* w = err + 1;
+    if (atomicCAS(&w[6], 0u, 1u) == 0u) {
+        w[0] = site;
+        w[1] = blockIdx.x;
+        w[2] = threadIdx.x >> 5;
+        w[3] = slot;
+        w[4] = round;
+        w[5] = item;
+    }
 }
 
 // ------------------------------------------------------------------ formats
@@ -145,5 +161,58 @@ __device__ __forceinline__ float4 ldcg_f4(const float* p) {    // written by an 
 // --------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+}  // namespace strata
+
+namespace strata {
+
+// ------------------------------------------------- mbarrier + bulk copies
+// One-dimensional bulk copies (global -> this CTA's shared memory) complete
+// on an mbarrier's transaction count.  Every wait is bounded: a wait that
+// runs out returns false and the caller latches STRATA_ETIMEOUT.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// dst, src 16-byte aligned; bytes a multiple of 16
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
 
 }  // namespace strata

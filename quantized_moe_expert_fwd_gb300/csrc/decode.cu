@@ -7,23 +7,29 @@
 // "Models and backends", section "What was tuned": a call's experts go
 // through one launch per stage, and one launch adds them up):
 //
-//   k_route_decode  router rows (E+1 of them: the last is the shared-expert
-//                   gate) and the shared expert's gate/up rows, spread over
-//                   every SM; the last CTA to finish selects the top-K of
-//                   each token, computes the renormalised softmax weights and
-//                   the sigmoid gate, and buckets the (token, k) pairs by
-//                   expert.
-//   k_gate_up       every touched expert's gate/up rows, each read once for
-//                   all tokens routed to it, with SwiGLU in the epilogue.
-//   k_down          for a block of output rows: every touched expert's down
-//                   rows and the shared expert's, then the weighted combine
-//                   (or, as separate calls, per-slot outputs / the combine of
-//                   given per-slot outputs).
+//   k_route    router rows (E+1 of them: the last is the shared-expert gate)
+//              and the shared expert's gate/up rows, spread over every SM:
+//              logits and the shared SwiGLU vectors.
+//   k_gate_up  every CTA first selects each token's top-K from the logits,
+//              computes the renormalised softmax weights and the sigmoid gate
+//              and buckets the (token, k) pairs by expert -- the same result
+//              in every CTA, so no CTA waits for another; CTA 0 publishes it.
+//              Then every touched expert's gate/up rows, each read once for
+//              all tokens routed to it, SwiGLU in the epilogue.
+//   k_down     for a block of output rows: every touched expert's down rows
+//              and the shared expert's, then the weighted combine (or, as
+//              separate calls, per-slot outputs / the combine of given
+//              per-slot outputs).
 //
-// Weights stream through 128-bit non-allocating loads, each 16-byte chunk
-// being one scale group of 32 int4 weights; dequantisation is the byte
-// placement of common.cuh (no conversion instructions) and packed f32x2 FMAs.
-// Every sum has a fixed order: results do not depend on timing.
+// k_gate_up and k_down stream weights through shared-memory rings: one
+// producer thread issues 1-D bulk copies (cp.async.bulk) that complete on
+// mbarriers, consumer warps compute from shared memory and release the
+// stage.  All three kernels chain with programmatic dependent launch: each
+// triggers its dependents at once and touches nothing the previous kernel
+// writes before griddepcontrol.wait; weights that do not depend on routing
+// (router rows, shared-expert rows) are requested before that wait.
+// int4 weights become fp32 by byte placement (common.cuh); every sum has a
+// fixed order, so results do not depend on timing.
 
 #include <math.h>
 
@@ -32,62 +38,237 @@
 
 namespace strata {
 
-// ---------------------------------------------------------------- experts
-// The touched experts, ascending, with their slot ranges.  Every CTA of the
-// expert kernels builds it from `offsets`, so those kernels accept a
-// bucketing from any source.
-struct ActiveList {
+// ------------------------------------------------------------------- plan
+// A layer's plan: the touched experts in ascending id, their slot ranges,
+// and the token of each slot (-1: none).
+struct SPlan {
     int n;
     int e[kMaxExperts];
     int off[kMaxExperts];
     int cnt[kMaxExperts];
+    int tok[kDecodeMaxTokens * kMaxTopK];
 };
 
-__device__ void build_active(ActiveList& A, const int32_t* offsets, int E, int TK,
-                             uint32_t* err) {
-    __shared__ int warp_base[32];
-    __shared__ int running;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
-    if (tid == 0) running = 0;
-    __syncthreads();
-    for (int base = 0; base < E; base += blockDim.x) {
-        const int e = base + tid;
-        int off = 0, cnt = 0;
-        if (e < E) {
-            off = __ldcg(offsets + e);
-            const int end = __ldcg(offsets + e + 1);
-            cnt = end - off;
-            if (off < 0 || cnt < 0 || end > TK) {
-                latch(err, STRATA_EBADROUTE);
-                cnt = 0;
-            }
-        }
-        const unsigned bal = __ballot_sync(0xffffffffu, cnt > 0);
-        const int pre = __popc(bal & ((1u << lane) - 1u));
-        if (lane == 0) warp_base[wid] = __popc(bal);
-        __syncthreads();
-        if (tid == 0) {
-            int r = running;
-            for (int w = 0; w < nw; ++w) {
-                const int c = warp_base[w];
-                warp_base[w] = r;
-                r += c;
-            }
-            running = r;
-        }
-        __syncthreads();
-        if (cnt > 0) {
-            const int pos = warp_base[wid] + pre;
-            A.e[pos] = e;
-            A.off[pos] = off;
-            A.cnt[pos] = cnt;
-        }
-        __syncthreads();
+__device__ void load_plan(SPlan& P, const int32_t* plan, int E, int TK) {
+    const int* base = plan + kPlanHeader;
+    for (int i = threadIdx.x; i < 3 * E + TK; i += blockDim.x) {
+        const int v = __ldcg(base + i);
+        if (i < E)
+            P.e[i] = v;
+        else if (i < 2 * E)
+            P.off[i - E] = v;
+        else if (i < 3 * E)
+            P.cnt[i - 2 * E] = v;
+        else
+            P.tok[i - 3 * E] = v;
     }
-    if (tid == 0) A.n = running;
+    if (threadIdx.x == 0) P.n = __ldcg(plan);
     __syncthreads();
 }
 
+__device__ void shared_plan(SPlan& P, int T) {
+    for (int s = threadIdx.x; s < T; s += blockDim.x) P.tok[s] = s;
+    if (threadIdx.x == 0) {
+        P.n = 1;
+        P.e[0] = 0;
+        P.off[0] = 0;
+        P.cnt[0] = T;
+    }
+    __syncthreads();
+}
+
+// Where a bucketing is published (any pointer may be null).
+struct BucketOut {
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm;
+    int32_t* inv;
+    int32_t* plan;
+};
+
+// Stable counting sort of the T*K (token, k) pairs by expert, by one CTA.
+// s_ids: the pairs' expert ids; an out-of-range id gets no slot (inv -1).
+// Fills P and s_inv in shared memory and, when given, the global copies:
+// counts[e], offsets[0..E], perm[slot] = t*K + k (slots of one expert in
+// ascending t), inv[t*K + k] = slot, and the plan.
+__device__ void bucket_cta(const int* s_ids, int T, int K, int E, int* s_cnt, int* s_off,
+                           int* s_wsum, SPlan& P, int* s_inv, const BucketOut& g) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, wpb = blockDim.x >> 5;
+    const int TK = T * K;
+    for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+    for (int p = tid; p < TK; p += blockDim.x) s_inv[p] = -1;
+    __syncthreads();
+    for (int p = tid; p < TK; p += blockDim.x) {
+        const int e = s_ids[p];
+        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    }
+    __syncthreads();
+    // exclusive scan over experts of (slots, touched experts), packed in one
+    // int (slots < 2^16, experts < 2^15); each thread one contiguous segment
+    const int seg = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, tid * seg), e1 = min(E, e0 + seg);
+    int local = 0, nz = 0;
+    for (int e = e0; e < e1; ++e) {
+        local += s_cnt[e];
+        nz += s_cnt[e] > 0 ? 1 : 0;
+    }
+    const int mine = local | (nz << 16);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wsum[wid] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        int r = 0;
+        for (int w = 0; w < wpb; ++w) {
+            const int c = s_wsum[w];
+            s_wsum[w] = r;
+            r += c;
+        }
+        s_off[E] = r & 0xffff;
+        P.n = r >> 16;
+    }
+    __syncthreads();
+    const int excl = s_wsum[wid] + incl - mine;
+    int run = excl & 0xffff, rank = excl >> 16;
+    for (int e = e0; e < e1; ++e) {
+        s_off[e] = run;
+        if (s_cnt[e] > 0) {
+            P.e[rank] = e;
+            P.off[rank] = run;
+            P.cnt[rank] = s_cnt[e];
+            ++rank;
+        }
+        run += s_cnt[e];
+    }
+    __syncthreads();
+    for (int s = s_off[E] + tid; s < TK; s += blockDim.x) P.tok[s] = -1;
+    for (int e = tid; e < E; e += blockDim.x) {
+        const int c = s_cnt[e];
+        if (g.counts) g.counts[e] = c;
+        if (g.offsets) g.offsets[e] = s_off[e];
+        if (c == 0) continue;
+        int slot = s_off[e];
+        for (int p = 0; p < TK; ++p)
+            if (s_ids[p] == e) {
+                s_inv[p] = slot;
+                P.tok[slot] = p / K;
+                if (g.perm) g.perm[slot] = p;
+                ++slot;
+            }
+    }
+    __syncthreads();
+    if (tid == 0 && g.offsets) g.offsets[E] = s_off[E];
+    if (g.inv)
+        for (int p = tid; p < TK; p += blockDim.x) g.inv[p] = s_inv[p];
+    if (g.plan) {
+        if (tid == 0) g.plan[0] = P.n;
+        for (int i = tid; i < P.n; i += blockDim.x) {
+            g.plan[kPlanHeader + i] = P.e[i];
+            g.plan[kPlanHeader + E + i] = P.off[i];
+            g.plan[kPlanHeader + 2 * E + i] = P.cnt[i];
+        }
+        for (int s = tid; s < TK; s += blockDim.x) g.plan[kPlanHeader + 3 * E + s] = P.tok[s];
+    }
+}
+
+// ------------------------------------------------------------- selection
+// Top-K of one token's logits (larger first, ties to the lower id), written
+// in ascending id to ids[0..K) with renormalised softmax weights w[0..K).
+// One warp.  L: this warp's shared scratch of E floats; ex: K floats.
+// A lane keeps the best of its own logits (ids lane, lane+32, ...); each
+// pick is a warp arg-max over the lanes' bests, after which only the winning
+// lane rescans its own logits.
+__device__ void select_topk_warp(const float* lg, int E, int K, float* L, float* ex, int* ids,
+                                 float* w, int lane) {
+    for (int e = lane; e < E; e += 32) L[e] = __ldcg(lg + e);
+    __syncwarp();
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+        const float v = L[e];
+        if (v > bv || (v == bv && e < be)) {
+            bv = v;
+            be = e;
+        }
+    }
+    float myv = 0.0f;
+    int mye = 0x7fffffff;
+    for (int k = 0; k < K; ++k) {
+        float wv = bv;
+        int we = be;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, we, o);
+            if (ov > wv || (ov == wv && oe < we)) {
+                wv = ov;
+                we = oe;
+            }
+        }
+        if (lane == k) {
+            myv = wv;
+            mye = we;
+        }
+        if (we < E && (we & 31) == lane) {
+            L[we] = __int_as_float(0x7fc00000);    // taken: NaN never wins
+            bv = -INFINITY;
+            be = 0x7fffffff;
+            for (int e = lane; e < E; e += 32) {
+                const float v = L[e];
+                if (v > bv || (v == bv && e < be)) {
+                    bv = v;
+                    be = e;
+                }
+            }
+        }
+    }
+    const float m = __shfl_sync(0xffffffffu, myv, 0);      // the first pick is the largest
+    int rank = 0;
+    for (int j = 0; j < K; ++j) rank += (__shfl_sync(0xffffffffu, mye, j) < mye) ? 1 : 0;
+    float e_k = 0.0f;
+    if (lane < K) {
+        e_k = expf(myv - m);
+        ex[rank] = e_k;
+        ids[rank] = mye;
+    }
+    __syncwarp();
+    float sum = 0.0f;
+    for (int r = 0; r < K; ++r) sum += ex[r];                 // ascending id
+    if (lane < K) w[rank] = e_k / sum;
+    __syncwarp();
+}
+
+// Routing of all T tokens by one CTA into shared memory: s_ids, s_w [T*K],
+// s_sig [T].  forced_ids / forced_w replace the selection when given.
+// scratch: (blockDim / 32) * (E + 16) floats.
+__device__ void route_cta(const float* logits, int T, int E, int K, const int32_t* forced_ids,
+                          const float* forced_w, int* s_ids, float* s_w, float* s_sig,
+                          float* scratch, uint32_t* err) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+    const int ldl = E + 1;
+    for (int t = wid; t < T; t += wpb) {
+        const float* lg = logits + size_t(t) * ldl;
+        if (forced_ids) {
+            for (int k = lane; k < K; k += 32) {
+                const int id = __ldg(forced_ids + t * K + k);
+                if (id < 0 || id >= E) latch(err, STRATA_EBADROUTE);
+                s_ids[t * K + k] = id;
+                s_w[t * K + k] = __ldg(forced_w + t * K + k);
+            }
+        } else {
+            float* L = scratch + size_t(wid) * (E + 16);
+            select_topk_warp(lg, E, K, L, L + E, s_ids + t * K, s_w + t * K, lane);
+        }
+        if (lane == 0) s_sig[t] = 1.0f / (1.0f + expf(-__ldcg(lg + E)));
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------- x activations
 // Lane `lane` owns chunks c = lane + 32 m (m < MC) of a length-H row; a chunk
 // is 32 elements.  Loads token row x (bf16) as fp32 pairs plus chunk sums.
 template <int MC>
@@ -118,203 +299,30 @@ __device__ __forceinline__ void load_x(const uint16_t* xrow, int NC, int lane,
     }
 }
 
-// Gate/up of row pairs [i0, i0 + nb) of one expert for the tokens of slots
-// [s0, s0 + scount): h[s][i] = silu(g_i) u_i.  perm == nullptr means slot s
-// is token s (the shared expert).  One warp.
-template <int MC, int RB>
-__device__ void gu_batch(const uint8_t* qe, const uint16_t* se, int H, int i0, int nb,
-                         const uint16_t* x, int s0, int scount, const int32_t* perm, int K,
-                         int TK, float* h, int ldh, uint32_t* err, int lane) {
-    const int NC = H >> 5;
-    const size_t qrow = size_t(H) >> 1;
-    const size_t srow = size_t(H) >> 5;
-    uint4 qv[RB][2][MC];
-    float sc[RB][2][MC];
-#pragma unroll
-    for (int p = 0; p < RB; ++p)
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int m = 0; m < MC; ++m) {
-                const int c = lane + 32 * m;
-                const size_t row = size_t(2 * (i0 + p) + r);
-                if (p < nb && c < NC) {
-                    qv[p][r][m] = ldg_stream(qe + row * qrow + size_t(c) * 16);
-                    sc[p][r][m] = f16_to_f32(ldg_u16(se + row * srow + c));
-                } else {
-                    qv[p][r][m] = make_uint4(0u, 0u, 0u, 0u);
-                    sc[p][r][m] = 0.0f;
-                }
-            }
-    for (int si = 0; si < scount; ++si) {
-        const int s = s0 + si;
-        int t = s;
-        if (perm != nullptr) {
-            const int pr = __ldcg(perm + s);
-            if (pr < 0 || pr >= TK) {
-                latch(err, STRATA_EBADROUTE);
-                continue;
-            }
-            t = pr / K;
-        }
-        uint64_t x2[MC][16];
-        float X[MC];
-        load_x<MC>(x + size_t(t) * H, NC, lane, x2, X);
-        float acc[RB][2];
-#pragma unroll
-        for (int p = 0; p < RB; ++p)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                float a = 0.0f;
-#pragma unroll
-                for (int m = 0; m < MC; ++m)
-                    if (lane + 32 * m < NC)
-                        a += group_dot(dot_chunk(qv[p][r][m], x2[m]), X[m], sc[p][r][m]);
-                acc[p][r] = warp_sum(a);
-            }
-        float g = 0.0f, u = 0.0f;
-#pragma unroll
-        for (int p = 0; p < RB; ++p)
-            if (p == lane) {
-                g = acc[p][0];
-                u = acc[p][1];
-            }
-        if (lane < nb) h[size_t(s) * ldh + i0 + lane] = silu_mul(g, u);
-    }
-}
-
-// ------------------------------------------------------------- k_gate_up
-template <int MC, int RB>
-__global__ void __launch_bounds__(256, 1) k_gate_up(GuLaunch a) {
-    __shared__ ActiveList s_act;
-    const int lane = threadIdx.x & 31;
-    const int TK = a.T * a.K;
-    if (a.shared) {
-        if (threadIdx.x == 0) {
-            s_act.n = 1;
-            s_act.e[0] = 0;
-            s_act.off[0] = 0;
-            s_act.cnt[0] = a.T;
-        }
-        __syncthreads();
-    } else {
-        build_active(s_act, a.offsets, a.E, TK, a.err);
-    }
-    const long long RP = (long long)s_act.n * a.I;
-    const int wpb = blockDim.x >> 5;
-    const long long NW = (long long)gridDim.x * wpb;
-    const long long gw = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
-    const long long beg = gw * RP / NW, end = (gw + 1) * RP / NW;
-    const size_t qexp = size_t(2) * a.I * (size_t(a.H) >> 1);
-    const size_t sexp = size_t(2) * a.I * (size_t(a.H) >> 5);
-    for (long long rp = beg; rp < end;) {
-        const int j = int(rp / a.I), i0 = int(rp % a.I);
-        const int nb = int(min((long long)RB, min((long long)(a.I - i0), end - rp)));
-        const int e = s_act.e[j];
-        gu_batch<MC, RB>(a.q + size_t(e) * qexp, a.sc + size_t(e) * sexp, a.H, i0, nb, a.x,
-                         s_act.off[j], s_act.cnt[j], a.shared ? nullptr : a.perm, a.K, TK, a.h,
-                         a.I, a.err, lane);
-        rp += nb;
-    }
-}
-
-// Stable counting sort of the T*K (token, k) pairs by expert, one CTA.
-// ids: the pairs' expert ids in shared memory; out-of-range ids get no slot
-// (inv = -1).  counts[e], offsets[0..E], perm[slot] = t*K + k with the slots
-// of one expert in ascending t, inv[t*K + k] = slot.
-__device__ void permute_block(const int32_t* s_ids, int T, int K, int E, int32_t* counts,
-                              int32_t* offsets, int32_t* perm, int32_t* inv, int* s_cnt,
-                              int* s_off, int* s_wsum) {
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, wpb = blockDim.x >> 5;
-    const int TK = T * K;
-    for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
-    __syncthreads();
-    for (int p = tid; p < TK; p += blockDim.x) {
-        const int e = s_ids[p];
-        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-    }
-    __syncthreads();
-    // exclusive scan of s_cnt: each thread one contiguous segment of experts
-    const int seg = (E + blockDim.x - 1) / blockDim.x;
-    const int e0 = min(E, tid * seg), e1 = min(E, e0 + seg);
-    int local = 0;
-    for (int e = e0; e < e1; ++e) local += s_cnt[e];
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) s_wsum[wid] = incl;
-    __syncthreads();
-    if (tid == 0) {
-        int r = 0;
-        for (int w = 0; w < wpb; ++w) {
-            const int c = s_wsum[w];
-            s_wsum[w] = r;
-            r += c;
-        }
-        s_off[E] = r;
-    }
-    __syncthreads();
-    int run = s_wsum[wid] + incl - local;
-    for (int e = e0; e < e1; ++e) {
-        s_off[e] = run;
-        run += s_cnt[e];
-    }
-    __syncthreads();
-    for (int p = tid; p < TK; p += blockDim.x) {
-        const int e = s_ids[p];
-        if (e < 0 || e >= E) inv[p] = -1;
-    }
-    for (int e = tid; e < E; e += blockDim.x) {
-        const int c = s_cnt[e];
-        counts[e] = c;
-        offsets[e] = s_off[e];
-        if (c == 0) continue;
-        int slot = s_off[e];
-        for (int p = 0; p < TK; ++p)
-            if (s_ids[p] == e) {
-                perm[slot] = p;
-                inv[p] = slot;
-                ++slot;
-            }
-    }
-    if (tid == 0) offsets[E] = s_off[E];
-}
-
-// Standalone bucketing of up to kDecodeMaxTokens * kMaxTopK pairs.
-__global__ void __launch_bounds__(256, 1) k_permute_small(const int32_t* ids, int T, int K, int E,
-                                                          int32_t* counts, int32_t* offsets,
-                                                          int32_t* perm, int32_t* inv,
-                                                          uint32_t* err) {
-    __shared__ int32_t s_ids[kDecodeMaxTokens * kMaxTopK];
-    __shared__ int s_cnt[kMaxExperts];
-    __shared__ int s_off[kMaxExperts + 1];
-    __shared__ int s_wsum[32];
-    for (int p = threadIdx.x; p < T * K; p += blockDim.x) {
-        const int e = __ldg(ids + p);
-        if (e < 0 || e >= E) latch(err, STRATA_EBADROUTE);
-        s_ids[p] = e;
-    }
-    __syncthreads();
-    permute_block(s_ids, T, K, E, counts, offsets, perm, inv, s_cnt, s_off, s_wsum);
-}
-
-// --------------------------------------------------------- k_route_decode
-// Router row e (bf16 weights) against every token: logits[t][e] (+ bias).
+// ---------------------------------------------------------------- k_route
 template <int MC>
-__device__ void router_row(const uint16_t* wrow, const uint16_t* x, int T, int H, float bias,
-                           float* logits, int ldl, int e, int lane) {
+struct RouterRow {
+    uint4 w[MC][4];
+};
+
+template <int MC>
+__device__ __forceinline__ void router_load(RouterRow<MC>& R, const uint16_t* wrow, int H,
+                                            int lane) {
     const int NC = H >> 5;
-    uint4 wv[MC][4];
 #pragma unroll
     for (int m = 0; m < MC; ++m)
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
             const int c = lane + 32 * m;
-            wv[m][v] = (c < NC) ? ldg_stream(wrow + 32 * c + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+            R.w[m][v] = (c < NC) ? ldg_stream(wrow + 32 * c + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
         }
+}
+
+// logits[t][e] = router row e . x[t] (+ bias), every token.  One warp.
+template <int MC>
+__device__ void router_compute(const RouterRow<MC>& R, const uint16_t* x, int T, int H,
+                               float bias, float* logits, int ldl, int e, int lane) {
+    const int NC = H >> 5;
     for (int t = 0; t < T; ++t) {
         uint64_t acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
@@ -326,7 +334,7 @@ __device__ void router_row(const uint16_t* wrow, const uint16_t* x, int T, int H
                 for (int v = 0; v < 4; ++v) {
                     const uint4 xu = ldg_keep(xp + v);
                     const uint32_t xw[4] = {xu.x, xu.y, xu.z, xu.w};
-                    const uint32_t ww[4] = {wv[m][v].x, wv[m][v].y, wv[m][v].z, wv[m][v].w};
+                    const uint32_t ww[4] = {R.w[m][v].x, R.w[m][v].y, R.w[m][v].z, R.w[m][v].w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const uint64_t a = pk(bf16_lo(ww[i]), bf16_hi(ww[i]));
@@ -345,225 +353,503 @@ __device__ void router_row(const uint16_t* wrow, const uint16_t* x, int T, int H
     }
 }
 
-// Top-K of one token's logits (larger first, ties to the lower id), stored
-// in ascending id with renormalised softmax weights.  One warp; L is this
-// warp's shared-memory copy of the logits.
-__device__ void select_token(const RouteLaunch& a, int t, int lane, float* L, int32_t* s_ids) {
-    const int E = a.E, K = a.K, ldl = E + 1;
-    const float* lg = a.logits + size_t(t) * ldl;
-    for (int e = lane; e < E; e += 32) L[e] = __ldcg(lg + e);
-    __syncwarp();
-    float selv[kMaxTopK];
-    int sele[kMaxTopK];
+// Registers of RB gate/up row pairs of the shared expert (k_route's share).
+template <int MC, int RB>
+struct GuRows {
+    uint4 q[RB][2][MC];
+    float s[RB][2][MC];
+};
+
+template <int MC, int RB>
+__device__ __forceinline__ void gu_load(GuRows<MC, RB>& R, const uint8_t* qe, const uint16_t* se,
+                                        int H, int i0, int nb, int lane) {
+    const int NC = H >> 5;
+    const size_t qrow = size_t(H) >> 1, srow = size_t(H) >> 5;
 #pragma unroll
-    for (int k = 0; k < kMaxTopK; ++k) {
-        selv[k] = 0.0f;
-        sele[k] = 0x7fffffff;
-        if (k < K) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
-            for (int e = lane; e < E; e += 32) {
-                const float v = L[e];
-                if (v > bv || (v == bv && e < be)) {
-                    bv = v;
-                    be = e;
+    for (int p = 0; p < RB; ++p)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int m = 0; m < MC; ++m) {
+                const int c = lane + 32 * m;
+                const size_t row = size_t(2 * (i0 + p) + r);
+                if (p < nb && c < NC) {
+                    R.q[p][r][m] = ldg_stream(qe + row * qrow + size_t(c) * 16);
+                    R.s[p][r][m] = f16_to_f32(ldg_u16(se + row * srow + c));
+                } else {
+                    R.q[p][r][m] = make_uint4(0u, 0u, 0u, 0u);
+                    R.s[p][r][m] = 0.0f;
                 }
             }
+}
+
+// hs[t][i0 + p] = silu(g) u for every token, row pairs p < nb.  One warp.
+template <int MC, int RB>
+__device__ void gu_compute_all_tokens(const GuRows<MC, RB>& R, int H, int T, int i0, int nb,
+                                      const uint16_t* x, float* h, int ldh, int lane) {
+    const int NC = H >> 5;
+    for (int t = 0; t < T; ++t) {
+        uint64_t x2[MC][16];
+        float X[MC];
+        load_x<MC>(x + size_t(t) * H, NC, lane, x2, X);
+        float acc[RB][2];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
+        for (int p = 0; p < RB; ++p)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                float a = 0.0f;
+#pragma unroll
+                for (int m = 0; m < MC; ++m)
+                    if (lane + 32 * m < NC)
+                        a += group_dot(dot_chunk(R.q[p][r][m], x2[m]), X[m], R.s[p][r][m]);
+                acc[p][r] = warp_sum(a);
             }
-            selv[k] = bv;
-            sele[k] = be;
-            if (be < E && lane == (be & 31)) L[be] = __int_as_float(0x7fc00000);  // taken
-            __syncwarp();
-        }
-    }
-    // rank of each pick in ascending id
-    int rank[kMaxTopK];
+        float g = 0.0f, u = 0.0f;
 #pragma unroll
-    for (int k = 0; k < kMaxTopK; ++k) {
-        int r = 0;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) r += (j < K && sele[j] < sele[k]) ? 1 : 0;
-        rank[k] = r;
+        for (int p = 0; p < RB; ++p)
+            if (p == lane) {
+                g = acc[p][0];
+                u = acc[p][1];
+            }
+        if (lane < nb) h[size_t(t) * ldh + i0 + lane] = silu_mul(g, u);
     }
-    const float m = selv[0];
-    float sum = 0.0f;
-    for (int r = 0; r < K; ++r) {
-#pragma unroll
-        for (int k = 0; k < kMaxTopK; ++k)
-            if (k < K && rank[k] == r) sum += expf(selv[k] - m);
-    }
-#pragma unroll
-    for (int k = 0; k < kMaxTopK; ++k) {
-        if (k < K && rank[k] == lane) {
-            const int id = sele[k];
-            const float wv = expf(selv[k] - m) / sum;
-            const size_t o = size_t(t) * K + lane;
-            a.ids[o] = id;
-            a.w[o] = wv;
-            if (a.ids_user) a.ids_user[o] = id;
-            if (a.w_user) a.w_user[o] = wv;
-            s_ids[o] = id;
-        }
-    }
-    if (a.logits_user)
-        for (int e = lane; e < E; e += 32) a.logits_user[size_t(t) * E + e] = __ldcg(lg + e);
 }
 
 template <int MC, int RB>
-__global__ void __launch_bounds__(256, 1) k_route_decode(RouteLaunch a) {
-    extern __shared__ float s_dyn[];           // [warps][E] logits for selection
-    __shared__ int s_last;
-    __shared__ int32_t s_ids[kDecodeMaxTokens * kMaxTopK];
-    __shared__ int s_cnt[kMaxExperts];
-    __shared__ int s_off[kMaxExperts + 1];
-    __shared__ int s_wsum[32];
-    Ctl* ctl = reinterpret_cast<Ctl*>(a.ctl);
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, wpb = blockDim.x >> 5;
+__global__ void __launch_bounds__(256, 1) k_route(RouteLaunch a) {
+    pdl_launch();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, wpb = blockDim.x >> 5;
     const int ldl = a.E + 1;
     const int n_router = a.do_select ? a.E + 1 : 1;
     const int n_sh = a.do_shared ? (a.Is + RB - 1) / RB : 0;
     const int ntask = n_router + n_sh;
-
+    // The first task's weights do not depend on the previous kernel: they are
+    // requested before waiting for it.
+    bool waited = false;
     for (int task = blockIdx.x + gridDim.x * wid; task < ntask; task += gridDim.x * wpb) {
         if (task < n_router) {
             const int e = a.do_select ? task : a.E;
+            RouterRow<MC> R;
+            router_load<MC>(R, a.router + size_t(e) * a.H, a.H, lane);
             const float b = (e < a.E && a.bias) ? __ldg(a.bias + e) : 0.0f;
-            router_row<MC>(a.router + size_t(e) * a.H, a.x, a.T, a.H, b, a.logits, ldl, e, lane);
+            if (!waited) pdl_wait();
+            waited = true;
+            router_compute<MC>(R, a.x, a.T, a.H, b, a.logits, ldl, e, lane);
         } else {
             const int i0 = (task - n_router) * RB;
-            gu_batch<MC, RB>(a.shq, a.shs, a.H, i0, min(RB, a.Is - i0), a.x, 0, a.T, nullptr, 1,
-                             a.T, a.hs, a.Is, &ctl->err, lane);
+            const int nb = min(RB, a.Is - i0);
+            GuRows<MC, RB> R;
+            gu_load<MC, RB>(R, a.shq, a.shs, a.H, i0, nb, lane);
+            if (!waited) pdl_wait();
+            waited = true;
+            gu_compute_all_tokens<MC, RB>(R, a.H, a.T, i0, nb, a.x, a.hs, a.Is, lane);
         }
     }
+    if (!waited) pdl_wait();
+}
 
-    // Last CTA to finish continues (no CTA waits for another).
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = (atomicAdd(&ctl->arrive, 1u) == gridDim.x - 1) ? 1 : 0;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+// The routing of moe_route: one CTA selects every token (T <= 32) from the
+// logits k_route wrote.
+__global__ void __launch_bounds__(256, 1) k_select(SelectLaunch a) {
+    extern __shared__ float s_dyn[];
+    __shared__ int s_ids[kDecodeMaxTokens * kMaxTopK];
+    __shared__ float s_w[kDecodeMaxTokens * kMaxTopK];
+    __shared__ float s_sig[kDecodeMaxTokens];
+    pdl_launch();
+    pdl_wait();
+    route_cta(a.logits, a.T, a.E, a.K, nullptr, nullptr, s_ids, s_w, s_sig, s_dyn, a.err);
+    const int TK = a.T * a.K;
+    for (int p = threadIdx.x; p < TK; p += blockDim.x) {
+        a.ids[p] = s_ids[p];
+        a.w[p] = s_w[p];
+    }
+    for (int t = threadIdx.x; t < a.T; t += blockDim.x) a.sig[t] = s_sig[t];
+    if (a.logits_out)
+        for (int i = threadIdx.x; i < a.T * a.E; i += blockDim.x)
+            a.logits_out[i] = __ldcg(a.logits + size_t(i / a.E) * (a.E + 1) + i % a.E);
+}
 
-    const int T = a.T, K = a.K, E = a.E;
-    for (int t = wid; t < T; t += wpb) {
-        if (a.do_select) {
-            select_token(a, t, lane, s_dyn + size_t(wid) * E, s_ids);
-        } else {
-            for (int k = lane; k < K; k += 32) {
-                const size_t o = size_t(t) * K + k;
-                const int id = __ldg(a.ids_in + o);
-                const float wv = __ldg(a.w_in + o);
-                if (id < 0 || id >= E) latch(&ctl->err, STRATA_EBADROUTE);
-                a.ids[o] = id;
-                a.w[o] = wv;
-                s_ids[o] = id;
+// -------------------------------------------------------------- bucketing
+// Standalone bucketing of up to kDecodeMaxTokens * kMaxTopK pairs.
+__global__ void __launch_bounds__(256, 1) k_permute_small(const int32_t* ids, int T, int K, int E,
+                                                          int32_t* counts, int32_t* offsets,
+                                                          int32_t* perm, int32_t* inv,
+                                                          uint32_t* err) {
+    __shared__ int s_ids[kDecodeMaxTokens * kMaxTopK];
+    __shared__ int s_inv[kDecodeMaxTokens * kMaxTopK];
+    __shared__ int s_cnt[kMaxExperts];
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ int s_wsum[32];
+    __shared__ SPlan P;
+    pdl_launch();
+    pdl_wait();
+    for (int p = threadIdx.x; p < T * K; p += blockDim.x) {
+        const int e = __ldg(ids + p);
+        if (e < 0 || e >= E) latch(err, STRATA_EBADROUTE);
+        s_ids[p] = e;
+    }
+    __syncthreads();
+    const BucketOut g{counts, offsets, perm, inv, nullptr};
+    bucket_cta(s_ids, T, K, E, s_cnt, s_off, s_wsum, P, s_inv, g);
+}
+
+// The plan from a bucketing given by the caller (offsets and perm from any
+// source); inconsistent entries latch STRATA_EBADROUTE and are left out.
+__global__ void __launch_bounds__(256, 1) k_plan(const int32_t* offsets, const int32_t* perm,
+                                                 int T, int K, int E, int32_t* plan,
+                                                 uint32_t* err) {
+    __shared__ int warp_base[32];
+    __shared__ int running;
+    pdl_launch();
+    pdl_wait();
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+    const int TK = T * K;
+    // token of each slot; without perm (the down product needs slots only) 0
+    for (int s = tid; s < TK; s += blockDim.x) {
+        int t = 0;
+        if (perm != nullptr) {
+            const int p = __ldg(perm + s);
+            if (p >= 0 && p < TK) {
+                t = p / K;
+            } else {
+                latch(err, STRATA_EBADROUTE);
+                t = -1;
             }
         }
-        if (lane == 0) {
-            const float s = 1.0f / (1.0f + expf(-__ldcg(a.logits + size_t(t) * ldl + E)));
-            a.sig[t] = s;
-            if (a.sig_user) a.sig_user[t] = s;
+        plan[kPlanHeader + 3 * E + s] = t;
+    }
+    if (tid == 0) running = 0;
+    __syncthreads();
+    for (int base = 0; base < E; base += blockDim.x) {
+        const int e = base + tid;
+        int off = 0, cnt = 0;
+        if (e < E) {
+            off = __ldg(offsets + e);
+            const int end = __ldg(offsets + e + 1);
+            cnt = end - off;
+            if (off < 0 || cnt < 0 || end > TK) {
+                latch(err, STRATA_EBADROUTE);
+                cnt = 0;
+            }
         }
+        const unsigned bal = __ballot_sync(0xffffffffu, cnt > 0);
+        const int pre = __popc(bal & ((1u << lane) - 1u));
+        if (lane == 0) warp_base[wid] = __popc(bal);
+        __syncthreads();
+        if (tid == 0) {
+            int r = running;
+            for (int w = 0; w < nw; ++w) {
+                const int c = warp_base[w];
+                warp_base[w] = r;
+                r += c;
+            }
+            running = r;
+        }
+        __syncthreads();
+        if (cnt > 0) {
+            const int pos = warp_base[wid] + pre;
+            plan[kPlanHeader + pos] = e;
+            plan[kPlanHeader + E + pos] = off;
+            plan[kPlanHeader + 2 * E + pos] = cnt;
+        }
+        __syncthreads();
+    }
+    if (tid == 0) plan[0] = running;
+}
+
+// -------------------------------------------------------------- k_gate_up
+// Consumer warps and row pairs per ring stage.  A stage holds kGuRowPairs
+// interleaved gate/up row pairs of one expert (their packed bytes and their
+// scales, two bulk copies); consumer warp w computes row pairs w and
+// w + kGuConsumers of every stage.
+constexpr int kGuConsumers = 8;
+constexpr int kGuRowPairs = 16;
+constexpr int kGuThreads = 32 * (kGuConsumers + 1);
+
+template <int MC>
+__global__ void __launch_bounds__(kGuThreads, 1) k_gate_up(GuLaunch a) {
+    extern __shared__ __align__(128) uint8_t g_ring[];
+    __shared__ SPlan P;
+    __shared__ int s_ids[kDecodeMaxTokens * kMaxTopK];
+    __shared__ float s_w[kDecodeMaxTokens * kMaxTopK];
+    __shared__ int s_inv[kDecodeMaxTokens * kMaxTopK];
+    __shared__ float s_sig[kDecodeMaxTokens];
+    __shared__ int s_cnt[kMaxExperts];
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ int s_wsum[32];
+    __shared__ __align__(8) uint64_t full[kGuMaxStages], empty[kGuMaxStages];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int S = a.stages;
+    pdl_launch();
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kGuConsumers);
+        }
+        mbar_fence_init();
     }
     __syncthreads();
+    pdl_wait();
 
-    if (a.do_permute)
-        permute_block(s_ids, T, K, E, a.counts, a.offsets, a.perm, a.inv, s_cnt, s_off, s_wsum);
-    if (tid == 0) atomicExch(&ctl->arrive, 0u);
+    const int T = a.T, K = a.K, E = a.E, H = a.H, I = a.I;
+    if (a.mode == kGuShared) {
+        shared_plan(P, T);
+    } else if (a.mode == kGuPlan) {
+        load_plan(P, a.plan, E, T * K);
+    } else {
+        // routing: the same in every CTA; CTA 0 publishes it
+        route_cta(a.logits, T, E, K, a.forced_ids, a.forced_w, s_ids, s_w, s_sig,
+                  reinterpret_cast<float*>(g_ring), a.err);
+        BucketOut g{nullptr, nullptr, nullptr, nullptr, nullptr};
+        if (blockIdx.x == 0) g = BucketOut{a.counts, a.offsets, a.perm, a.inv, a.plan_out};
+        bucket_cta(s_ids, T, K, E, s_cnt, s_off, s_wsum, P, s_inv, g);
+        if (blockIdx.x == 0) {
+            for (int p = tid; p < T * K; p += blockDim.x) {
+                a.ids[p] = s_ids[p];
+                a.w[p] = s_w[p];
+                if (a.ids_user) a.ids_user[p] = s_ids[p];
+                if (a.w_user) a.w_user[p] = s_w[p];
+            }
+            for (int t = tid; t < T; t += blockDim.x) {
+                a.sig[t] = s_sig[t];
+                if (a.sig_user) a.sig_user[t] = s_sig[t];
+            }
+        }
+        __syncthreads();
+    }
+
+    // this CTA's contiguous share of the touched experts' row pairs
+    const long long RP = (long long)P.n * I;
+    const long long beg = (long long)blockIdx.x * RP / gridDim.x;
+    const long long end = (long long)(blockIdx.x + 1) * RP / gridDim.x;
+    const size_t qrow = size_t(H) >> 1, srow = size_t(H) >> 5;   // bytes, scales per row
+    const size_t qexp = size_t(2) * I * qrow, sexp = size_t(2) * I * srow;
+    const uint32_t stage_q = uint32_t(kGuRowPairs * 2 * qrow);
+    const uint32_t stage_bytes = stage_q + uint32_t(kGuRowPairs * 2 * srow * 2);
+
+    if (wid == 0) {
+        // producer
+        if (lane == 0) {
+            int i = 0;
+            for (long long rp = beg; rp < end; ++i) {
+                const int j = int(rp / I), i0 = int(rp % I);
+                const int nb = int(min((long long)kGuRowPairs, min((long long)(I - i0), end - rp)));
+                const int slot = i % S, round = i / S;
+                if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1))
+                    latch_timeout(a.err, 1, slot, round, i);
+                const int e = P.e[j];
+                uint8_t* dq = g_ring + size_t(slot) * stage_bytes;
+                const uint32_t bq = uint32_t(nb * 2 * qrow), bs = uint32_t(nb * 2 * srow * 2);
+                mbar_expect_tx(&full[slot], bq + bs);
+                bulk_g2s(dq, a.q + size_t(e) * qexp + size_t(2 * i0) * qrow, bq, &full[slot]);
+                bulk_g2s(dq + stage_q, a.sc + size_t(e) * sexp + size_t(2 * i0) * srow, bs,
+                         &full[slot]);
+                rp += nb;
+            }
+        }
+        return;
+    }
+
+    // consumers
+    const int cw = wid - 1;
+    const int NC = H >> 5;
+    uint64_t x2[MC][16];
+    float X[MC];
+    int xt = -1;              // token whose activations x2 holds
+    int i = 0;
+    for (long long rp = beg; rp < end; ++i) {
+        const int j = int(rp / I), i0 = int(rp % I);
+        const int nb = int(min((long long)kGuRowPairs, min((long long)(I - i0), end - rp)));
+        const int slot = i % S, round = i / S;
+        const int s0 = P.off[j], scount = P.cnt[j];
+        if (scount > 0 && P.tok[s0] != xt && P.tok[s0] >= 0 && P.tok[s0] < T) {
+            xt = P.tok[s0];
+            load_x<MC>(a.x + size_t(xt) * H, NC, lane, x2, X);      // overlaps the copy
+        }
+        if (!mbar_wait(&full[slot], round & 1)) latch_timeout(a.err, 2, slot, round, i);
+        const uint8_t* sq = g_ring + size_t(slot) * stage_bytes;
+        const uint16_t* ss = reinterpret_cast<const uint16_t*>(sq + stage_q);
+        for (int si = 0; si < scount; ++si) {
+            const int s = s0 + si;
+            const int t = P.tok[s];
+            if (t < 0 || t >= T) continue;
+            if (t != xt) {
+                xt = t;
+                load_x<MC>(a.x + size_t(t) * H, NC, lane, x2, X);
+            }
+#pragma unroll
+            for (int pp = 0; pp < kGuRowPairs / kGuConsumers; ++pp) {
+                const int p = cw + pp * kGuConsumers;
+                if (p >= nb) break;
+                float acc[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint8_t* qr = sq + size_t(2 * p + r) * qrow;
+                    const uint16_t* sr = ss + size_t(2 * p + r) * srow;
+                    float v = 0.0f;
+#pragma unroll
+                    for (int m = 0; m < MC; ++m) {
+                        const int c = lane + 32 * m;
+                        if (c < NC) {
+                            const uint4 q = *reinterpret_cast<const uint4*>(qr + 16 * c);
+                            const float sc = f16_to_f32(sr[c]);
+                            v += group_dot(dot_chunk(q, x2[m]), X[m], sc);
+                        }
+                    }
+                    acc[r] = warp_sum(v);
+                }
+                if (lane == 0) a.h[size_t(s) * I + i0 + p] = silu_mul(acc[0], acc[1]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        rp += nb;
+    }
 }
 
 // ----------------------------------------------------------------- k_down
-constexpr int kDownMaxRowsPerLane = kDownRowsPerCta;
+// A CTA owns kDownRowsPerCta output rows.  Ring stages hold one expert's
+// slice of those rows (packed bytes and scales, two bulk copies); consumer
+// warp w computes the units w, w + kDnConsumers, ...: unit 0 is the shared
+// expert (its copy is requested before griddepcontrol.wait), units 1.. the
+// touched experts.  Lane (rs, c) of a warp holds chunk c of rows rs,
+// rs + RPW, ... (RPW = 32 / chunks per row).
+constexpr int kDnConsumers = 12;
+constexpr int kDnThreads = 32 * (kDnConsumers + 1);
+static_assert(kDnMaxStages % kDnConsumers == 0, "stages must be a multiple of consumer warps");
 
-__global__ void __launch_bounds__(384, 1) k_down(DownLaunch a) {
-    extern __shared__ float s_y[];          // [(T*K + T)][kDownRowsPerCta]
-    __shared__ ActiveList s_act;
+template <int MR>
+__device__ void down_unit(const uint8_t* sq, const uint16_t* ss, int len, int nrow, int lane,
+                          const float* hb, int s0, int scount, const int* tok, float* s_y,
+                          int ybase) {
     constexpr int RBc = kDownRowsPerCta;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, wpb = blockDim.x >> 5;
+    const int NCd = len >> 5, RPW = 32 / NCd;
+    const int c = lane & (NCd - 1), rs = lane / NCd;
+    const int nr = (nrow > rs) ? (nrow - rs + RPW - 1) / RPW : 0;
+    const int npass = (RBc + RPW - 1) / RPW;     // uniform over the warp
+    const size_t qrow = size_t(len) >> 1, srow = size_t(len) >> 5;
+    uint4 q[MR];
+    float sc[MR];
+#pragma unroll
+    for (int m = 0; m < MR; ++m) {
+        if (m < nr) {
+            const int row = rs + m * RPW;
+            q[m] = *reinterpret_cast<const uint4*>(sq + row * qrow + 16 * c);
+            sc[m] = f16_to_f32(ss[row * srow + c]);
+        } else {
+            q[m] = make_uint4(0u, 0u, 0u, 0u);
+            sc[m] = 0.0f;
+        }
+    }
+    for (int si = 0; si < scount; ++si) {
+        const int s = s0 + si;
+        if (tok != nullptr && tok[s] < 0) continue;
+        const float* hp = hb + size_t(s) * len + 32 * c;
+        uint64_t x2[16];
+        float X = 0.0f;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const float4 f = ldcg_f4(hp + 4 * v);
+            x2[2 * v] = pk(f.x, f.y);
+            x2[2 * v + 1] = pk(f.z, f.w);
+            X += (f.x + f.y) + (f.z + f.w);
+        }
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+            if (m < npass) {
+                float part = (m < nr) ? group_dot(dot_chunk(q[m], x2), X, sc[m]) : 0.0f;
+                part = group_sum(part, NCd);
+                if (c == 0 && m < nr) s_y[size_t(ybase + s) * RBc + rs + m * RPW] = part;
+            }
+        }
+    }
+}
+
+template <int MR>
+__global__ void __launch_bounds__(kDnThreads, 1) k_down(DownLaunch a) {
+    extern __shared__ __align__(128) uint8_t d_dyn[];
+    __shared__ SPlan P;
+    __shared__ int s_inv[kDecodeMaxTokens * kMaxTopK];
+    __shared__ float s_w[kDecodeMaxTokens * kMaxTopK];
+    __shared__ float s_sig[kDecodeMaxTokens];
+    __shared__ __align__(8) uint64_t full[kDnMaxStages], empty[kDnMaxStages];
+    constexpr int RBc = kDownRowsPerCta;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int S = a.stages;
     const int o0 = blockIdx.x * RBc;
     const int nrow = min(RBc, a.H - o0);
     const int TK = a.T * a.K;
-    const int nslot = TK + a.T;
-    for (int i = tid; i < nslot * RBc; i += blockDim.x) s_y[i] = 0.0f;
-    if (a.mode != kDownCombine) {
-        build_active(s_act, a.offsets, a.E, TK, a.err);
-    } else {
-        if (tid == 0) s_act.n = 0;
-        __syncthreads();
-    }
-    const int n_routed = s_act.n;
-    const int n_units = n_routed + (a.mode != kDownSlots ? 1 : 0);
+    const bool with_shared = a.mode != kDownSlots;
+    const int len = a.I > a.Is ? a.I : a.Is;
+    const uint32_t stage_q = uint32_t(RBc * (len >> 1));
+    const uint32_t stage_bytes = stage_q + uint32_t(RBc * (len >> 5) * 2);
+    float* s_y = reinterpret_cast<float*>(d_dyn + size_t(S) * stage_bytes);
 
-    for (int u = wid; u < n_units; u += wpb) {
-        const uint8_t* qe;
-        const uint16_t* se;
-        const float* hb;
-        int len, s0, scount, ybase;
-        if (u < n_routed) {
-            const int e = s_act.e[u];
-            len = a.I;
-            qe = a.q + size_t(e) * a.H * (size_t(a.I) >> 1);
-            se = a.sc + size_t(e) * a.H * (size_t(a.I) >> 5);
-            s0 = s_act.off[u];
-            scount = s_act.cnt[u];
-            hb = a.h;
-            ybase = 0;
-        } else {
-            len = a.Is;
-            qe = a.shq;
-            se = a.shs;
-            s0 = 0;
-            scount = a.T;
-            hb = a.hs;
-            ybase = TK;
+    // unit u's packed rows and scales: the shared expert is unit 0 when present
+    auto issue = [&](int u, int slot, int e) {
+        const bool sh = with_shared && u == 0;
+        const int L = sh ? a.Is : a.I;
+        const uint8_t* q = sh ? a.shq : a.q + size_t(e) * a.H * (size_t(L) >> 1);
+        const uint16_t* sc = sh ? a.shs : a.sc + size_t(e) * a.H * (size_t(L) >> 5);
+        const uint32_t bq = uint32_t(nrow * (L >> 1)), bs = uint32_t(nrow * (L >> 5) * 2);
+        uint8_t* dst = d_dyn + size_t(slot) * stage_bytes;
+        mbar_expect_tx(&full[slot], bq + bs);
+        bulk_g2s(dst, q + size_t(o0) * (L >> 1), bq, &full[slot]);
+        bulk_g2s(dst + stage_q, sc + size_t(o0) * (L >> 5), bs, &full[slot]);
+    };
+
+    pdl_launch();
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
         }
-        const int NCd = len >> 5;               // chunks per row (power of two <= 32)
-        const int RPW = 32 / NCd;               // rows per warp pass
-        const int c = lane & (NCd - 1), rs = lane / NCd;
-        const int nr = (nrow > rs) ? (nrow - rs + RPW - 1) / RPW : 0;
-        const size_t qrow = size_t(len) >> 1, srow = size_t(len) >> 5;
-        uint4 qv[kDownMaxRowsPerLane];
-        float sc[kDownMaxRowsPerLane];
-#pragma unroll
-        for (int m = 0; m < kDownMaxRowsPerLane; ++m) {
-            if (m < nr) {
-                const size_t row = size_t(o0 + rs + m * RPW);
-                qv[m] = ldg_stream(qe + row * qrow + size_t(c) * 16);
-                sc[m] = f16_to_f32(ldg_u16(se + row * srow + c));
+        mbar_fence_init();
+        if (with_shared) issue(0, 0, 0);       // static weights: before the wait
+    }
+    __syncthreads();
+    pdl_wait();
+
+    for (int i = tid; i < (TK + a.T) * RBc; i += blockDim.x) s_y[i] = 0.0f;
+    if (a.mode == kDownCombine) {
+        if (tid == 0) P.n = 0;
+    } else {
+        load_plan(P, a.plan, a.E, TK);
+    }
+    if (a.mode != kDownSlots) {
+        for (int i = tid; i < TK; i += blockDim.x) {
+            s_inv[i] = __ldcg(a.inv + i);
+            s_w[i] = __ldcg(a.w + i);
+        }
+        for (int t = tid; t < a.T; t += blockDim.x) s_sig[t] = __ldcg(a.sig + t);
+    }
+    __syncthreads();
+
+    const int sh = with_shared ? 1 : 0;
+    const int n_units = P.n + sh;
+    if (wid == 0) {
+        if (lane == 0) {
+            for (int u = sh; u < n_units; ++u) {
+                const int slot = u % S, round = u / S;
+                if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1))
+                    latch_timeout(a.err, 3, slot, round, u);
+                issue(u, slot, P.e[u - sh]);
+            }
+        }
+    } else {
+        for (int u = wid - 1; u < n_units; u += kDnConsumers) {
+            const int slot = u % S, round = u / S;
+            if (!mbar_wait(&full[slot], round & 1)) latch_timeout(a.err, 4, slot, round, u);
+            const uint8_t* sq = d_dyn + size_t(slot) * stage_bytes;
+            const uint16_t* ss = reinterpret_cast<const uint16_t*>(sq + stage_q);
+            if (with_shared && u == 0) {
+                down_unit<MR>(sq, ss, a.Is, nrow, lane, a.hs, 0, a.T, nullptr, s_y, TK);
             } else {
-                qv[m] = make_uint4(0u, 0u, 0u, 0u);
-                sc[m] = 0.0f;
+                const int j = u - sh;
+                down_unit<MR>(sq, ss, a.I, nrow, lane, a.h, P.off[j], P.cnt[j], P.tok, s_y, 0);
             }
-        }
-        for (int si = 0; si < scount; ++si) {
-            const int s = s0 + si;
-            const float* hp = hb + size_t(s) * len + 32 * c;
-            uint64_t x2[16];
-            float X = 0.0f;
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const float4 f = ldcg_f4(hp + 4 * v);
-                x2[2 * v] = pk(f.x, f.y);
-                x2[2 * v + 1] = pk(f.z, f.w);
-                X += (f.x + f.y) + (f.z + f.w);
-            }
-#pragma unroll
-            for (int m = 0; m < kDownMaxRowsPerLane; ++m) {
-                float part = 0.0f;
-                if (m < nr) part = group_dot(dot_chunk(qv[m], x2), X, sc[m]);
-                if (m < (RBc + RPW - 1) / RPW || m < nr) {
-                    part = group_sum(part, NCd);
-                    if (c == 0 && m < nr) s_y[size_t(ybase + s) * RBc + rs + m * RPW] = part;
-                }
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
         }
     }
     __syncthreads();
@@ -579,15 +865,15 @@ __global__ void __launch_bounds__(384, 1) k_down(DownLaunch a) {
         const int t = i / nrow, r = i - t * nrow, o = o0 + r;
         float acc = 0.0f;
         for (int k = 0; k < a.K; ++k) {
-            const int sl = __ldcg(a.inv + size_t(t) * a.K + k);
+            const int sl = s_inv[t * a.K + k];
             if (sl < 0 || sl >= TK) continue;
             const float yv = (a.mode == kDownFused)
                                  ? s_y[size_t(sl) * RBc + r]
                                  : __uint_as_float(uint32_t(__ldg(a.y_in + size_t(sl) * a.H + o))
                                                    << 16);
-            acc += __ldcg(a.w + size_t(t) * a.K + k) * yv;
+            acc += s_w[t * a.K + k] * yv;
         }
-        const float v = acc + __ldcg(a.sig + t) * s_y[size_t(TK + t) * RBc + r];
+        const float v = acc + s_sig[t] * s_y[size_t(TK + t) * RBc + r];
         const uint16_t ob = f32_to_bf16(v);
         a.out[size_t(t) * a.H + o] = ob;
         if (a.resid) a.resid[size_t(t) * a.H + o] += __uint_as_float(uint32_t(ob) << 16);
@@ -596,6 +882,8 @@ __global__ void __launch_bounds__(384, 1) k_down(DownLaunch a) {
 
 // --------------------------------------------------------------- RMSNorm
 __global__ void k_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x) {
+    pdl_launch();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -618,54 +906,113 @@ __global__ void k_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x) 
 }
 
 // -------------------------------------------------------------- launchers
-template <int MC, int RB>
-static cudaError_t route_mc(const RouteLaunch& a, cudaStream_t s, int grid) {
-    // 8 warps x E logits (<= 32 KB): within the default dynamic limit
-    const size_t dyn = size_t(8) * a.E * sizeof(float);
-    k_route_decode<MC, RB><<<grid, 256, dyn, s>>>(a);
-    return cudaGetLastError();
+// Every launch carries the programmatic-stream-serialization attribute, so a
+// kernel may start while its predecessor on the stream drains; the kernels
+// themselves wait (griddepcontrol.wait) before touching anything the
+// predecessor writes.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem,
+                              cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename K>
+static cudaError_t allow_smem(K kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
 }
 
 cudaError_t launch_route_decode(const RouteLaunch& a, cudaStream_t s) {
     const Dev d = device_info();
-    const int grid = d.sms;
     const int mc = (a.H + 1023) / 1024;
-    if (mc <= 1) return route_mc<1, 4>(a, s, grid);
-    if (mc <= 2) return route_mc<2, 4>(a, s, grid);
-    return route_mc<4, 2>(a, s, grid);
+    if (mc <= 1) return launch_pdl(k_route<1, 4>, d.sms, 256, 0, s, a);
+    if (mc <= 2) return launch_pdl(k_route<2, 4>, d.sms, 256, 0, s, a);
+    return launch_pdl(k_route<4, 2>, d.sms, 256, 0, s, a);
 }
 
-cudaError_t launch_gate_up_decode(const GuLaunch& a, cudaStream_t s) {
+cudaError_t launch_select(const SelectLaunch& a, cudaStream_t s) {
+    const size_t dyn = size_t(8) * (a.E + 16) * sizeof(float);     // <= 33 KB
+    return launch_pdl(k_select, 1, 256, dyn, s, a);
+}
+
+int gate_up_stages(int H) {
+    const size_t stage = size_t(kGuRowPairs) * 2 * (size_t(H) / 2 + size_t(H) / 16);
+    int S = int(kGuRingBytes / stage);
+    return S < kGuMaxStages ? S : kGuMaxStages;
+}
+
+cudaError_t launch_gate_up_decode(GuLaunch a, cudaStream_t s) {
     const Dev d = device_info();
     const int mc = (a.H + 1023) / 1024;
-    if (mc <= 1)
-        k_gate_up<1, 4><<<d.sms, 256, 0, s>>>(a);
-    else if (mc <= 2)
-        k_gate_up<2, 4><<<d.sms, 256, 0, s>>>(a);
-    else
-        k_gate_up<4, 2><<<d.sms, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    a.stages = gate_up_stages(a.H);
+    const size_t stage = size_t(kGuRowPairs) * 2 * (size_t(a.H) / 2 + size_t(a.H) / 16);
+    size_t dyn = size_t(a.stages) * stage;
+    const size_t sel = size_t(kGuConsumers + 1) * (a.E + 16) * sizeof(float);
+    if (dyn < sel) dyn = sel;
+    cudaError_t err;
+    if (mc <= 1) {
+        if ((err = allow_smem(k_gate_up<1>, dyn)) != cudaSuccess) return err;
+        return launch_pdl(k_gate_up<1>, d.sms, kGuThreads, dyn, s, a);
+    }
+    if (mc <= 2) {
+        if ((err = allow_smem(k_gate_up<2>, dyn)) != cudaSuccess) return err;
+        return launch_pdl(k_gate_up<2>, d.sms, kGuThreads, dyn, s, a);
+    }
+    if ((err = allow_smem(k_gate_up<4>, dyn)) != cudaSuccess) return err;
+    return launch_pdl(k_gate_up<4>, d.sms, kGuThreads, dyn, s, a);
 }
 
-cudaError_t launch_down_decode(const DownLaunch& a, cudaStream_t s) {
+cudaError_t launch_down_decode(DownLaunch a, cudaStream_t s) {
     const int grid = (a.H + kDownRowsPerCta - 1) / kDownRowsPerCta;
-    // (T*K + T) slots x 14 rows of fp32 (<= 30 KB): within the default dynamic limit
-    const size_t dyn = size_t(a.T * a.K + a.T) * kDownRowsPerCta * sizeof(float);
-    k_down<<<grid, 384, dyn, s>>>(a);
-    return cudaGetLastError();
+    const int len = a.I > a.Is ? a.I : a.Is;
+    const size_t stage = size_t(kDownRowsPerCta) * (size_t(len) / 2 + size_t(len) / 16);
+    // A multiple of the consumer warps: unit u goes to warp u % kDnConsumers
+    // and slot u % S, so every round of a slot belongs to one warp and its
+    // parity waits never run ahead of the slot's phase.
+    int S = int(kDnRingBytes / (stage * kDnConsumers)) * kDnConsumers;
+    if (S < kDnConsumers) S = kDnConsumers;
+    a.stages = S < kDnMaxStages ? S : (kDnMaxStages / kDnConsumers) * kDnConsumers;
+    const size_t dyn = size_t(a.stages) * stage +
+                       size_t(a.T * a.K + a.T) * kDownRowsPerCta * sizeof(float);
+    // rows per lane: kDownRowsPerCta rows over 32 / (len / 32) row groups
+    const int rpw = 1024 / len;
+    const int mr = (kDownRowsPerCta + rpw - 1) / rpw;
+    cudaError_t err;
+#define STRATA_DOWN(MRV)                                                        \
+    if ((err = allow_smem(k_down<MRV>, dyn)) != cudaSuccess) return err;        \
+    return launch_pdl(k_down<MRV>, grid, kDnThreads, dyn, s, a)
+    if (mr <= 1) { STRATA_DOWN(1); }
+    if (mr <= 2) { STRATA_DOWN(2); }
+    if (mr <= 4) { STRATA_DOWN(4); }
+    if (mr <= 8) { STRATA_DOWN(8); }
+    STRATA_DOWN(16);
+#undef STRATA_DOWN
+}
+
+cudaError_t launch_plan(const int32_t* offsets, const int32_t* perm, int T, int K, int E,
+                        int32_t* plan, uint32_t* err, cudaStream_t s) {
+    return launch_pdl(k_plan, 1, 256, 0, s, offsets, perm, T, K, E, plan, err);
 }
 
 cudaError_t launch_permute_small(const int32_t* ids, int T, int K, int E, int32_t* counts,
                                  int32_t* offsets, int32_t* perm, int32_t* inv, uint32_t* err,
                                  cudaStream_t s) {
-    k_permute_small<<<1, 256, 0, s>>>(ids, T, K, E, counts, offsets, perm, inv, err);
-    return cudaGetLastError();
+    return launch_pdl(k_permute_small, 1, 256, 0, s, ids, T, K, E, counts, offsets, perm, inv,
+                      err);
 }
 
 cudaError_t launch_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x, cudaStream_t s) {
     const int warps = 8;
-    k_rmsnorm<<<(T + warps - 1) / warps, warps * 32, 0, s>>>(r, T, H, eps, x);
-    return cudaGetLastError();
+    return launch_pdl(k_rmsnorm, (T + warps - 1) / warps, warps * 32, 0, s, r, T, H, eps, x);
 }
 
 }  // namespace strata

@@ -12,14 +12,19 @@ namespace strata {
 constexpr int kDecodeMaxTokens = 32;
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
-constexpr int kDownRowsPerCta = 14;
+constexpr int kDownRowsPerCta = 16;
+// shared-memory rings of the decode expert kernels
+constexpr int kGuMaxStages = 8;
+constexpr size_t kGuRingBytes = 147456;   // 4 stages of 16 gate/up row pairs at H = 2048
+constexpr int kDnMaxStages = 24;
+constexpr size_t kDnRingBytes = 114688;
+// plan: [0] touched experts, header pad, then e[E], off[E], cnt[E], tok[T*K]
+constexpr int kPlanHeader = 4;
 
 // Byte offsets of the workspace regions for a call with T tokens.  Every
 // region starts on a 256-byte boundary; the control block is at 0.
 struct WsLayout {
-    size_t ctl, logits, ids, w, sig, counts, offsets, perm, inv, h, hs, x, out, total;
-    // prefill (T > kDecodeMaxTokens)
-    size_t tiles, xf16, hf16, y, shy;
+    size_t ctl, logits, ids, w, sig, counts, offsets, perm, inv, plan, h, hs, x, out, total;
 };
 
 WsLayout ws_layout(const strata_moe_dims& d, int T);
@@ -35,49 +40,60 @@ struct RouteLaunch {
     const uint16_t* x;
     float* logits;                    // ws [T][E+1]
     const uint8_t* shq; const uint16_t* shs; float* hs; int Is; int do_shared;
-    int do_select;
-    int32_t* ids; float* w; float* sig;                 // ws copies
-    int32_t* ids_user; float* w_user; float* sig_user; float* logits_user;
-    const int32_t* ids_in; const float* w_in;           // forced routing
-    int do_permute;
-    int32_t* counts; int32_t* offsets; int32_t* perm; int32_t* inv;
-    void* ctl;
+    int do_select;                    // 0: only the shared-gate row (forced routing)
     int T, H, E, K;
 };
 cudaError_t launch_route_decode(const RouteLaunch& a, cudaStream_t s);
 
+struct SelectLaunch {
+    const float* logits;
+    int32_t* ids; float* w; float* sig; float* logits_out;
+    uint32_t* err;
+    int T, E, K;
+};
+cudaError_t launch_select(const SelectLaunch& a, cudaStream_t s);
+
+enum GuMode { kGuRoute = 0, kGuPlan = 1, kGuShared = 2 };
 struct GuLaunch {
     const uint8_t* q; const uint16_t* sc;
     const uint16_t* x;
-    const int32_t* offsets; const int32_t* perm;
+    // kGuRoute: routing from logits (or forced ids/w), published by CTA 0
+    const float* logits;
+    const int32_t* forced_ids; const float* forced_w;
+    int32_t* ids; float* w; float* sig;
+    int32_t* ids_user; float* w_user; float* sig_user;
+    int32_t* counts; int32_t* offsets; int32_t* perm; int32_t* inv; int32_t* plan_out;
+    // kGuPlan: plan built by k_plan
+    const int32_t* plan;
     float* h;
     uint32_t* err;
     int T, H, I, E, K;
-    int shared;
+    int mode;
+    int stages;                       // set by the launcher
 };
-cudaError_t launch_gate_up_decode(const GuLaunch& a, cudaStream_t s);
+cudaError_t launch_gate_up_decode(GuLaunch a, cudaStream_t s);
 
 enum DownMode { kDownFused = 0, kDownSlots = 1, kDownCombine = 2 };
 struct DownLaunch {
     const uint8_t* q; const uint16_t* sc;
     const uint8_t* shq; const uint16_t* shs;
     const float* h; const float* hs;
-    const int32_t* offsets; const int32_t* inv;
+    const int32_t* plan; const int32_t* inv;
     const float* w; const float* sig;
     const uint16_t* y_in; uint16_t* y_out;
     uint16_t* out; float* resid;
     uint32_t* err;
     int T, H, I, Is, E, K;
     int mode;
+    int stages;                       // set by the launcher
 };
-cudaError_t launch_down_decode(const DownLaunch& a, cudaStream_t s);
+cudaError_t launch_down_decode(DownLaunch a, cudaStream_t s);
 
-cudaError_t launch_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x, cudaStream_t s);
-
-}  // namespace strata
-
-namespace strata {
+cudaError_t launch_plan(const int32_t* offsets, const int32_t* perm, int T, int K, int E,
+                        int32_t* plan, uint32_t* err, cudaStream_t s);
 cudaError_t launch_permute_small(const int32_t* ids, int T, int K, int E, int32_t* counts,
                                  int32_t* offsets, int32_t* perm, int32_t* inv, uint32_t* err,
                                  cudaStream_t s);
+cudaError_t launch_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x, cudaStream_t s);
+
 }  // namespace strata

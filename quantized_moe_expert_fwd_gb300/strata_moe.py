@@ -73,6 +73,9 @@ def load() -> ctypes.CDLL:
             "moe_layer_forward": (I32, [D, L, P, I32, P, P, P, P, P, SZ, P]),
             "moe_layer_forward_routed": (I32, [D, L, P, I32, P, P, P, P, SZ, P]),
             "moe_block_forward": (I32, [D, L, P, I32, ctypes.c_float, P, P, P, P, P, SZ, P]),
+            "moe_decode_route": (I32, [D, L, P, I32, I32, P, SZ, P]),
+            "moe_decode_gate_up": (I32, [D, L, P, I32, P, P, P, P, P, P, SZ, P]),
+            "moe_decode_down_combine": (I32, [D, L, I32, P, P, P, SZ, P]),
             "moe_get_device_status": (I32, [P, P]),
             "strata_status_str": (ctypes.c_char_p, [I32]),
         }
@@ -87,7 +90,8 @@ def load() -> ctypes.CDLL:
 EXPORTED = ("moe_workspace_bytes", "moe_decode_max_tokens", "moe_rmsnorm", "moe_route",
             "moe_permute", "moe_expert_gate_up", "moe_expert_down", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_routed",
-            "moe_block_forward", "moe_get_device_status", "strata_status_str")
+            "moe_block_forward", "moe_decode_route", "moe_decode_gate_up",
+            "moe_decode_down_combine", "moe_get_device_status", "strata_status_str")
 
 
 # ---------------------------------------------------------------- helpers
@@ -236,6 +240,29 @@ def moe_block_forward(dims, layer: DeviceLayer, resid, ws, eps: float = 1e-6, id
     _check("moe_block_forward", load().moe_block_forward(
         ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(resid), resid.shape[0],
         ctypes.c_float(eps), _ptr(ids), _ptr(weights), _ptr(x_out), _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_decode_route(dims, layer: DeviceLayer, x, ws, forced: bool = False, stream=None):
+    d = dims_struct(dims)
+    _check("moe_decode_route", load().moe_decode_route(
+        ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(x), x.shape[0], int(bool(forced)),
+        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_decode_gate_up(dims, layer: DeviceLayer, x, ws, forced_ids=None, forced_weights=None,
+                       ids=None, weights=None, shared_gate=None, stream=None):
+    d = dims_struct(dims)
+    _check("moe_decode_gate_up", load().moe_decode_gate_up(
+        ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(x), x.shape[0], _ptr(forced_ids),
+        _ptr(forced_weights), _ptr(ids), _ptr(weights), _ptr(shared_gate), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_decode_down_combine(dims, layer: DeviceLayer, T: int, out, ws, resid=None, stream=None):
+    d = dims_struct(dims)
+    _check("moe_decode_down_combine", load().moe_decode_down_combine(
+        ctypes.byref(d), ctypes.byref(layer.ptrs), int(T), _ptr(out), _ptr(resid), _ptr(ws),
         ws.numel(), _stream(stream)))
 
 

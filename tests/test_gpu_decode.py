@@ -50,6 +50,7 @@ def gpu_layer(dims, dl, xb, forced=None):
     else:
         q.moe_layer_forward_routed(dims, dl, x, G.i32(forced[0]), G.f32(forced[1]), out, ws)
     torch.cuda.synchronize()
+    res["where"] = ws[:32].cpu().numpy().view(np.uint32)[1:8].tolist()
     res["status"] = q.moe_get_device_status(ws)
     res["out"] = G.bf16_to_np(out)
     return res
@@ -58,7 +59,7 @@ def gpu_layer(dims, dl, xb, forced=None):
 def check_layer(dims, planes, dl, xb, what):
     ref = oracle.moe_forward(dims, planes, xb)
     got = gpu_layer(dims, dl, xb)
-    assert got["status"] == q.STRATA_OK
+    assert got["status"] == q.STRATA_OK, (what, got["status"], got["where"])
     clear = G.clear_tokens(ref["gap"])
     for t in clear:
         assert np.array_equal(got["ids"][t], ref["ids"][t]), (what, t)
@@ -288,3 +289,26 @@ def test_block_forward_stack(lib):
     torch.cuda.synchronize()
     if all(np.all(rec["gap"] >= 1e-3) for rec in recs):
         G.assert_close(resid.cpu().numpy(), rref, "4-block stack, own routing")
+
+
+def test_stage_calls_equal_layer_forward(lib):
+    """moe_decode_route -> moe_decode_gate_up -> moe_decode_down_combine is
+    moe_layer_forward, bit for bit, and publishes the same routing."""
+    dims = gen.QWEN
+    planes, dl = layer(dims, 8)
+    for T in (1, 9):
+        xb = qwen_x(T, 80 + T)
+        x = G.u16(xb)
+        ws = q.make_workspace(dims, T, G.dev())
+        out_a = torch.empty((T, dims.hidden), dtype=torch.int16, device=G.dev())
+        ids_a = torch.empty((T, dims.top_k), dtype=torch.int32, device=G.dev())
+        q.moe_layer_forward(dims, dl, x, out_a, ws, ids=ids_a)
+        out_b = torch.empty_like(out_a)
+        ids_b = torch.empty_like(ids_a)
+        ws2 = q.make_workspace(dims, T, G.dev())
+        q.moe_decode_route(dims, dl, x, ws2)
+        q.moe_decode_gate_up(dims, dl, x, ws2, ids=ids_b)
+        q.moe_decode_down_combine(dims, dl, T, out_b, ws2)
+        torch.cuda.synchronize()
+        assert torch.equal(out_a, out_b) and torch.equal(ids_a, ids_b)
+        assert q.moe_get_device_status(ws2) == q.STRATA_OK
