@@ -242,6 +242,33 @@ STRATA_API strata_status moe_decode_down_combine(const strata_moe_dims* dims,
                                                  void* out_dev, float* resid_dev, void* ws_dev,
                                                  size_t ws_bytes, void* stream);
 
+/* moe_layer_forward without a caller-supplied workspace.  The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory -- a plugin whose host framework owns every device allocation and
+ * hands it only inputs and outputs, or a serving path that must not call
+ * cudaMalloc.  The workspace is a fixed 2 MiB array inside the library: every
+ * GPU that loads the library holds it until the process exits, and every call
+ * of this function on a device uses the same array.
+ *   - Limits: T <= moe_decode_max_tokens() and moe_workspace_bytes(dims, T)
+ *     <= 2 MiB (every decode T of the 2048-hidden, 256-expert, top-8 shape
+ *     fits); a larger request returns STRATA_EINVAL with nothing launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.  No call allocates or frees anything.
+ *   - Calls that may overlap on the GPU (several streams, or several host
+ *     threads on one device) race on the shared array and give wrong results:
+ *     serialise them, or use moe_layer_forward with one workspace each.
+ *   - Device-side checks latch into the array's own error word, which each
+ *     call clears first and this call cannot report; use moe_layer_forward and
+ *     moe_get_device_status where those checks matter.
+ * Arguments as moe_layer_forward. */
+STRATA_API strata_status moe_layer_forward_static(const strata_moe_dims* dims,
+                                                  const strata_moe_layer* layer,
+                                                  const void* x_dev, int32_t T,
+                                                  int32_t* ids_dev, float* weights_dev,
+                                                  float* shared_gate_dev, void* out_dev,
+                                                  void* stream);
+
 /* Synchronises `stream`, returns the status latched in the workspace's error
  * word (STRATA_OK when none) and clears the word.  For tests and debugging;
  * it is the one call that synchronises. */

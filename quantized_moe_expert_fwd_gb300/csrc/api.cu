@@ -2,6 +2,7 @@
 // dispatch to the decode (GEMV) or prefill (tcgen05 GEMM) kernels.
 #include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -524,3 +525,56 @@ const char* strata_status_str(strata_status s) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// A workspace that lives inside the library, for callers that cannot allocate
+// device memory: a plugin whose host framework owns every device allocation
+// and hands the plugin only its inputs and outputs, or an engine that must
+// not call cudaMalloc (which may synchronise the device) on its serving path.
+// It is one fixed 2 MiB array per device that loads the library, kept until
+// the process exits, shared by every call of moe_layer_forward_static.
+
+namespace {
+
+constexpr size_t kStaticWsBytes = size_t(2) << 20;
+static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+// The array's device address, looked up once per device with that device
+// current (host code may not use the symbol itself as a device pointer).
+void* static_ws_address() {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+
+extern "C" strata_status moe_layer_forward_static(const strata_moe_dims* dims,
+                                                  const strata_moe_layer* layer,
+                                                  const void* x_dev, int32_t T, int32_t* ids_dev,
+                                                  float* weights_dev, float* shared_gate_dev,
+                                                  void* out_dev, void* stream) {
+    if (!dims_ok(dims) || T < 0 || !layer_ok(layer, kRouter | kRouted | kShared))
+        return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(x_dev) || !opt4(ids_dev) || !opt4(weights_dev) || !opt4(shared_gate_dev) ||
+        !al16(out_dev))
+        return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens || ws_layout(*dims, T).total > kStaticWsBytes) return STRATA_EINVAL;
+    void* ws = static_ws_address();
+    if (ws == nullptr) return STRATA_ECUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the error word must start at zero; every other region is written
+    // before it is read
+    if (cudaMemsetAsync(ws, 0, sizeof(Ctl), s) != cudaSuccess) return STRATA_ECUDA;
+    return decode_layer(dims, layer, x_dev, T, nullptr, nullptr, ids_dev, weights_dev,
+                        shared_gate_dev, out_dev, nullptr, ws, s);
+}

@@ -76,6 +76,7 @@ def load() -> ctypes.CDLL:
             "moe_decode_route": (I32, [D, L, P, I32, I32, P, SZ, P]),
             "moe_decode_gate_up": (I32, [D, L, P, I32, P, P, P, P, P, P, SZ, P]),
             "moe_decode_down_combine": (I32, [D, L, I32, P, P, P, SZ, P]),
+            "moe_layer_forward_static": (I32, [D, L, P, I32, P, P, P, P, P]),
             "moe_get_device_status": (I32, [P, P]),
             "strata_status_str": (ctypes.c_char_p, [I32]),
         }
@@ -91,7 +92,8 @@ EXPORTED = ("moe_workspace_bytes", "moe_decode_max_tokens", "moe_rmsnorm", "moe_
             "moe_permute", "moe_expert_gate_up", "moe_expert_down", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_routed",
             "moe_block_forward", "moe_decode_route", "moe_decode_gate_up",
-            "moe_decode_down_combine", "moe_get_device_status", "strata_status_str")
+            "moe_decode_down_combine", "moe_layer_forward_static", "moe_get_device_status",
+            "strata_status_str")
 
 
 # ---------------------------------------------------------------- helpers
@@ -264,6 +266,16 @@ def moe_decode_down_combine(dims, layer: DeviceLayer, T: int, out, ws, resid=Non
     _check("moe_decode_down_combine", load().moe_decode_down_combine(
         ctypes.byref(d), ctypes.byref(layer.ptrs), int(T), _ptr(out), _ptr(resid), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def moe_layer_forward_static(dims, layer: DeviceLayer, x, out, ids=None, weights=None,
+                             shared_gate=None, stream=None):
+    """moe_layer_forward on the library's own fixed workspace (no caller
+    allocation); see include/strata_moe.h for its limits."""
+    d = dims_struct(dims)
+    _check("moe_layer_forward_static", load().moe_layer_forward_static(
+        ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(x), x.shape[0], _ptr(ids),
+        _ptr(weights), _ptr(shared_gate), _ptr(out), _stream(stream)))
 
 
 def moe_get_device_status(ws, stream=None) -> int:
