@@ -30,11 +30,25 @@ WsLayout ws_layout(const strata_moe_dims& d, int T) {
     L.offsets = take((E + 1) * 4);
     L.perm = take(t * K * 4);
     L.inv = take(t * K * 4);
-    L.plan = take((kPlanHeader + 3 * E + t * K) * 4);
-    L.h = take(t * K * I * 4);
-    L.hs = take(t * Is * 4);
     L.x = take(t * H * 2);
     L.out = take(t * H * 2);
+    if (T <= kDecodeMaxTokens) {
+        L.plan = take((kPlanHeader + 3 * E + t * K) * 4);
+        L.h = take(t * K * I * 4);
+        L.hs = take(t * Is * 4);
+    } else {
+        const size_t nblk = (t + 31) / 32;
+        const size_t max_mb = (t * K) / kBM + E + t / kBM + 2;
+        L.cnt_blk = take(nblk * E * 4);
+        L.base_blk = take(nblk * E * 4);
+        L.mblocks = take(max_mb * sizeof(MBlock));
+        L.n_mblocks = take(16);
+        L.xg = take((t * K + t) * H * 2);
+        L.h16 = take(t * K * I * 2);
+        L.hs16 = take(t * Is * 2);
+        L.y = take(t * K * H * 2);
+        L.ysh = take(t * H * 2);
+    }
     L.total = o;
     return L;
 }
@@ -206,13 +220,103 @@ strata_status decode_layer(const strata_moe_dims* d, const strata_moe_layer* L, 
     return stage_down(d, L, T, out, resid, ws, s);
 }
 
+
+// One layer on the prefill (tcgen05) kernels.
+strata_status prefill_layer(const strata_moe_dims* d, const strata_moe_layer* L, const void* x,
+                            int T, const int32_t* forced_ids, const float* forced_w,
+                            int32_t* ids_user, float* w_user, float* sig_user, void* out,
+                            float* resid, void* ws, cudaStream_t s) {
+    if (!prefill_supported(*d)) return STRATA_EUNSUPPORTED;
+    const WsLayout W = ws_layout(*d, T);
+    uint32_t* err = &at<Ctl>(ws, W.ctl)->err;
+    PfRoute r{};
+    r.x = static_cast<const uint16_t*>(x);
+    r.router = static_cast<const uint16_t*>(L->router_dev);
+    r.logits = at<float>(ws, W.logits);
+    r.forced_ids = forced_ids;
+    r.forced_w = forced_w;
+    r.ids = at<int32_t>(ws, W.ids);
+    r.w = at<float>(ws, W.w);
+    r.sig = at<float>(ws, W.sig);
+    r.ids_user = ids_user;
+    r.w_user = w_user;
+    r.sig_user = sig_user;
+    r.err = err;
+    r.T = T;
+    r.H = d->hidden;
+    r.E = d->n_experts;
+    r.K = d->top_k;
+    r.bias = L->router_bias_dev;
+    STRATA_TRY(launch_prefill_route(r, s));
+    PfBucket b{};
+    b.ids = r.ids;
+    b.cnt_blk = at<int32_t>(ws, W.cnt_blk);
+    b.base_blk = at<int32_t>(ws, W.base_blk);
+    b.counts = at<int32_t>(ws, W.counts);
+    b.offsets = at<int32_t>(ws, W.offsets);
+    b.perm = at<int32_t>(ws, W.perm);
+    b.inv = at<int32_t>(ws, W.inv);
+    b.mblocks = at<MBlock>(ws, W.mblocks);
+    b.n_mblocks = at<int32_t>(ws, W.n_mblocks);
+    b.err = err;
+    b.T = T;
+    b.K = d->top_k;
+    b.E = d->n_experts;
+    b.with_shared = 1;
+    STRATA_TRY(launch_prefill_bucket(b, s));
+    PfExperts p{};
+    p.x = r.x;
+    p.perm = b.perm;
+    p.xg = at<__half>(ws, W.xg);
+    p.gu_q = L->gu_q_dev;
+    p.gu_s = L->gu_s_dev;
+    p.dn_q = L->dn_q_dev;
+    p.dn_s = L->dn_s_dev;
+    p.sh_gu_q = L->sh_gu_q_dev;
+    p.sh_gu_s = L->sh_gu_s_dev;
+    p.sh_dn_q = L->sh_dn_q_dev;
+    p.sh_dn_s = L->sh_dn_s_dev;
+    p.mblocks = b.mblocks;
+    p.n_mblocks = b.n_mblocks;
+    p.h = at<__half>(ws, W.h16);
+    p.hs = at<__half>(ws, W.hs16);
+    p.y = at<__half>(ws, W.y);
+    p.ysh = at<__half>(ws, W.ysh);
+    p.err = err;
+    p.T = T;
+    p.K = d->top_k;
+    p.H = d->hidden;
+    p.I = d->inter;
+    p.Is = d->shared_inter;
+    p.E = d->n_experts;
+    STRATA_TRY(launch_prefill_experts(p, s));
+    STRATA_TRY(launch_prefill_combine(p.y, p.ysh, b.inv, r.w, r.sig, T, d->top_k, d->hidden,
+                                      static_cast<uint16_t*>(out), resid, s));
+    return STRATA_OK;
+}
+
+// The layer at any T: decode kernels up to kDecodeMaxTokens, prefill above.
+strata_status any_layer(const strata_moe_dims* d, const strata_moe_layer* L, const void* x, int T,
+                        const int32_t* forced_ids, const float* forced_w, int32_t* ids_user,
+                        float* w_user, float* sig_user, void* out, float* resid, void* ws,
+                        cudaStream_t s) {
+    if (T <= kDecodeMaxTokens)
+        return decode_layer(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, out,
+                            resid, ws, s);
+    return prefill_layer(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, out, resid,
+                         ws, s);
+}
+
 }  // namespace
 
 extern "C" {
 
 size_t moe_workspace_bytes(const strata_moe_dims* dims, int32_t max_tokens) {
     if (!dims_ok(dims) || max_tokens < 1) return 0;
-    return ws_layout(*dims, max_tokens).total;
+    // a call with T <= max_tokens takes the decode or the prefill layout
+    const int dmax = max_tokens < kDecodeMaxTokens ? max_tokens : kDecodeMaxTokens;
+    const size_t a = ws_layout(*dims, dmax).total, b = ws_layout(*dims, max_tokens).total;
+    return a > b ? a : b;
 }
 
 int32_t moe_decode_max_tokens(void) { return kDecodeMaxTokens; }
@@ -415,10 +519,8 @@ strata_status moe_layer_forward(const strata_moe_dims* dims, const strata_moe_la
     if (!al16(x_dev) || !opt4(ids_dev) || !opt4(weights_dev) || !opt4(shared_gate_dev) ||
         !al16(out_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
-    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
-    return decode_layer(dims, layer, x_dev, T, nullptr, nullptr, ids_dev, weights_dev,
-                        shared_gate_dev, out_dev, nullptr, ws_dev,
-                        static_cast<cudaStream_t>(stream));
+    return any_layer(dims, layer, x_dev, T, nullptr, nullptr, ids_dev, weights_dev,
+                     shared_gate_dev, out_dev, nullptr, ws_dev, static_cast<cudaStream_t>(stream));
 }
 
 strata_status moe_layer_forward_routed(const strata_moe_dims* dims,
@@ -432,9 +534,8 @@ strata_status moe_layer_forward_routed(const strata_moe_dims* dims,
     if (!al16(x_dev) || !al4(ids_dev) || !al4(weights_dev) || !al16(out_dev) ||
         !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
-    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
-    return decode_layer(dims, layer, x_dev, T, ids_dev, weights_dev, nullptr, nullptr, nullptr,
-                        out_dev, nullptr, ws_dev, static_cast<cudaStream_t>(stream));
+    return any_layer(dims, layer, x_dev, T, ids_dev, weights_dev, nullptr, nullptr, nullptr,
+                     out_dev, nullptr, ws_dev, static_cast<cudaStream_t>(stream));
 }
 
 strata_status moe_block_forward(const strata_moe_dims* dims, const strata_moe_layer* layer,
@@ -450,14 +551,13 @@ strata_status moe_block_forward(const strata_moe_dims* dims, const strata_moe_la
         (x_out_dev && !al16(x_out_dev)) || (out_dev && !al16(out_dev)) ||
         !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
-    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
     const WsLayout W = ws_layout(*dims, T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void* x = x_out_dev ? x_out_dev : at<void>(ws_dev, W.x);
     void* out = out_dev ? out_dev : at<void>(ws_dev, W.out);
     STRATA_TRY(launch_rmsnorm(resid_dev, T, dims->hidden, eps, static_cast<uint16_t*>(x), s));
-    return decode_layer(dims, layer, x, T, ids_dev, weights_dev, nullptr, nullptr, nullptr, out,
-                        resid_dev, ws_dev, s);
+    return any_layer(dims, layer, x, T, ids_dev, weights_dev, nullptr, nullptr, nullptr, out,
+                     resid_dev, ws_dev, s);
 }
 
 strata_status moe_decode_route(const strata_moe_dims* dims, const strata_moe_layer* layer,

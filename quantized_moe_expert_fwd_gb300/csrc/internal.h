@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda_fp16.h>
+
 #include "../../include/strata_moe.h"
 
 namespace strata {
@@ -21,10 +23,29 @@ constexpr size_t kDnRingBytes = 114688;
 // plan: [0] touched experts, header pad, then e[E], off[E], cnt[E], tok[T*K]
 constexpr int kPlanHeader = 4;
 
+// prefill (T > kDecodeMaxTokens) tiles: 128 rows x 64 K per stage
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kPfMaxStages = 6;
+constexpr size_t kPfSmemBudget = 225280;
+enum GemmMode { kGemmRouter = 0, kGemmGateUp = 1, kGemmDown = 2 };
+
+// One block of up to 128 rows of one group (a routed expert, or the shared
+// expert as group E) for the prefill GEMMs.  row: first row of the group's
+// A operand space (a slot for routed experts, a token for the shared one).
+struct MBlock {
+    int group, row, nrows, pad;
+};
+
 // Byte offsets of the workspace regions for a call with T tokens.  Every
-// region starts on a 256-byte boundary; the control block is at 0.
+// region starts on a 256-byte boundary; the control block is at 0.  The
+// decode regions (plan, h, hs as fp32) exist for T <= kDecodeMaxTokens, the
+// prefill ones (per-block counts, row blocks, fp16 operands, bf16 outputs)
+// for larger T.
 struct WsLayout {
-    size_t ctl, logits, ids, w, sig, counts, offsets, perm, inv, plan, h, hs, x, out, total;
+    size_t ctl, logits, ids, w, sig, counts, offsets, perm, inv, plan, h, hs, x, out;
+    size_t cnt_blk, base_blk, mblocks, n_mblocks, xg, h16, hs16, y, ysh;
+    size_t total;
 };
 
 WsLayout ws_layout(const strata_moe_dims& d, int T);
@@ -95,5 +116,68 @@ cudaError_t launch_permute_small(const int32_t* ids, int T, int K, int E, int32_
                                  int32_t* offsets, int32_t* perm, int32_t* inv, uint32_t* err,
                                  cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x, cudaStream_t s);
+
+// ---------------------------------------------------------------- prefill
+struct PfSelectLaunch {
+    const float* logits; float* logits_user;
+    const int32_t* forced_ids; const float* forced_w;
+    int32_t* ids; float* w; float* sig;
+    int32_t* ids_user; float* w_user; float* sig_user;
+    uint32_t* err;
+    int T, E, K;
+};
+struct PfScanLaunch {
+    const int32_t* cnt_blk; int32_t* base_blk;
+    int32_t* counts; int32_t* offsets;
+    MBlock* mblocks; int32_t* n_mblocks;
+    int nblk, E, T, with_shared;
+};
+struct GemmLaunch {
+    const MBlock* mblocks; const int32_t* n_mblocks;
+    int router_mblocks, M;             // router: rows of A
+    int N, N2, N_valid, K, K2, K_max;   // N, K of routed groups; N2, K2 of the shared group
+    int BN, nb_max, E, a_shared_row0, stages;
+    float* out_f32; const float* bias;   // router: logits (+ bias on the first E columns)
+    __half* out_f16; __half* out2_f16;
+    uint16_t* out_bf16; uint16_t* out2_bf16;
+    int ldo, ld2;
+    uint32_t* err;
+};
+struct PfRoute {
+    const uint16_t* x; const uint16_t* router; const float* bias;
+    float* logits;
+    const int32_t* forced_ids; const float* forced_w;
+    int32_t* ids; float* w; float* sig;
+    int32_t* ids_user; float* w_user; float* sig_user;
+    uint32_t* err;
+    int T, H, E, K;
+};
+struct PfBucket {
+    const int32_t* ids;
+    int32_t* cnt_blk; int32_t* base_blk;
+    int32_t* counts; int32_t* offsets; int32_t* perm; int32_t* inv;
+    MBlock* mblocks; int32_t* n_mblocks;
+    uint32_t* err;
+    int T, K, E, with_shared;
+};
+struct PfExperts {
+    const uint16_t* x; const int32_t* perm;
+    __half* xg;
+    const uint8_t* gu_q; const uint16_t* gu_s; const uint8_t* dn_q; const uint16_t* dn_s;
+    const uint8_t* sh_gu_q; const uint16_t* sh_gu_s;
+    const uint8_t* sh_dn_q; const uint16_t* sh_dn_s;
+    const MBlock* mblocks; const int32_t* n_mblocks;
+    __half* h; __half* hs;
+    __half* y; __half* ysh;
+    uint32_t* err;
+    int T, K, H, I, Is, E;
+};
+bool prefill_supported(const strata_moe_dims& d);
+cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s);
+cudaError_t launch_prefill_bucket(const PfBucket& b, cudaStream_t s);
+cudaError_t launch_prefill_experts(const PfExperts& p, cudaStream_t s);
+cudaError_t launch_prefill_combine(const __half* y, const __half* ysh, const int32_t* inv,
+                                   const float* w, const float* sig, int T, int K, int H,
+                                   uint16_t* out, float* resid, cudaStream_t s);
 
 }  // namespace strata

@@ -2,7 +2,12 @@
 near-tie rule.
 
 Tolerance of floating outputs (bf16 from the GPU against the fp32 oracle):
-relative L2 <= 5e-3 and max |diff| <= 2e-2 * rms(reference).
+relative L2 <= 5e-3 of the raw difference, and for every element
+|got - ref| - half a bf16 ulp of max(|got|, |ref|) <= 2e-2 * rms(ref): the
+max-abs bar bounds the error beyond the output format's own rounding.  Read
+literally it cannot be met by any bf16 output whose largest elements exceed
+about 5 rms: rounding the exact (float64) result of a Qwen-shaped layer at
+T=100 to bf16 alone gives max |diff| = 2.01e-2 * rms.
 Near ties: a token whose oracle K-th and (K+1)-th logits differ by less than
 1e-4 may be routed differently by an fp32 sum taken in another order; its ids
 are not compared, and its floats are checked on a run with the oracle's
@@ -45,10 +50,29 @@ def err_stats(got, want):
     return rel, mx
 
 
+def bf16_half_ulp(v):
+    """Half the spacing of bf16 numbers at |v| (8 significant bits)."""
+    a = np.maximum(np.abs(np.asarray(v, dtype=np.float64)), np.finfo(np.float32).tiny)
+    return np.exp2(np.floor(np.log2(a)) - 8.0)
+
+
+def excess_stats(got, want):
+    """max over elements of (|got - want| - half a bf16 ulp), over rms(want)."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    if want.size == 0:
+        return 0.0
+    rms = float(np.sqrt((want ** 2).mean()))
+    ex = np.abs(got - want) - bf16_half_ulp(np.maximum(np.abs(got), np.abs(want)))
+    return float(max(ex.max(), 0.0) / max(rms, 1e-30))
+
+
 def assert_close(got, want, what=""):
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     rel, mx = err_stats(got, want)
-    assert rel <= REL_L2 and mx <= MAX_ABS_RMS, f"{what}: rel_l2 {rel:.3e}, max_abs/rms {mx:.3e}"
+    ex = excess_stats(got, want)
+    assert rel <= REL_L2 and ex <= MAX_ABS_RMS, \
+        f"{what}: rel_l2 {rel:.3e}, max_abs/rms {mx:.3e}, beyond bf16 rounding {ex:.3e}"
     return rel, mx
 
 
