@@ -269,6 +269,19 @@ STRATA_API strata_status moe_layer_forward_static(const strata_moe_dims* dims,
                                                   float* shared_gate_dev, void* out_dev,
                                                   void* stream);
 
+/* Measurement: runs moe_layer_forward once with a CUDA event recorded after
+ * every kernel launch, synchronises `stream`, and writes each kernel's
+ * duration in microseconds to us[0..max_n) in launch order; *n_out gets the
+ * number of kernels.  The events serialise the kernels, so each duration is
+ * the kernel alone.  Order: decode (T <= moe_decode_max_tokens()): route,
+ * gate/up, down+combine; prefill: router GEMM, top-K, count, scan, scatter,
+ * gather, gate/up GEMM, down GEMM, combine. */
+STRATA_API strata_status moe_layer_profile(const strata_moe_dims* dims,
+                                           const strata_moe_layer* layer, const void* x_dev,
+                                           int32_t T, void* out_dev, void* ws_dev,
+                                           size_t ws_bytes, void* stream, float* us,
+                                           int32_t max_n, int32_t* n_out);
+
 /* Synchronises `stream`, returns the status latched in the workspace's error
  * word (STRATA_OK when none) and clears the word.  For tests and debugging;
  * it is the one call that synchronises. */

@@ -53,6 +53,21 @@ WsLayout ws_layout(const strata_moe_dims& d, int T) {
     return L;
 }
 
+// Events of moe_layer_profile, per host thread.
+struct Prof {
+    cudaEvent_t ev[64];
+    int n;
+};
+static thread_local Prof* t_prof = nullptr;
+
+void prof_after_launch(cudaStream_t s) {
+    Prof* p = t_prof;
+    if (p == nullptr || p->n >= 64) return;
+    if (cudaEventCreate(&p->ev[p->n]) != cudaSuccess) return;
+    cudaEventRecord(p->ev[p->n], s);
+    ++p->n;
+}
+
 Dev device_info() {
     static std::atomic<int> cache[64];
     int dev = 0;
@@ -597,6 +612,41 @@ strata_status moe_decode_down_combine(const strata_moe_dims* dims, const strata_
         return STRATA_EINVAL;
     return stage_down(dims, layer, T, out_dev, resid_dev, ws_dev,
                       static_cast<cudaStream_t>(stream));
+}
+
+
+strata_status moe_layer_profile(const strata_moe_dims* dims, const strata_moe_layer* layer,
+                                const void* x_dev, int32_t T, void* out_dev, void* ws_dev,
+                                size_t ws_bytes, void* stream, float* us, int32_t max_n,
+                                int32_t* n_out) {
+    if (!dims_ok(dims) || T < 1 || !layer_ok(layer, kRouter | kRouted | kShared) ||
+        !al16(x_dev) || !al16(out_dev) || us == nullptr || n_out == nullptr || max_n < 1 ||
+        !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Prof prof{};
+    cudaEvent_t start;
+    if (cudaEventCreate(&start) != cudaSuccess) return STRATA_ECUDA;
+    cudaEventRecord(start, s);
+    t_prof = &prof;
+    const strata_status st = any_layer(dims, layer, x_dev, T, nullptr, nullptr, nullptr, nullptr,
+                                       nullptr, out_dev, nullptr, ws_dev, s);
+    t_prof = nullptr;
+    strata_status rc = st;
+    if (cudaStreamSynchronize(s) != cudaSuccess) rc = STRATA_ECUDA;
+    int n = 0;
+    cudaEvent_t prev = start;
+    for (int i = 0; i < prof.n; ++i) {
+        float ms = 0.0f;
+        if (rc == STRATA_OK && cudaEventElapsedTime(&ms, prev, prof.ev[i]) != cudaSuccess)
+            rc = STRATA_ECUDA;
+        if (n < max_n) us[n++] = ms * 1000.0f;
+        prev = prof.ev[i];
+    }
+    for (int i = 0; i < prof.n; ++i) cudaEventDestroy(prof.ev[i]);
+    cudaEventDestroy(start);
+    *n_out = prof.n;
+    return rc;
 }
 
 strata_status moe_get_device_status(void* ws_dev, void* stream) {

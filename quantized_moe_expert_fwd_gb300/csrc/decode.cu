@@ -923,7 +923,9 @@ static cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, siz
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e == cudaSuccess) prof_after_launch(s);
+    return e;
 }
 
 template <typename K>

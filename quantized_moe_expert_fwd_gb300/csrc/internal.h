@@ -55,6 +55,10 @@ struct Dev {
 };
 Dev device_info();
 
+// Called after every kernel launch: when moe_layer_profile is running on
+// this host thread, records a CUDA event on the launch's stream.
+void prof_after_launch(cudaStream_t s);
+
 // -------------------------------------------------------------- launchers
 struct RouteLaunch {
     const uint16_t* router; const float* bias;

@@ -77,6 +77,7 @@ def load() -> ctypes.CDLL:
             "moe_decode_gate_up": (I32, [D, L, P, I32, P, P, P, P, P, P, SZ, P]),
             "moe_decode_down_combine": (I32, [D, L, I32, P, P, P, SZ, P]),
             "moe_layer_forward_static": (I32, [D, L, P, I32, P, P, P, P, P]),
+            "moe_layer_profile": (I32, [D, L, P, I32, P, P, SZ, P, P, I32, P]),
             "moe_get_device_status": (I32, [P, P]),
             "strata_status_str": (ctypes.c_char_p, [I32]),
         }
@@ -92,7 +93,8 @@ EXPORTED = ("moe_workspace_bytes", "moe_decode_max_tokens", "moe_rmsnorm", "moe_
             "moe_permute", "moe_expert_gate_up", "moe_expert_down", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_routed",
             "moe_block_forward", "moe_decode_route", "moe_decode_gate_up",
-            "moe_decode_down_combine", "moe_layer_forward_static", "moe_get_device_status",
+            "moe_decode_down_combine", "moe_layer_forward_static", "moe_layer_profile",
+            "moe_get_device_status",
             "strata_status_str")
 
 
@@ -276,6 +278,23 @@ def moe_layer_forward_static(dims, layer: DeviceLayer, x, out, ids=None, weights
     _check("moe_layer_forward_static", load().moe_layer_forward_static(
         ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(x), x.shape[0], _ptr(ids),
         _ptr(weights), _ptr(shared_gate), _ptr(out), _stream(stream)))
+
+
+PROFILE_DECODE = ("k_route", "k_gate_up", "k_down")
+PROFILE_PREFILL = ("router_gemm", "select", "count", "scan", "scatter", "gather",
+                   "gemm_gate_up", "gemm_down", "combine")
+
+
+def moe_layer_profile(dims, layer: DeviceLayer, x, out, ws, stream=None):
+    """Per-kernel durations (microseconds, launch order) of one layer forward."""
+    d = dims_struct(dims)
+    us = (ctypes.c_float * 64)()
+    n = ctypes.c_int32(0)
+    _check("moe_layer_profile", load().moe_layer_profile(
+        ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(x), x.shape[0], _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream), us, 64, ctypes.byref(n)))
+    names = PROFILE_DECODE if x.shape[0] <= moe_decode_max_tokens() else PROFILE_PREFILL
+    return {names[i] if i < len(names) else f"k{i}": float(us[i]) for i in range(n.value)}
 
 
 def moe_get_device_status(ws, stream=None) -> int:
