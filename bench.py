@@ -460,6 +460,132 @@ def run_strata(args, rank, world, local, ctl):
     return result, (dims, planes, xs, nl)
 
 
+def prefill_flops(d, T):
+    H, E, K, I, Is = d.hidden, d.n_experts, d.top_k, d.inter, d.shared_inter
+    routed = 2.0 * T * K * (2 * I * H + H * I)
+    shared = 2.0 * T * (2 * Is * H + H * Is)
+    router = 2.0 * T * (E + 1) * H
+    return routed + shared + router, 2.0 * (T * K * 2 * I * H + T * 2 * Is * H)
+
+
+def run_prefill(dev, reps=20, warmup=3):
+    """Prefill T=2048 through one Zipf-routed layer: time per layer (CUDA
+    graph), tokens/s, tensor-core FLOP rate, and the per-kernel split."""
+    import torch
+    import quantized_moe_expert_fwd_gb300 as q
+    cfg = gen.CONFIGS["prefill"]
+    dims, T = cfg.dims, cfg.tokens
+    planes = gen.draw_layer(dims, 0, bias=cfg.bias, alpha=cfg.alpha)
+    dl = q.DeviceLayer(planes, dev)
+    r = torch.from_numpy(gen.draw_tokens(dims, T, 0, cfg.token_kind)).to(dev)
+    x = torch.empty((T, dims.hidden), dtype=torch.int16, device=dev)
+    q.moe_rmsnorm(r, x)
+    out = torch.empty((T, dims.hidden), dtype=torch.int16, device=dev)
+    ws = q.make_workspace(dims, T, dev)
+    st = torch.cuda.Stream(dev)
+    with torch.cuda.stream(st):
+        q.moe_layer_forward(dims, dl, x, out, ws, stream=st)
+        st.synchronize()
+        if q.moe_get_device_status(ws, st) != q.STRATA_OK:
+            raise RuntimeError("prefill: device status")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            q.moe_layer_forward(dims, dl, x, out, ws, stream=st)
+        for _ in range(warmup):
+            g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            g.replay()
+        e1.record(st)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        prof = None
+        for _ in range(3):
+            prof = q.moe_layer_profile(dims, dl, x, out, ws, stream=st)
+    total, gu_flops = prefill_flops(dims, T)
+    _, bf16_peak, src = measured_peaks()
+    gu_us = prof["gemm_gate_up"]
+    return {
+        "workload": cfg.description,
+        "tokens": T,
+        "us_per_layer": us,
+        "tok_per_s": T / (us / 1e6),
+        "tflops": total / (us / 1e6) / 1e12,
+        "tc_frac_of_peak": total / (us / 1e6) / 1e12 / bf16_peak,
+        "peak_tflops": bf16_peak,
+        "peak_source": src,
+        "kernels_us": {k: round(v, 2) for k, v in prof.items()},
+        "gate_up_gemm": {"us": gu_us, "tflops": gu_flops / (gu_us / 1e6) / 1e12,
+                         "frac": gu_flops / (gu_us / 1e6) / 1e12 / bf16_peak},
+        "launches_per_layer": len(prof),
+    }
+
+
+def run_prefill_line(args, rank, world, local, ctl):
+    """The prefill workload as the primary line: value = prompt tokens/s
+    through one MoE layer at T=2048."""
+    import torch
+    import quantized_moe_expert_fwd_gb300 as q
+    q.build.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if args.profile:
+        # lean run for ncu: plain calls, no graphs, no oracle
+        cfg = gen.CONFIGS["prefill"]
+        dims, T = cfg.dims, cfg.tokens
+        dl = q.DeviceLayer(gen.draw_layer(dims, 0, bias=cfg.bias, alpha=cfg.alpha), dev)
+        r = torch.from_numpy(gen.draw_tokens(dims, T, 0, cfg.token_kind)).to(dev)
+        x = torch.empty((T, dims.hidden), dtype=torch.int16, device=dev)
+        q.moe_rmsnorm(r, x)
+        out = torch.empty((T, dims.hidden), dtype=torch.int16, device=dev)
+        ws = q.make_workspace(dims, T, dev)
+        for _ in range(args.warmup + args.steps):
+            q.moe_layer_forward(dims, dl, x, out, ws)
+        torch.cuda.synchronize()
+        return {"profile": True, "status": q.moe_get_device_status(ws)}
+    clocks = ClockSampler(local)
+    clocks.start()
+    pf = run_prefill(dev, reps=args.steps, warmup=args.warmup)
+    clocks.stop()
+    us = ctl.max(pf["us_per_layer"])
+    total, _ = prefill_flops(gen.CONFIGS["prefill"].dims, pf["tokens"])
+    hbm, peak, src = measured_peaks()
+    line = {
+        "metric": METRIC,
+        "value": pf["tokens"] * world / (us / 1e6),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": us / 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded random int4 weights and activations of the real shapes)",
+        "config": {"workload": pf["workload"], "tokens_per_call": pf["tokens"],
+                   "value_unit": "prompt tokens per second through one MoE layer",
+                   "l2": "inputs larger than L2: 455.8 MB of weights read per step",
+                   "arithmetic": "int4 weights dequantised to fp16 x fp16 activations on "
+                                 "tcgen05, fp32 accumulate"},
+        "roofline": {"kernel": "k_pf_gemm<gate/up>", "bound": "tensor",
+                     "achieved": pf["gate_up_gemm"]["tflops"], "peak": peak,
+                     "unit": "TFLOP/s", "frac": pf["gate_up_gemm"]["frac"],
+                     "peak_source": f"{src} bf16 (fp16 runs at the same rate), burst",
+                     "traffic": kernel_traffic("k_pf_gemm_gate_up"),
+                     "us_per_launch": pf["gate_up_gemm"]["us"]},
+        "tc_frac_whole_layer": pf["tc_frac_of_peak"],
+        "kernels_us": pf["kernels_us"],
+        "clocks": clocks.summary(),
+        "gpu_launches": args.steps * pf["launches_per_layer"],
+        "cpu_baseline": None,
+        "e2e": None,
+    }
+    return line
+
+
 def cpu_baseline_block(dims, planes, xs_dev, nl, budget):
     import torch
     xs = [xs_dev[0][li].cpu().numpy().view(np.uint16) for li in range(nl)]
@@ -527,12 +653,14 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["strata", "reference"], default="strata")
-    ap.add_argument("--workload", choices=["decode1", "decode16"], default="decode1")
+    ap.add_argument("--workload", choices=["decode1", "decode16", "prefill"], default="decode1")
     ap.add_argument("--variants", type=int, default=16)
     ap.add_argument("--layers", type=int, default=10)
     ap.add_argument("--profile", action="store_true",
                     help="lean run for ncu: no clock warm loop, stage timing, e2e or oracle")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="leave out the prefill (T=2048) block of the line")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -546,6 +674,14 @@ def main():
         return
 
     ctl = Control(world)
+    if args.workload == "prefill":
+        try:
+            print_line = run_prefill_line(args, rank, world, local, ctl)
+            if rank == 0 and print_line is not None:
+                print(json.dumps(print_line), flush=True)
+        finally:
+            ctl.close()
+        return
     try:
         result, extra = run_strata(args, rank, world, local, ctl)
         if extra is None:
