@@ -586,6 +586,105 @@ def run_prefill_line(args, rank, world, local, ctl):
     return line
 
 
+def run_stack_line(args, rank, world, local, ctl):
+    """One decode step of T tokens through the 40-layer residual MoE stack
+    (moe_block_forward x 40 in one CUDA graph): value = tokens/s through the
+    whole stack."""
+    import torch
+    import quantized_moe_expert_fwd_gb300 as q
+    q.build.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = gen.CONFIGS["stack"]
+    dims, T = cfg.dims, args.tokens
+    layers = []
+    for s in cfg.seeds:
+        layers.append(q.DeviceLayer(gen.draw_layer(dims, s), dev))
+    nvar = args.variants
+    r0s = [torch.from_numpy(gen.draw_tokens(dims, T, 5000 + v, "resid")).to(dev)
+           for v in range(nvar)]
+    resid = torch.empty((T, dims.hidden), dtype=torch.float32, device=dev)
+    ws = q.make_workspace(dims, T, dev)
+    st = torch.cuda.Stream(dev)
+    ids = torch.empty((T, dims.top_k), dtype=torch.int32, device=dev)
+
+    def step(v):
+        resid.copy_(r0s[v])
+        for dl in layers:
+            q.moe_block_forward(dims, dl, resid, ws, stream=st)
+
+    with torch.cuda.stream(st):
+        step(0)
+        st.synchronize()
+        if q.moe_get_device_status(ws, st) != q.STRATA_OK:
+            raise RuntimeError("stack: device status")
+        graphs = []
+        for v in range(nvar):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                step(v)
+            graphs.append(g)
+        for i in range(max(args.warmup, 3)):
+            graphs[i % nvar].replay()
+        st.synchronize()
+        clocks = ClockSampler(local)
+        clocks.start()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        ctl.barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(st)
+        for i in range(args.steps):
+            graphs[i % nvar].replay()
+        e1.record(st)
+        e1.synchronize()
+        ctl.barrier()
+        clocks.stop()
+        ms = ctl.max(e0.elapsed_time(e1)) / args.steps
+        # touched experts per layer (routing of variant 0 through the stack)
+        resid.copy_(r0s[0])
+        touched = 0
+        xo = torch.empty((T, dims.hidden), dtype=torch.int16, device=dev)
+        for dl in layers:
+            q.moe_block_forward(dims, dl, resid, ws, x_out=xo, stream=st)
+            q.moe_route(dims, dl, xo, ids, torch.empty((T, dims.top_k), device=dev),
+                        torch.empty((T,), device=dev), ws, stream=st)
+            st.synchronize()
+            touched += len(np.unique(ids.cpu().numpy()))
+    nl = len(layers)
+    step_bytes = touched * expert_bytes(dims) + nl * (shared_bytes(dims) + router_bytes(dims))
+    gbs = step_bytes / (ms / 1e3) / 1e9
+    hbm, _, src = measured_peaks()
+    launches = nl * (4 if T <= 32 else 11)
+    return {
+        "metric": METRIC,
+        "value": T * world / (ms / 1e3),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded random int4 weights and activations of the real shapes)",
+        "config": {"workload": f"{cfg.description}; T={T}", "tokens_per_call": T,
+                   "layers_per_step": nl,
+                   "value_unit": "tokens per second through the whole 40-layer stack",
+                   "l2": "inputs larger than L2: 18.2 GB of weights resident, "
+                         f"{nvar} token variants rotating"},
+        "expert_weight_gbs": gbs,
+        "expert_weight_frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+        "hbm_frac_of_measured": gbs / hbm,
+        "us_per_layer": ms * 1e3 / nl,
+        "clocks": clocks.summary(),
+        "gpu_launches": args.steps * launches,
+        "cpu_baseline": None,
+        "e2e": None,
+    }
+
+
 def cpu_baseline_block(dims, planes, xs_dev, nl, budget):
     import torch
     xs = [xs_dev[0][li].cpu().numpy().view(np.uint16) for li in range(nl)]
@@ -653,7 +752,9 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["strata", "reference"], default="strata")
-    ap.add_argument("--workload", choices=["decode1", "decode16", "prefill"], default="decode1")
+    ap.add_argument("--workload", choices=["decode1", "decode16", "prefill", "stack"],
+                    default="decode1")
+    ap.add_argument("--tokens", type=int, default=1, help="stack workload: tokens per step")
     ap.add_argument("--variants", type=int, default=16)
     ap.add_argument("--layers", type=int, default=10)
     ap.add_argument("--profile", action="store_true",
@@ -674,6 +775,14 @@ def main():
         return
 
     ctl = Control(world)
+    if args.workload == "stack":
+        try:
+            line = run_stack_line(args, rank, world, local, ctl)
+            if rank == 0:
+                print(json.dumps(line), flush=True)
+        finally:
+            ctl.close()
+        return
     if args.workload == "prefill":
         try:
             print_line = run_prefill_line(args, rank, world, local, ctl)
