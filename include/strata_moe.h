@@ -149,7 +149,12 @@ STRATA_API strata_status moe_permute(const strata_moe_dims* dims, const int32_t*
  * For each slot s of expert e (offsets) and token t = perm[s] / K:
  *   g_i = sum_h x[t][h] Wg[e][i][h],  u_i = sum_h x[t][h] Wu[e][i][h]
  *   h[s][i] = g_i / (1 + exp(-g_i)) * u_i
- * with W = fp16 scale * (nibble - 8).  h_dev fp32 [T*K][I] (out). */
+ * with W = fp16 scale * (nibble - 8).  h_dev fp32 [T*K][I] (out).
+ * Above moe_decode_max_tokens() the product runs on the tensor cores with
+ * fp16 operands (x rounded to fp16) and fp32 accumulation; at and below it,
+ * on the CUDA cores in fp32.  The same holds for the down product and the
+ * shared expert below (h rounded to fp16 there).  An expert whose offsets
+ * leave [0, T*K] is skipped and latches STRATA_EBADROUTE. */
 STRATA_API strata_status moe_expert_gate_up(const strata_moe_dims* dims, const strata_moe_layer* layer,
                                  const void* x_dev, int32_t T, const int32_t* offsets_dev,
                                  const int32_t* perm_dev, float* h_dev, void* ws_dev,

@@ -304,9 +304,81 @@ strata_status prefill_layer(const strata_moe_dims* d, const strata_moe_layer* L,
     p.I = d->inter;
     p.Is = d->shared_inter;
     p.E = d->n_experts;
+    p.routed = 1;
+    p.shared = 1;
+    p.xg_rows = T * d->top_k + T;
+    p.xg_shared_row0 = T * d->top_k;
     STRATA_TRY(launch_prefill_experts(p, s));
-    STRATA_TRY(launch_prefill_combine(p.y, p.ysh, b.inv, r.w, r.sig, T, d->top_k, d->hidden,
-                                      static_cast<uint16_t*>(out), resid, s));
+    STRATA_TRY(launch_prefill_combine(p.y, nullptr, p.ysh, b.inv, r.w, r.sig, T, d->top_k,
+                                      d->hidden, static_cast<uint16_t*>(out), resid, s));
+    return STRATA_OK;
+}
+
+// Prefill operands of a stage-wise call at T > kDecodeMaxTokens: the
+// workspace's block list, fp16 operands and shared-expert outputs.
+PfExperts pf_stage(const strata_moe_dims* d, const strata_moe_layer* L, int T, void* ws) {
+    const WsLayout W = ws_layout(*d, T);
+    PfExperts p{};
+    p.gu_q = L->gu_q_dev;
+    p.gu_s = L->gu_s_dev;
+    p.dn_q = L->dn_q_dev;
+    p.dn_s = L->dn_s_dev;
+    p.sh_gu_q = L->sh_gu_q_dev;
+    p.sh_gu_s = L->sh_gu_s_dev;
+    p.sh_dn_q = L->sh_dn_q_dev;
+    p.sh_dn_s = L->sh_dn_s_dev;
+    p.xg = at<__half>(ws, W.xg);
+    p.mblocks = at<MBlock>(ws, W.mblocks);
+    p.n_mblocks = at<int32_t>(ws, W.n_mblocks);
+    p.h = at<__half>(ws, W.h16);
+    p.hs = at<__half>(ws, W.hs16);
+    p.y = at<__half>(ws, W.y);
+    p.ysh = at<__half>(ws, W.ysh);
+    p.err = &at<Ctl>(ws, W.ctl)->err;
+    p.T = T;
+    p.K = d->top_k;
+    p.H = d->hidden;
+    p.I = d->inter;
+    p.Is = d->shared_inter;
+    p.E = d->n_experts;
+    return p;
+}
+
+// Routed gate/up at T > kDecodeMaxTokens from caller offsets/perm: block
+// list, gather, GEMM.  h_f32: NULL to keep h only as the fp16 operand.
+strata_status pf_gate_up(const strata_moe_dims* d, const strata_moe_layer* L, const void* x,
+                         int T, const int32_t* offsets, const int32_t* perm, float* h_f32,
+                         void* ws, cudaStream_t s) {
+    if (!prefill_supported(*d)) return STRATA_EUNSUPPORTED;
+    PfExperts p = pf_stage(d, L, T, ws);
+    p.x = static_cast<const uint16_t*>(x);
+    p.perm = perm;
+    p.routed = 1;
+    p.xg_rows = T * d->top_k;
+    p.h_f32 = h_f32;
+    STRATA_TRY(launch_prefill_blocks(offsets, T, d->top_k, d->n_experts, 0,
+                                     const_cast<MBlock*>(p.mblocks),
+                                     const_cast<int32_t*>(p.n_mblocks), p.err, s));
+    STRATA_TRY(launch_prefill_gather(p.x, perm, T, d->top_k, d->hidden, p.xg, p.xg_rows, s));
+    STRATA_TRY(launch_prefill_gate_up(p, s));
+    return STRATA_OK;
+}
+
+// Routed down at T > kDecodeMaxTokens into bf16 y (slot order); A is the
+// workspace's fp16 h, the block list the one pf_gate_up or the caller's
+// offsets built.
+strata_status pf_down(const strata_moe_dims* d, const strata_moe_layer* L, int T,
+                      const int32_t* offsets, bool build_blocks, void* y, void* ws,
+                      cudaStream_t s) {
+    if (!prefill_supported(*d)) return STRATA_EUNSUPPORTED;
+    PfExperts p = pf_stage(d, L, T, ws);
+    p.routed = 1;
+    p.y_bf16 = static_cast<uint16_t*>(y);
+    if (build_blocks)
+        STRATA_TRY(launch_prefill_blocks(offsets, T, d->top_k, d->n_experts, 0,
+                                         const_cast<MBlock*>(p.mblocks),
+                                         const_cast<int32_t*>(p.n_mblocks), p.err, s));
+    STRATA_TRY(launch_prefill_down(p, s));
     return STRATA_OK;
 }
 
@@ -354,9 +426,29 @@ strata_status moe_route(const strata_moe_dims* dims, const strata_moe_layer* lay
     if (!al16(x_dev) || !al4(ids_dev) || !al4(weights_dev) || !al4(shared_gate_dev) ||
         !opt4(logits_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
-    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
     const WsLayout W = ws_layout(*dims, T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > kDecodeMaxTokens) {
+        if (!prefill_supported(*dims)) return STRATA_EUNSUPPORTED;
+        PfRoute r{};
+        r.x = static_cast<const uint16_t*>(x_dev);
+        r.router = static_cast<const uint16_t*>(layer->router_dev);
+        r.bias = layer->router_bias_dev;
+        r.logits = at<float>(ws_dev, W.logits);
+        r.logits_user = logits_dev;
+        r.ids = at<int32_t>(ws_dev, W.ids);
+        r.w = at<float>(ws_dev, W.w);
+        r.sig = at<float>(ws_dev, W.sig);
+        r.ids_user = ids_dev;
+        r.w_user = weights_dev;
+        r.sig_user = shared_gate_dev;
+        r.err = &at<Ctl>(ws_dev, W.ctl)->err;
+        r.T = T;
+        r.H = dims->hidden;
+        r.E = dims->n_experts;
+        r.K = dims->top_k;
+        return cuda_status(launch_prefill_route(r, s));
+    }
     RouteLaunch r{};
     r.router = static_cast<const uint16_t*>(layer->router_dev);
     r.bias = layer->router_bias_dev;
@@ -391,8 +483,25 @@ strata_status moe_permute(const strata_moe_dims* dims, const int32_t* ids_dev, i
     if (!al4(ids_dev) || !al4(counts_dev) || !al4(offsets_dev) || !al4(perm_dev) ||
         !al4(inv_perm_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
-    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
     const WsLayout W = ws_layout(*dims, T);
+    if (T > kDecodeMaxTokens) {
+        PfBucket b{};
+        b.ids = ids_dev;
+        b.cnt_blk = at<int32_t>(ws_dev, W.cnt_blk);
+        b.base_blk = at<int32_t>(ws_dev, W.base_blk);
+        b.counts = counts_dev;
+        b.offsets = offsets_dev;
+        b.perm = perm_dev;
+        b.inv = inv_perm_dev;
+        b.mblocks = at<MBlock>(ws_dev, W.mblocks);
+        b.n_mblocks = at<int32_t>(ws_dev, W.n_mblocks);
+        b.err = &at<Ctl>(ws_dev, W.ctl)->err;
+        b.T = T;
+        b.K = dims->top_k;
+        b.E = dims->n_experts;
+        b.with_shared = 0;
+        return cuda_status(launch_prefill_bucket(b, static_cast<cudaStream_t>(stream)));
+    }
     return cuda_status(launch_permute_small(ids_dev, T, dims->top_k, dims->n_experts, counts_dev,
                                             offsets_dev, perm_dev, inv_perm_dev,
                                             &at<Ctl>(ws_dev, W.ctl)->err,
@@ -408,9 +517,10 @@ strata_status moe_expert_gate_up(const strata_moe_dims* dims, const strata_moe_l
     if (!al16(x_dev) || !al4(offsets_dev) || !al4(perm_dev) || !al16(h_dev) ||
         !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
-    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
-    const WsLayout W = ws_layout(*dims, T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > kDecodeMaxTokens)
+        return pf_gate_up(dims, layer, x_dev, T, offsets_dev, perm_dev, h_dev, ws_dev, s);
+    const WsLayout W = ws_layout(*dims, T);
     int32_t* plan = at<int32_t>(ws_dev, W.plan);
     STRATA_TRY(launch_plan(offsets_dev, perm_dev, T, dims->top_k, dims->n_experts, plan,
                            &at<Ctl>(ws_dev, W.ctl)->err, s));
@@ -437,9 +547,15 @@ strata_status moe_expert_down(const strata_moe_dims* dims, const strata_moe_laye
     if (T == 0) return STRATA_OK;
     if (!al16(h_dev) || !al4(offsets_dev) || !al16(y_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
-    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
-    const WsLayout W = ws_layout(*dims, T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > kDecodeMaxTokens) {
+        if (!prefill_supported(*dims)) return STRATA_EUNSUPPORTED;
+        const WsLayout W = ws_layout(*dims, T);
+        STRATA_TRY(launch_prefill_pack(h_dev, (long long)T * dims->top_k * dims->inter,
+                                       at<__half>(ws_dev, W.h16), s));
+        return pf_down(dims, layer, T, offsets_dev, true, y_dev, ws_dev, s);
+    }
+    const WsLayout W = ws_layout(*dims, T);
     int32_t* plan = at<int32_t>(ws_dev, W.plan);
     STRATA_TRY(launch_plan(offsets_dev, nullptr, T, dims->top_k, dims->n_experts, plan,
                            &at<Ctl>(ws_dev, W.ctl)->err, s));
@@ -469,7 +585,13 @@ strata_status moe_expert_ffn(const strata_moe_dims* dims, const strata_moe_layer
     if (!al16(x_dev) || !al4(offsets_dev) || !al4(perm_dev) || !al16(y_dev) ||
         !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
-    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
+    if (T > kDecodeMaxTokens) {
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        const strata_status st =
+            pf_gate_up(dims, layer, x_dev, T, offsets_dev, perm_dev, nullptr, ws_dev, s);
+        if (st != STRATA_OK) return st;
+        return pf_down(dims, layer, T, offsets_dev, false, y_dev, ws_dev, s);
+    }
     const WsLayout W = ws_layout(*dims, T);
     float* h = at<float>(ws_dev, W.h);
     strata_status st = moe_expert_gate_up(dims, layer, x_dev, T, offsets_dev, perm_dev, h,
@@ -488,9 +610,28 @@ strata_status moe_combine(const strata_moe_dims* dims, const strata_moe_layer* l
     if (!al16(x_dev) || !al16(y_dev) || !al4(inv_perm_dev) || !al4(weights_dev) ||
         !al4(shared_gate_dev) || !al16(out_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
-    if (T > kDecodeMaxTokens) return STRATA_EUNSUPPORTED;
     const WsLayout W = ws_layout(*dims, T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > kDecodeMaxTokens) {
+        // the shared expert over the T tokens, then the combine of bf16 y
+        if (!prefill_supported(*dims)) return STRATA_EUNSUPPORTED;
+        PfExperts p = pf_stage(dims, layer, T, ws_dev);
+        p.x = static_cast<const uint16_t*>(x_dev);
+        p.shared = 1;
+        p.xg_rows = T;
+        p.xg_shared_row0 = 0;
+        STRATA_TRY(launch_prefill_blocks(nullptr, T, dims->top_k, dims->n_experts, 1,
+                                         const_cast<MBlock*>(p.mblocks),
+                                         const_cast<int32_t*>(p.n_mblocks), p.err, s));
+        STRATA_TRY(launch_prefill_gather(p.x, nullptr, T, 0, dims->hidden, p.xg, T, s));
+        STRATA_TRY(launch_prefill_gate_up(p, s));
+        STRATA_TRY(launch_prefill_down(p, s));
+        STRATA_TRY(launch_prefill_combine(nullptr, static_cast<const uint16_t*>(y_dev), p.ysh,
+                                          inv_perm_dev, weights_dev, shared_gate_dev, T,
+                                          dims->top_k, dims->hidden,
+                                          static_cast<uint16_t*>(out_dev), nullptr, s));
+        return STRATA_OK;
+    }
     GuLaunch g{};
     g.q = layer->sh_gu_q_dev;
     g.sc = layer->sh_gu_s_dev;

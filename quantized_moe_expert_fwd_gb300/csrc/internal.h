@@ -149,7 +149,7 @@ struct GemmLaunch {
 };
 struct PfRoute {
     const uint16_t* x; const uint16_t* router; const float* bias;
-    float* logits;
+    float* logits; float* logits_user;
     const int32_t* forced_ids; const float* forced_w;
     int32_t* ids; float* w; float* sig;
     int32_t* ids_user; float* w_user; float* sig_user;
@@ -173,15 +173,33 @@ struct PfExperts {
     const MBlock* mblocks; const int32_t* n_mblocks;
     __half* h; __half* hs;
     __half* y; __half* ysh;
+    float* h_f32;          // non-NULL: routed h also in fp32, natural order, [T*K][I]
+    uint16_t* y_bf16;      // non-NULL: routed y in bf16 [T*K][H] instead of fp16 y
+    int routed, shared;    // weight sets the block list may name (the other's maps alias)
+    int xg_rows, xg_shared_row0;   // rows of xg; first row of the shared expert's tokens
     uint32_t* err;
     int T, K, H, I, Is, E;
 };
 bool prefill_supported(const strata_moe_dims& d);
 cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s);
 cudaError_t launch_prefill_bucket(const PfBucket& b, cudaStream_t s);
+// block list of the routed slots from caller offsets (offsets NULL: none)
+// and/or of the shared expert over the T tokens
+cudaError_t launch_prefill_blocks(const int32_t* offsets, int T, int K, int E, int with_shared,
+                                  MBlock* mblocks, int32_t* n_mblocks, uint32_t* err,
+                                  cudaStream_t s);
+// xg rows: the T*K routed slots (token perm[row] / K), then the T tokens
+cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, int T, int K, int H,
+                                  __half* xg, int rows, cudaStream_t s);
+// fp32 [n] -> fp16 in the operand order (n a multiple of 8)
+cudaError_t launch_prefill_pack(const float* src, long long n, __half* dst, cudaStream_t s);
+cudaError_t launch_prefill_gate_up(const PfExperts& p, cudaStream_t s);
+cudaError_t launch_prefill_down(const PfExperts& p, cudaStream_t s);
+// gather + gate/up + down of the routed experts and the shared one
 cudaError_t launch_prefill_experts(const PfExperts& p, cudaStream_t s);
-cudaError_t launch_prefill_combine(const __half* y, const __half* ysh, const int32_t* inv,
-                                   const float* w, const float* sig, int T, int K, int H,
-                                   uint16_t* out, float* resid, cudaStream_t s);
+// y: fp16 (y_f16) or bf16 (y_bf16), slot order; ysh fp16
+cudaError_t launch_prefill_combine(const __half* y_f16, const uint16_t* y_bf16, const __half* ysh,
+                                   const int32_t* inv, const float* w, const float* sig, int T,
+                                   int K, int H, uint16_t* out, float* resid, cudaStream_t s);
 
 }  // namespace strata

@@ -259,6 +259,50 @@ __global__ void __launch_bounds__(1024) k_pf_scan(PfScanLaunch a) {
     }
 }
 
+// The 128-row blocks of the routed slots from caller-supplied offsets (one
+// thread an expert; an expert whose range leaves [0, T*K] is skipped and
+// latches STRATA_EBADROUTE) and, with_shared, of the shared expert's tokens.
+__global__ void __launch_bounds__(1024) k_pf_blocks(const int32_t* offsets, int T, int K, int E,
+                                                    int with_shared, MBlock* mblocks,
+                                                    int32_t* n_mblocks, uint32_t* err) {
+    __shared__ int s_warp[33];
+    pdl_launch();
+    pdl_wait();
+    const int e = threadIdx.x;
+    int off = 0, total = 0;
+    if (offsets != nullptr && e < E) {
+        off = __ldg(offsets + e);
+        total = __ldg(offsets + e + 1) - off;
+        if (off < 0 || total < 0 || (long long)off + total > (long long)T * K) {
+            latch(err, STRATA_EBADROUTE);
+            total = 0;
+        }
+    }
+    const int nmb = (total + kBM - 1) / kBM;
+    int sum_mb = 0;
+    const int mbo = block_exclusive_scan(nmb, s_warp, &sum_mb);
+    for (int j = 0; j < nmb; ++j) {
+        MBlock mb;
+        mb.group = e;
+        mb.row = off + j * kBM;
+        mb.nrows = min(kBM, total - j * kBM);
+        mb.pad = 0;
+        mblocks[mbo + j] = mb;
+    }
+    if (threadIdx.x == 0) {
+        const int nsh = with_shared ? (T + kBM - 1) / kBM : 0;
+        for (int j = 0; j < nsh; ++j) {
+            MBlock mb;
+            mb.group = E;
+            mb.row = j * kBM;
+            mb.nrows = min(kBM, T - j * kBM);
+            mb.pad = 0;
+            mblocks[sum_mb + j] = mb;
+        }
+        n_mblocks[0] = sum_mb + nsh;
+    }
+}
+
 // Slots of the block's pairs: base of (block, expert) + rank among the
 // block's earlier pairs of the same expert (pairs in ascending t*K + k, so
 // an expert's slots ascend in t).
@@ -327,6 +371,24 @@ __global__ void k_pf_gather(const uint16_t* x, const int32_t* perm, int T, int K
     *reinterpret_cast<uint4*>(xg + size_t(row) * H + 8 * g) = out;
 }
 
+// fp32 -> fp16 in the operand order, 8 elements a thread.
+__global__ void k_pf_pack(const float* src, long long n8, __half* dst) {
+    pdl_launch();
+    pdl_wait();
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(src) + 2 * i);
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 2 * i + 1);
+    const __half2 h0 = __floats2half2_rn(a.x, b.x);
+    const __half2 h1 = __floats2half2_rn(a.y, b.y);
+    const __half2 h2 = __floats2half2_rn(a.z, b.z);
+    const __half2 h3 = __floats2half2_rn(a.w, b.w);
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(*reinterpret_cast<const uint32_t*>(&h0),
+                                                  *reinterpret_cast<const uint32_t*>(&h1),
+                                                  *reinterpret_cast<const uint32_t*>(&h2),
+                                                  *reinterpret_cast<const uint32_t*>(&h3));
+}
+
 // out[t] = bf16( sum_k w[t][k] y[inv[t*K+k]] + sig[t] y_sh[t] ), 8 columns
 // a thread, k ascending; y in fp16.  resid (optional) += the bf16 output.
 __device__ __forceinline__ void h8_to_f32(const uint4& v, float (&f)[8]) {
@@ -339,7 +401,17 @@ __device__ __forceinline__ void h8_to_f32(const uint4& v, float (&f)[8]) {
     }
 }
 
-__global__ void k_pf_combine(const __half* y, const __half* y_sh, const int32_t* inv,
+__device__ __forceinline__ void b8_to_f32(const uint4& v, float (&f)[8]) {
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        f[2 * j] = bf16_lo(wv[j]);
+        f[2 * j + 1] = bf16_hi(wv[j]);
+    }
+}
+
+template <bool Y_BF16>
+__global__ void k_pf_combine(const void* y, const __half* y_sh, const int32_t* inv,
                              const float* w, const float* sig, int T, int K, int H,
                              uint16_t* out, float* resid) {
     pdl_launch();
@@ -354,7 +426,11 @@ __global__ void k_pf_combine(const __half* y, const __half* y_sh, const int32_t*
         if (sl < 0 || sl >= T * K) continue;
         const float wk = __ldcg(w + size_t(t) * K + k);
         float f[8];
-        h8_to_f32(__ldcg(reinterpret_cast<const uint4*>(y + size_t(sl) * H + 8 * g)), f);
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(y) + (size_t(sl) * H + 8 * g) / 8);
+        if (Y_BF16)
+            b8_to_f32(v, f);
+        else
+            h8_to_f32(v, f);
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] += wk * f[j];
     }
@@ -623,6 +699,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     for (int i = 0; i < 16; ++i)
                         hv[i] = silu_mul(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
                     const int ld = sh ? a.ld2 : a.ldo;
+                    if (!sh && a.out_f32 != nullptr) {
+                        // natural order, fp32 (the h of the stage-wise calls)
+                        float4* h32 = reinterpret_cast<float4*>(a.out_f32 + size_t(row + m) * ld +
+                                                                col0 / 2);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            h32[j] = make_float4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2],
+                                                 hv[4 * j + 3]);
+                    }
                     __half* hrow = (sh ? a.out2_f16 : a.out_f16) + size_t(row + m) * ld + col0 / 2;
 #pragma unroll
                     for (int gq = 0; gq < 2; ++gq) {
@@ -636,6 +721,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                        *reinterpret_cast<const uint32_t*>(&h1),
                                        *reinterpret_cast<const uint32_t*>(&h2),
                                        *reinterpret_cast<const uint32_t*>(&h3));
+                    }
+                } else if (!sh && a.out_bf16 != nullptr) {
+                    // y in bf16 (the stage-wise calls' format)
+                    uint16_t* yrow = a.out_bf16 + size_t(row + m) * a.ldo + col0;
+#pragma unroll
+                    for (int gq = 0; gq < 4; ++gq) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            o[j] = uint32_t(f32_to_bf16(__uint_as_float(v[8 * gq + 2 * j]))) |
+                                   (uint32_t(f32_to_bf16(__uint_as_float(v[8 * gq + 2 * j + 1])))
+                                    << 16);
+                        *reinterpret_cast<uint4*>(yrow + 8 * gq) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 } else {
                     // y in fp16: the combine sums several of them before the
@@ -772,6 +870,7 @@ cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     PfSelectLaunch sl{};
     sl.logits = r.logits;
+    sl.logits_user = r.logits_user;
     sl.forced_ids = r.forced_ids;
     sl.forced_w = r.forced_w;
     sl.ids = r.ids;
@@ -809,27 +908,51 @@ cudaError_t launch_prefill_bucket(const PfBucket& b, cudaStream_t s) {
                       static_cast<const int32_t*>(b.base_blk), b.perm, b.inv, b.err);
 }
 
-cudaError_t launch_prefill_experts(const PfExperts& p, cudaStream_t s) {
+cudaError_t launch_prefill_blocks(const int32_t* offsets, int T, int K, int E, int with_shared,
+                                  MBlock* mblocks, int32_t* n_mblocks, uint32_t* err,
+                                  cudaStream_t s) {
+    return launch_pdl(k_pf_blocks, 1, 1024, 0, s, offsets, T, K, E, with_shared, mblocks,
+                      n_mblocks, err);
+}
+
+cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, int T, int K, int H,
+                                  __half* xg, int rows, cudaStream_t s) {
+    const long long n = (long long)rows * (H / 8);
+    return launch_pdl(k_pf_gather, int((n + 255) / 256), 256, 0, s, x, perm, T, K, H, xg, rows);
+}
+
+cudaError_t launch_prefill_pack(const float* src, long long n, __half* dst, cudaStream_t s) {
+    const long long n8 = n / 8;
+    return launch_pdl(k_pf_pack, int((n8 + 255) / 256), 256, 0, s, src, n8, dst);
+}
+
+cudaError_t launch_prefill_gate_up(const PfExperts& p, cudaStream_t s) {
     const int T = p.T, K = p.K, H = p.H, I = p.I, Is = p.Is, E = p.E;
-    const int rows = T * K + T;
-    {
-        const long long n = (long long)rows * (H / 8);
-        cudaError_t e = launch_pdl(k_pf_gather, int((n + 255) / 256), 256, 0, s, p.x, p.perm, T, K,
-                                   H, p.xg, rows);
-        if (e != cudaSuccess) return e;
-    }
-    // gate/up: A = xg [rows][H]; B = interleaved gate/up rows
+    // A = xg [xg_rows][H]; B = interleaved gate/up rows.  A weight set the
+    // block list cannot name gets the other set's maps.
     CUtensorMap ma, mq, ms, mq2, ms2;
-    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.xg, H, rows, kBK, kBM, true) ||
-        !make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.gu_q, H / 2, uint64_t(E) * 2 * I,
-                  kBK / 2, 256, false) ||
-        !make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.gu_s, H / 32, uint64_t(E) * 2 * I,
-                  H / 32, 256, false) ||
-        !make_map(&mq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_gu_q, H / 2, 2 * Is, kBK / 2, 256,
-                  false) ||
-        !make_map(&ms2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.sh_gu_s, H / 32, 2 * Is, H / 32, 256,
-                  false))
+    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.xg, H, p.xg_rows, kBK, kBM, true))
         return cudaErrorInvalidValue;
+    if (p.routed &&
+        (!make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.gu_q, H / 2, uint64_t(E) * 2 * I,
+                   kBK / 2, 256, false) ||
+         !make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.gu_s, H / 32, uint64_t(E) * 2 * I,
+                   H / 32, 256, false)))
+        return cudaErrorInvalidValue;
+    if (p.shared &&
+        (!make_map(&mq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_gu_q, H / 2, 2 * Is, kBK / 2, 256,
+                   false) ||
+         !make_map(&ms2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.sh_gu_s, H / 32, 2 * Is, H / 32, 256,
+                   false)))
+        return cudaErrorInvalidValue;
+    if (!p.routed) {
+        mq = mq2;
+        ms = ms2;
+    }
+    if (!p.shared) {
+        mq2 = mq;
+        ms2 = ms;
+    }
     GemmLaunch g{};
     g.BN = 256;
     g.N = 2 * I;
@@ -841,29 +964,47 @@ cudaError_t launch_prefill_experts(const PfExperts& p, cudaStream_t s) {
     g.mblocks = p.mblocks;
     g.n_mblocks = p.n_mblocks;
     g.nb_max = (2 * (I > Is ? I : Is)) / 256;
-    g.a_shared_row0 = T * K;
+    g.a_shared_row0 = p.xg_shared_row0;
     g.out_f16 = p.h;
+    g.out_f32 = p.h_f32;
     g.ldo = I;
     g.out2_f16 = p.hs;
     g.ld2 = Is;
     g.err = p.err;
-    cudaError_t e = run_gemm<kGemmGateUp>(g, ma, ma, mq, ms, mq2, ms2, s);
-    if (e != cudaSuccess) return e;
+    (void)T;
+    (void)K;
+    return run_gemm<kGemmGateUp>(g, ma, ma, mq, ms, mq2, ms2, s);
+}
 
-    // down: A = h [T*K][I] (routed) or hs [T][Is] (shared); B = down rows
+cudaError_t launch_prefill_down(const PfExperts& p, cudaStream_t s) {
+    const int T = p.T, K = p.K, H = p.H, I = p.I, Is = p.Is, E = p.E;
+    // A = h [T*K][I] (routed) or hs [T][Is] (shared); B = down rows
     CUtensorMap da, da2, dq, ds, dq2, ds2;
-    if (!make_map(&da, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.h, I, uint64_t(T) * K, kBK, kBM,
-                  true) ||
-        !make_map(&da2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.hs, Is, T, kBK, kBM, true) ||
-        !make_map(&dq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.dn_q, I / 2, uint64_t(E) * H, kBK / 2,
-                  256, false) ||
-        !make_map(&ds, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.dn_s, I / 32, uint64_t(E) * H, I / 32,
-                  256, false) ||
-        !make_map(&dq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_dn_q, Is / 2, H, kBK / 2, 256,
-                  false) ||
-        !make_map(&ds2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.sh_dn_s, Is / 32, H, Is / 32, 256,
-                  false))
+    if (p.routed &&
+        (!make_map(&da, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.h, I, uint64_t(T) * K, kBK, kBM,
+                   true) ||
+         !make_map(&dq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.dn_q, I / 2, uint64_t(E) * H, kBK / 2,
+                   256, false) ||
+         !make_map(&ds, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.dn_s, I / 32, uint64_t(E) * H, I / 32,
+                   256, false)))
         return cudaErrorInvalidValue;
+    if (p.shared &&
+        (!make_map(&da2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.hs, Is, T, kBK, kBM, true) ||
+         !make_map(&dq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_dn_q, Is / 2, H, kBK / 2, 256,
+                   false) ||
+         !make_map(&ds2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.sh_dn_s, Is / 32, H, Is / 32, 256,
+                   false)))
+        return cudaErrorInvalidValue;
+    if (!p.routed) {
+        da = da2;
+        dq = dq2;
+        ds = ds2;
+    }
+    if (!p.shared) {
+        da2 = da;
+        dq2 = dq;
+        ds2 = ds;
+    }
     GemmLaunch d{};
     d.BN = 256;
     d.N = H;
@@ -877,18 +1018,31 @@ cudaError_t launch_prefill_experts(const PfExperts& p, cudaStream_t s) {
     d.nb_max = H / 256;
     d.a_shared_row0 = 0;
     d.out_f16 = p.y;
+    d.out_bf16 = p.y_bf16;
     d.out2_f16 = p.ysh;
     d.ldo = H;
     d.err = p.err;
     return run_gemm<kGemmDown>(d, da, da2, dq, ds, dq2, ds2, s);
 }
 
-cudaError_t launch_prefill_combine(const __half* y, const __half* ysh, const int32_t* inv,
-                                   const float* w, const float* sig, int T, int K, int H,
-                                   uint16_t* out, float* resid, cudaStream_t s) {
+cudaError_t launch_prefill_experts(const PfExperts& p, cudaStream_t s) {
+    cudaError_t e = launch_prefill_gather(p.x, p.perm, p.T, p.K, p.H, p.xg, p.xg_rows, s);
+    if (e != cudaSuccess) return e;
+    e = launch_prefill_gate_up(p, s);
+    if (e != cudaSuccess) return e;
+    return launch_prefill_down(p, s);
+}
+
+cudaError_t launch_prefill_combine(const __half* y_f16, const uint16_t* y_bf16, const __half* ysh,
+                                   const int32_t* inv, const float* w, const float* sig, int T,
+                                   int K, int H, uint16_t* out, float* resid, cudaStream_t s) {
     const long long n = (long long)T * (H / 8);
-    return launch_pdl(k_pf_combine, int((n + 255) / 256), 256, 0, s, y, ysh, inv, w, sig, T, K, H,
-                      out, resid);
+    const int grid = int((n + 255) / 256);
+    if (y_bf16 != nullptr)
+        return launch_pdl(k_pf_combine<true>, grid, 256, 0, s, static_cast<const void*>(y_bf16),
+                          ysh, inv, w, sig, T, K, H, out, resid);
+    return launch_pdl(k_pf_combine<false>, grid, 256, 0, s, static_cast<const void*>(y_f16), ysh,
+                      inv, w, sig, T, K, H, out, resid);
 }
 
 }  // namespace strata

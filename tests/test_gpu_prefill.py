@@ -121,3 +121,77 @@ def test_prefill_block_forward_residual():
     torch.cuda.synchronize()
     assert q.moe_get_device_status(ws) == q.STRATA_OK
     G.assert_close(resid.cpu().numpy() - r0, rref - r0, "prefill block residual update")
+
+
+@pytest.mark.parametrize("T", [33, 300])
+def test_prefill_separate_calls(T):
+    """route -> permute -> gate/up -> down / expert_ffn -> combine at T > 32
+    (the tensor-core kernels), each stage against the oracle."""
+    dims = gen.QWEN
+    planes, dl = layer(dims, 6)
+    K, E, I, H = dims.top_k, dims.n_experts, dims.inter, dims.hidden
+    xb = oracle.rmsnorm(gen.draw_tokens(dims, T, 80 + T, "resid"))
+    ref = oracle.moe_forward(dims, planes, xb, want_y=True, want_h=True)
+    x = G.u16(xb)
+    ws = q.make_workspace(dims, T, G.dev())
+    ids = torch.empty((T, K), dtype=torch.int32, device=G.dev())
+    w = torch.empty((T, K), dtype=torch.float32, device=G.dev())
+    sig = torch.empty((T,), dtype=torch.float32, device=G.dev())
+    logits = torch.empty((T, E), dtype=torch.float32, device=G.dev())
+    q.moe_route(dims, dl, x, ids, w, sig, ws, logits=logits)
+    torch.cuda.synchronize()
+    # tensor-core fp32 accumulation of 2048 bf16 products of logits ~N(0, 1)
+    assert np.allclose(logits.cpu().numpy(), ref["logits"], rtol=0, atol=5e-5)
+    clear = G.clear_tokens(ref["gap"])
+    assert np.array_equal(ids.cpu().numpy()[clear], ref["ids"][clear])
+    assert np.allclose(w.cpu().numpy()[clear], ref["w"][clear], rtol=1e-4, atol=1e-6)
+    assert np.allclose(sig.cpu().numpy(), ref["sig"], rtol=1e-4, atol=1e-6)
+    # the oracle's routing from here on, so every stage sees the same input
+    ids = G.i32(ref["ids"])
+    w = G.f32(ref["w"])
+    counts = torch.empty(E, dtype=torch.int32, device=G.dev())
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=G.dev())
+    perm = torch.empty(T * K, dtype=torch.int32, device=G.dev())
+    inv = torch.empty(T * K, dtype=torch.int32, device=G.dev())
+    q.moe_permute(dims, ids, counts, offsets, perm, inv, ws)
+    oc, oo, op, oi = oracle.permute(ref["ids"], E)
+    assert np.array_equal(counts.cpu().numpy(), oc)
+    assert np.array_equal(offsets.cpu().numpy(), oo)
+    assert np.array_equal(perm.cpu().numpy(), op) and np.array_equal(inv.cpu().numpy(), oi)
+    h = torch.empty((T * K, I), dtype=torch.float32, device=G.dev())
+    q.moe_expert_gate_up(dims, dl, x, offsets, perm, h, ws)
+    G.assert_close(h.cpu().numpy(), ref["h"].reshape(T * K, I)[op], "gate/up h")
+    y = torch.empty((T * K, H), dtype=torch.int16, device=G.dev())
+    q.moe_expert_ffn(dims, dl, x, offsets, perm, y, ws)
+    G.assert_close(G.bf16_to_np(y), ref["y"].reshape(T * K, H)[op], "expert y")
+    # the same fp16 operand either way: identical bits
+    y2 = torch.empty_like(y)
+    q.moe_expert_down(dims, dl, h, T, offsets, y2, ws)
+    assert torch.equal(y, y2)
+    out = torch.empty((T, H), dtype=torch.int16, device=G.dev())
+    q.moe_combine(dims, dl, x, y, inv, w, G.f32(ref["sig"]), out, ws)
+    torch.cuda.synchronize()
+    G.assert_close(G.bf16_to_np(out), ref["out"], "combine")
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+
+
+def test_prefill_stage_calls_reject_bad_offsets():
+    """Caller offsets that leave [0, T*K] are skipped and latch EBADROUTE."""
+    dims = gen.QWEN
+    planes, dl = layer(dims, 6)
+    T, K, E, I = 40, dims.top_k, dims.n_experts, dims.inter
+    xb = oracle.rmsnorm(gen.draw_tokens(dims, T, 90, "resid"))
+    x = G.u16(xb)
+    ws = q.make_workspace(dims, T, G.dev())
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    offsets[1:] = T * K
+    offsets[E] = T * K + 500                     # expert E-1 runs past the slots
+    perm = G.i32(np.arange(T * K, dtype=np.int32))
+    h = torch.zeros((T * K, I), dtype=torch.float32, device=G.dev())
+    q.moe_expert_gate_up(dims, dl, x, G.i32(offsets), perm, h, ws)
+    assert q.moe_get_device_status(ws) == q.STRATA_EBADROUTE
+    # expert 0 (all T*K slots) is still computed
+    ids = np.zeros((T, K), dtype=np.int32)
+    ref = oracle.moe_forward(dims, planes, xb, ids=ids, w=np.full((T, K), 1.0 / K, np.float32),
+                             want_h=True)
+    G.assert_close(h.cpu().numpy(), ref["h"].reshape(T * K, I), "valid expert beside bad offsets")
