@@ -12,7 +12,8 @@ constexpr int kWarp = 32;
 struct Ctl {
     uint32_t err;       // latched strata_status (first error wins)
     uint32_t where[7];  // first timed-out wait: site, block, warp, slot, round, item, 1
-    uint32_t pad[56];
+    uint32_t bar;       // grid barrier of the persistent decode kernel (low 31 bits 0 at rest)
+    uint32_t pad[55];
 };
 
 __device__ __forceinline__ void latch(uint32_t* err, uint32_t code) {

@@ -35,269 +35,9 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "route.cuh"
 
 namespace strata {
-
-// ------------------------------------------------------------------- plan
-// A layer's plan: the touched experts in ascending id, their slot ranges,
-// and the token of each slot (-1: none).
-struct SPlan {
-    int n;
-    int e[kMaxExperts];
-    int off[kMaxExperts];
-    int cnt[kMaxExperts];
-    int tok[kDecodeMaxTokens * kMaxTopK];
-};
-
-__device__ void load_plan(SPlan& P, const int32_t* plan, int E, int TK) {
-    const int* base = plan + kPlanHeader;
-    for (int i = threadIdx.x; i < 3 * E + TK; i += blockDim.x) {
-        const int v = __ldcg(base + i);
-        if (i < E)
-            P.e[i] = v;
-        else if (i < 2 * E)
-            P.off[i - E] = v;
-        else if (i < 3 * E)
-            P.cnt[i - 2 * E] = v;
-        else
-            P.tok[i - 3 * E] = v;
-    }
-    if (threadIdx.x == 0) P.n = __ldcg(plan);
-    __syncthreads();
-}
-
-__device__ void shared_plan(SPlan& P, int T) {
-    for (int s = threadIdx.x; s < T; s += blockDim.x) P.tok[s] = s;
-    if (threadIdx.x == 0) {
-        P.n = 1;
-        P.e[0] = 0;
-        P.off[0] = 0;
-        P.cnt[0] = T;
-    }
-    __syncthreads();
-}
-
-// Where a bucketing is published (any pointer may be null).
-struct BucketOut {
-    int32_t* counts;
-    int32_t* offsets;
-    int32_t* perm;
-    int32_t* inv;
-    int32_t* plan;
-};
-
-// Stable counting sort of the T*K (token, k) pairs by expert, by one CTA.
-// s_ids: the pairs' expert ids; an out-of-range id gets no slot (inv -1).
-// Fills P and s_inv in shared memory and, when given, the global copies:
-// counts[e], offsets[0..E], perm[slot] = t*K + k (slots of one expert in
-// ascending t), inv[t*K + k] = slot, and the plan.
-__device__ void bucket_cta(const int* s_ids, int T, int K, int E, int* s_cnt, int* s_off,
-                           int* s_wsum, SPlan& P, int* s_inv, const BucketOut& g) {
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, wpb = blockDim.x >> 5;
-    const int TK = T * K;
-    for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
-    for (int p = tid; p < TK; p += blockDim.x) s_inv[p] = -1;
-    __syncthreads();
-    for (int p = tid; p < TK; p += blockDim.x) {
-        const int e = s_ids[p];
-        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-    }
-    __syncthreads();
-    // exclusive scan over experts of (slots, touched experts), packed in one
-    // int (slots < 2^16, experts < 2^15); each thread one contiguous segment
-    const int seg = (E + blockDim.x - 1) / blockDim.x;
-    const int e0 = min(E, tid * seg), e1 = min(E, e0 + seg);
-    int local = 0, nz = 0;
-    for (int e = e0; e < e1; ++e) {
-        local += s_cnt[e];
-        nz += s_cnt[e] > 0 ? 1 : 0;
-    }
-    const int mine = local | (nz << 16);
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) s_wsum[wid] = incl;
-    __syncthreads();
-    if (tid == 0) {
-        int r = 0;
-        for (int w = 0; w < wpb; ++w) {
-            const int c = s_wsum[w];
-            s_wsum[w] = r;
-            r += c;
-        }
-        s_off[E] = r & 0xffff;
-        P.n = r >> 16;
-    }
-    __syncthreads();
-    const int excl = s_wsum[wid] + incl - mine;
-    int run = excl & 0xffff, rank = excl >> 16;
-    for (int e = e0; e < e1; ++e) {
-        s_off[e] = run;
-        if (s_cnt[e] > 0) {
-            P.e[rank] = e;
-            P.off[rank] = run;
-            P.cnt[rank] = s_cnt[e];
-            ++rank;
-        }
-        run += s_cnt[e];
-    }
-    __syncthreads();
-    for (int s = s_off[E] + tid; s < TK; s += blockDim.x) P.tok[s] = -1;
-    for (int e = tid; e < E; e += blockDim.x) {
-        const int c = s_cnt[e];
-        if (g.counts) g.counts[e] = c;
-        if (g.offsets) g.offsets[e] = s_off[e];
-        if (c == 0) continue;
-        int slot = s_off[e];
-        for (int p = 0; p < TK; ++p)
-            if (s_ids[p] == e) {
-                s_inv[p] = slot;
-                P.tok[slot] = p / K;
-                if (g.perm) g.perm[slot] = p;
-                ++slot;
-            }
-    }
-    __syncthreads();
-    if (tid == 0 && g.offsets) g.offsets[E] = s_off[E];
-    if (g.inv)
-        for (int p = tid; p < TK; p += blockDim.x) g.inv[p] = s_inv[p];
-    if (g.plan) {
-        if (tid == 0) g.plan[0] = P.n;
-        for (int i = tid; i < P.n; i += blockDim.x) {
-            g.plan[kPlanHeader + i] = P.e[i];
-            g.plan[kPlanHeader + E + i] = P.off[i];
-            g.plan[kPlanHeader + 2 * E + i] = P.cnt[i];
-        }
-        for (int s = tid; s < TK; s += blockDim.x) g.plan[kPlanHeader + 3 * E + s] = P.tok[s];
-    }
-}
-
-// ------------------------------------------------------------- selection
-// Top-K of one token's logits (larger first, ties to the lower id), written
-// in ascending id to ids[0..K) with renormalised softmax weights w[0..K).
-// One warp.  L: this warp's shared scratch of E floats; ex: K floats.
-// A lane keeps the best of its own logits (ids lane, lane+32, ...); each
-// pick is a warp arg-max over the lanes' bests, after which only the winning
-// lane rescans its own logits.
-__device__ void select_topk_warp(const float* lg, int E, int K, float* L, float* ex, int* ids,
-                                 float* w, int lane) {
-    for (int e = lane; e < E; e += 32) L[e] = __ldcg(lg + e);
-    __syncwarp();
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-        const float v = L[e];
-        if (v > bv || (v == bv && e < be)) {
-            bv = v;
-            be = e;
-        }
-    }
-    float myv = 0.0f;
-    int mye = 0x7fffffff;
-    for (int k = 0; k < K; ++k) {
-        float wv = bv;
-        int we = be;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, we, o);
-            if (ov > wv || (ov == wv && oe < we)) {
-                wv = ov;
-                we = oe;
-            }
-        }
-        if (lane == k) {
-            myv = wv;
-            mye = we;
-        }
-        if (we < E && (we & 31) == lane) {
-            L[we] = __int_as_float(0x7fc00000);    // taken: NaN never wins
-            bv = -INFINITY;
-            be = 0x7fffffff;
-            for (int e = lane; e < E; e += 32) {
-                const float v = L[e];
-                if (v > bv || (v == bv && e < be)) {
-                    bv = v;
-                    be = e;
-                }
-            }
-        }
-    }
-    const float m = __shfl_sync(0xffffffffu, myv, 0);      // the first pick is the largest
-    int rank = 0;
-    for (int j = 0; j < K; ++j) rank += (__shfl_sync(0xffffffffu, mye, j) < mye) ? 1 : 0;
-    float e_k = 0.0f;
-    if (lane < K) {
-        e_k = expf(myv - m);
-        ex[rank] = e_k;
-        ids[rank] = mye;
-    }
-    __syncwarp();
-    float sum = 0.0f;
-    for (int r = 0; r < K; ++r) sum += ex[r];                 // ascending id
-    if (lane < K) w[rank] = e_k / sum;
-    __syncwarp();
-}
-
-// Routing of all T tokens by one CTA into shared memory: s_ids, s_w [T*K],
-// s_sig [T].  forced_ids / forced_w replace the selection when given.
-// scratch: (blockDim / 32) * (E + 16) floats.
-__device__ void route_cta(const float* logits, int T, int E, int K, const int32_t* forced_ids,
-                          const float* forced_w, int* s_ids, float* s_w, float* s_sig,
-                          float* scratch, uint32_t* err) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, wpb = blockDim.x >> 5;
-    const int ldl = E + 1;
-    for (int t = wid; t < T; t += wpb) {
-        const float* lg = logits + size_t(t) * ldl;
-        if (forced_ids) {
-            for (int k = lane; k < K; k += 32) {
-                const int id = __ldg(forced_ids + t * K + k);
-                if (id < 0 || id >= E) latch(err, STRATA_EBADROUTE);
-                s_ids[t * K + k] = id;
-                s_w[t * K + k] = __ldg(forced_w + t * K + k);
-            }
-        } else {
-            float* L = scratch + size_t(wid) * (E + 16);
-            select_topk_warp(lg, E, K, L, L + E, s_ids + t * K, s_w + t * K, lane);
-        }
-        if (lane == 0) s_sig[t] = 1.0f / (1.0f + expf(-__ldcg(lg + E)));
-    }
-    __syncthreads();
-}
-
-// ---------------------------------------------------------- x activations
-// Lane `lane` owns chunks c = lane + 32 m (m < MC) of a length-H row; a chunk
-// is 32 elements.  Loads token row x (bf16) as fp32 pairs plus chunk sums.
-template <int MC>
-__device__ __forceinline__ void load_x(const uint16_t* xrow, int NC, int lane,
-                                       uint64_t (&x2)[MC][16], float (&X)[MC]) {
-#pragma unroll
-    for (int m = 0; m < MC; ++m) {
-        const int c = lane + 32 * m;
-        float sum = 0.0f;
-        if (c < NC) {
-            const uint4* p = reinterpret_cast<const uint4*>(xrow + 32 * c);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const uint4 u = ldg_keep(p + v);
-                const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float lo = bf16_lo(wv[i]), hi = bf16_hi(wv[i]);
-                    x2[m][4 * v + i] = pk(lo, hi);
-                    sum += lo + hi;
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) x2[m][j] = 0ull;
-        }
-        X[m] = sum;
-    }
-}
 
 // ---------------------------------------------------------------- k_route
 template <int MC>
@@ -457,7 +197,8 @@ __global__ void __launch_bounds__(256, 1) k_select(SelectLaunch a) {
     __shared__ float s_sig[kDecodeMaxTokens];
     pdl_launch();
     pdl_wait();
-    route_cta(a.logits, a.T, a.E, a.K, nullptr, nullptr, s_ids, s_w, s_sig, s_dyn, a.err);
+    route_cta(a.logits, a.T, a.E, a.K, nullptr, nullptr, s_ids, s_w, s_sig, s_dyn, a.err,
+              int(threadIdx.x), int(blockDim.x), BlockSync{});
     const int TK = a.T * a.K;
     for (int p = threadIdx.x; p < TK; p += blockDim.x) {
         a.ids[p] = s_ids[p];
@@ -490,7 +231,8 @@ __global__ void __launch_bounds__(256, 1) k_permute_small(const int32_t* ids, in
     }
     __syncthreads();
     const BucketOut g{counts, offsets, perm, inv, nullptr};
-    bucket_cta(s_ids, T, K, E, s_cnt, s_off, s_wsum, P, s_inv, g);
+    bucket_cta(s_ids, T, K, E, s_cnt, s_off, s_wsum, P, s_inv, g, int(threadIdx.x),
+               int(blockDim.x), BlockSync{});
 }
 
 // The plan from a bucketing given by the caller (offsets and perm from any
@@ -599,10 +341,11 @@ __global__ void __launch_bounds__(kGuThreads, 1) k_gate_up(GuLaunch a) {
     } else {
         // routing: the same in every CTA; CTA 0 publishes it
         route_cta(a.logits, T, E, K, a.forced_ids, a.forced_w, s_ids, s_w, s_sig,
-                  reinterpret_cast<float*>(g_ring), a.err);
+                  reinterpret_cast<float*>(g_ring), a.err, tid, int(blockDim.x), BlockSync{});
         BucketOut g{nullptr, nullptr, nullptr, nullptr, nullptr};
         if (blockIdx.x == 0) g = BucketOut{a.counts, a.offsets, a.perm, a.inv, a.plan_out};
-        bucket_cta(s_ids, T, K, E, s_cnt, s_off, s_wsum, P, s_inv, g);
+        bucket_cta(s_ids, T, K, E, s_cnt, s_off, s_wsum, P, s_inv, g, tid, int(blockDim.x),
+                   BlockSync{});
         if (blockIdx.x == 0) {
             for (int p = tid; p < T * K; p += blockDim.x) {
                 a.ids[p] = s_ids[p];

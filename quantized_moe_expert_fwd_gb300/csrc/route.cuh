@@ -1,0 +1,299 @@
+// route.cuh -- device helpers of the decode-size kernels: the plan of the
+// touched experts, the per-CTA bucketing, top-K selection and the loading of
+// token activations.  The CTA-wide helpers take the participating threads'
+// index and count and a synchronisation functor, so a kernel whose producer
+// warp runs apart can call them on its consumer warps alone.
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace strata {
+
+struct BlockSync {
+    __device__ void operator()() const { __syncthreads(); }
+};
+
+// ------------------------------------------------------------------- plan
+// A layer's plan: the touched experts in ascending id, their slot ranges,
+// and the token of each slot (-1: none).
+struct SPlan {
+    int n;
+    int e[kMaxExperts];
+    int off[kMaxExperts];
+    int cnt[kMaxExperts];
+    int tok[kDecodeMaxTokens * kMaxTopK];
+};
+
+__device__ inline void load_plan(SPlan& P, const int32_t* plan, int E, int TK) {
+    const int* base = plan + kPlanHeader;
+    for (int i = threadIdx.x; i < 3 * E + TK; i += blockDim.x) {
+        const int v = __ldcg(base + i);
+        if (i < E)
+            P.e[i] = v;
+        else if (i < 2 * E)
+            P.off[i - E] = v;
+        else if (i < 3 * E)
+            P.cnt[i - 2 * E] = v;
+        else
+            P.tok[i - 3 * E] = v;
+    }
+    if (threadIdx.x == 0) P.n = __ldcg(plan);
+    __syncthreads();
+}
+
+__device__ inline void shared_plan(SPlan& P, int T) {
+    for (int s = threadIdx.x; s < T; s += blockDim.x) P.tok[s] = s;
+    if (threadIdx.x == 0) {
+        P.n = 1;
+        P.e[0] = 0;
+        P.off[0] = 0;
+        P.cnt[0] = T;
+    }
+    __syncthreads();
+}
+
+// Where a bucketing is published (any pointer may be null).
+struct BucketOut {
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm;
+    int32_t* inv;
+    int32_t* plan;
+};
+
+// Stable counting sort of the T*K (token, k) pairs by expert, by one CTA.
+// s_ids: the pairs' expert ids; an out-of-range id gets no slot (inv -1).
+// Fills P and s_inv in shared memory and, when given, the global copies:
+// counts[e], offsets[0..E], perm[slot] = t*K + k (slots of one expert in
+// ascending t), inv[t*K + k] = slot, and the plan.
+template <typename Sync>
+__device__ void bucket_cta(const int* s_ids, int T, int K, int E, int* s_cnt, int* s_off,
+                           int* s_wsum, SPlan& P, int* s_inv, const BucketOut& g, int tid,
+                           int nthr, Sync sync) {
+    const int lane = tid & 31, wid = tid >> 5, wpb = nthr >> 5;
+    const int TK = T * K;
+    #pragma unroll 1
+    for (int e = tid; e < E; e += nthr) s_cnt[e] = 0;
+    #pragma unroll 1
+    for (int p = tid; p < TK; p += nthr) s_inv[p] = -1;
+    sync();
+    #pragma unroll 1
+    for (int p = tid; p < TK; p += nthr) {
+        const int e = s_ids[p];
+        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    }
+    sync();
+    // exclusive scan over experts of (slots, touched experts), packed in one
+    // int (slots < 2^16, experts < 2^15); each thread one contiguous segment
+    const int seg = (E + nthr - 1) / nthr;
+    const int e0 = min(E, tid * seg), e1 = min(E, e0 + seg);
+    int local = 0, nz = 0;
+    #pragma unroll 1
+    for (int e = e0; e < e1; ++e) {
+        local += s_cnt[e];
+        nz += s_cnt[e] > 0 ? 1 : 0;
+    }
+    const int mine = local | (nz << 16);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wsum[wid] = incl;
+    sync();
+    if (tid == 0) {
+        int r = 0;
+        #pragma unroll 1
+        for (int w = 0; w < wpb; ++w) {
+            const int c = s_wsum[w];
+            s_wsum[w] = r;
+            r += c;
+        }
+        s_off[E] = r & 0xffff;
+        P.n = r >> 16;
+    }
+    sync();
+    const int excl = s_wsum[wid] + incl - mine;
+    int run = excl & 0xffff, rank = excl >> 16;
+    #pragma unroll 1
+    for (int e = e0; e < e1; ++e) {
+        s_off[e] = run;
+        if (s_cnt[e] > 0) {
+            P.e[rank] = e;
+            P.off[rank] = run;
+            P.cnt[rank] = s_cnt[e];
+            ++rank;
+        }
+        run += s_cnt[e];
+    }
+    sync();
+    #pragma unroll 1
+    for (int s = s_off[E] + tid; s < TK; s += nthr) P.tok[s] = -1;
+    #pragma unroll 1
+    for (int e = tid; e < E; e += nthr) {
+        const int c = s_cnt[e];
+        if (g.counts) g.counts[e] = c;
+        if (g.offsets) g.offsets[e] = s_off[e];
+        if (c == 0) continue;
+        int slot = s_off[e];
+        #pragma unroll 1
+        for (int p = 0; p < TK; ++p)
+            if (s_ids[p] == e) {
+                s_inv[p] = slot;
+                P.tok[slot] = p / K;
+                if (g.perm) g.perm[slot] = p;
+                ++slot;
+            }
+    }
+    sync();
+    if (tid == 0 && g.offsets) g.offsets[E] = s_off[E];
+    if (g.inv)
+        #pragma unroll 1
+        for (int p = tid; p < TK; p += nthr) g.inv[p] = s_inv[p];
+    if (g.plan) {
+        if (tid == 0) g.plan[0] = P.n;
+        #pragma unroll 1
+        for (int i = tid; i < P.n; i += nthr) {
+            g.plan[kPlanHeader + i] = P.e[i];
+            g.plan[kPlanHeader + E + i] = P.off[i];
+            g.plan[kPlanHeader + 2 * E + i] = P.cnt[i];
+        }
+        #pragma unroll 1
+        for (int s = tid; s < TK; s += nthr) g.plan[kPlanHeader + 3 * E + s] = P.tok[s];
+    }
+}
+
+// ------------------------------------------------------------- selection
+// Order-preserving 32-bit key of a logit: a larger float has a larger key.
+// NaN (and a taken entry) gets key 0, which never wins.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    const uint32_t u = __float_as_uint(v);
+    const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (v == v) ? k : 0u;
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Top-K of one token's logits (larger first, ties to the lower id), written
+// in ascending id to ids[0..K) with renormalised softmax weights w[0..K).
+// One warp.  L: this warp's shared scratch of E words; ex: K floats.
+// A lane keeps the best key of its own logits (ids lane, lane+32, ...); each
+// pick is a warp maximum of the lanes' bests (redux), then the lowest id
+// holding it, after which only the winning lane rescans its own logits.
+__device__ inline void select_topk_warp(const float* lg, int E, int K, float* L, float* ex,
+                                        int* ids, float* w, int lane) {
+    uint32_t* Lk = reinterpret_cast<uint32_t*>(L);
+    for (int e = lane; e < E; e += 32) Lk[e] = logit_key(__ldcg(lg + e));
+    __syncwarp();
+    uint32_t bk = 0u, be = 0x7fffffffu;          // ascending ids: the first maximum stays
+    for (int e = lane; e < E; e += 32) {
+        const uint32_t k = Lk[e];
+        if (be == 0x7fffffffu || k > bk) {
+            bk = k;
+            be = uint32_t(e);
+        }
+    }
+    uint32_t myk = 0u, mye = 0x7fffffffu;
+    for (int k = 0; k < K; ++k) {
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t emin = __reduce_min_sync(0xffffffffu, bk == kmax ? be : 0x7fffffffu);
+        if (lane == k) {
+            myk = kmax;
+            mye = emin;
+        }
+        if (emin < uint32_t(E) && int(emin & 31u) == lane) {
+            Lk[emin] = 0u;
+            bk = 0u;
+            be = 0x7fffffffu;
+            for (int e = lane; e < E; e += 32) {
+                const uint32_t kk = Lk[e];
+                if (be == 0x7fffffffu || kk > bk) {
+                    bk = kk;
+                    be = uint32_t(e);
+                }
+            }
+        }
+    }
+    const float myv = key_logit(myk);
+    const float m = __shfl_sync(0xffffffffu, myv, 0);      // the first pick is the largest
+    int rank = 0;
+    for (int j = 0; j < K; ++j) rank += (__shfl_sync(0xffffffffu, mye, j) < mye) ? 1 : 0;
+    float e_k = 0.0f;
+    if (lane < K) {
+        e_k = expf(myv - m);
+        ex[rank] = e_k;
+        ids[rank] = int(mye);
+    }
+    __syncwarp();
+    float sum = 0.0f;
+    for (int r = 0; r < K; ++r) sum += ex[r];                 // ascending id
+    if (lane < K) w[rank] = e_k / sum;
+    __syncwarp();
+}
+
+// Routing of all T tokens by one CTA into shared memory: s_ids, s_w [T*K],
+// s_sig [T].  forced_ids / forced_w replace the selection when given.
+// scratch: (nthr / 32) * (E + 16) floats.
+template <typename Sync>
+__device__ void route_cta(const float* logits, int T, int E, int K, const int32_t* forced_ids,
+                          const float* forced_w, int* s_ids, float* s_w, float* s_sig,
+                          float* scratch, uint32_t* err, int tid, int nthr, Sync sync) {
+    const int lane = tid & 31, wid = tid >> 5, wpb = nthr >> 5;
+    const int ldl = E + 1;
+    #pragma unroll 1
+    for (int t = wid; t < T; t += wpb) {
+        const float* lg = logits + size_t(t) * ldl;
+        if (forced_ids) {
+            #pragma unroll 1
+            for (int k = lane; k < K; k += 32) {
+                const int id = __ldg(forced_ids + t * K + k);
+                if (id < 0 || id >= E) latch(err, STRATA_EBADROUTE);
+                s_ids[t * K + k] = id;
+                s_w[t * K + k] = __ldg(forced_w + t * K + k);
+            }
+        } else {
+            float* L = scratch + size_t(wid) * (E + 16);
+            select_topk_warp(lg, E, K, L, L + E, s_ids + t * K, s_w + t * K, lane);
+        }
+        if (lane == 0) s_sig[t] = 1.0f / (1.0f + expf(-__ldcg(lg + E)));
+    }
+    sync();
+}
+
+// ---------------------------------------------------------- x activations
+// Lane `lane` owns chunks c = lane + 32 m (m < MC) of a length-H row; a chunk
+// is 32 elements.  Loads token row x (bf16) as fp32 pairs plus chunk sums.
+template <int MC>
+__device__ __forceinline__ void load_x(const uint16_t* xrow, int NC, int lane,
+                                       uint64_t (&x2)[MC][16], float (&X)[MC]) {
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+        const int c = lane + 32 * m;
+        float sum = 0.0f;
+        if (c < NC) {
+            const uint4* p = reinterpret_cast<const uint4*>(xrow + 32 * c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint4 u = ldg_keep(p + v);
+                const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float lo = bf16_lo(wv[i]), hi = bf16_hi(wv[i]);
+                    x2[m][4 * v + i] = pk(lo, hi);
+                    sum += lo + hi;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x2[m][j] = 0ull;
+        }
+        X[m] = sum;
+    }
+}
+
+}  // namespace strata

@@ -26,7 +26,10 @@ _lib = None
 class StrataError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn}: {strata_status_str(status)} ({status})")
+        detail = ""
+        if status == STRATA_ECUDA:
+            detail = f" [{load().strata_last_cuda_error().decode()}]"
+        super().__init__(f"{fn}: {strata_status_str(status)} ({status}){detail}")
 
 
 class Dims(ctypes.Structure):
@@ -73,6 +76,7 @@ def load() -> ctypes.CDLL:
             "moe_layer_forward": (I32, [D, L, P, I32, P, P, P, P, P, SZ, P]),
             "moe_layer_forward_routed": (I32, [D, L, P, I32, P, P, P, P, SZ, P]),
             "moe_block_forward": (I32, [D, L, P, I32, ctypes.c_float, P, P, P, P, P, SZ, P]),
+            "moe_stack_forward": (I32, [D, L, I32, P, I32, ctypes.c_float, P, P, P, P, SZ, P]),
             "moe_decode_route": (I32, [D, L, P, I32, I32, P, SZ, P]),
             "moe_decode_gate_up": (I32, [D, L, P, I32, P, P, P, P, P, P, SZ, P]),
             "moe_decode_down_combine": (I32, [D, L, I32, P, P, P, SZ, P]),
@@ -80,6 +84,7 @@ def load() -> ctypes.CDLL:
             "moe_layer_profile": (I32, [D, L, P, I32, P, P, SZ, P, P, I32, P]),
             "moe_get_device_status": (I32, [P, P]),
             "strata_status_str": (ctypes.c_char_p, [I32]),
+            "strata_last_cuda_error": (ctypes.c_char_p, []),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -92,10 +97,10 @@ def load() -> ctypes.CDLL:
 EXPORTED = ("moe_workspace_bytes", "moe_decode_max_tokens", "moe_rmsnorm", "moe_route",
             "moe_permute", "moe_expert_gate_up", "moe_expert_down", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_routed",
-            "moe_block_forward", "moe_decode_route", "moe_decode_gate_up",
+            "moe_block_forward", "moe_stack_forward", "moe_decode_route", "moe_decode_gate_up",
             "moe_decode_down_combine", "moe_layer_forward_static", "moe_layer_profile",
             "moe_get_device_status",
-            "strata_status_str")
+            "strata_status_str", "strata_last_cuda_error")
 
 
 # ---------------------------------------------------------------- helpers
@@ -247,6 +252,18 @@ def moe_block_forward(dims, layer: DeviceLayer, resid, ws, eps: float = 1e-6, id
         ws.numel(), _stream(stream)))
 
 
+def moe_stack_forward(dims, layers, resid, ws, eps: float = 1e-6, ids=None, weights=None,
+                      out=None, stream=None):
+    """resid (fp32 [T][H], in/out) through every layer of `layers` (DeviceLayer
+    list): x = bf16(rmsnorm(resid)); resid += layer(x).  ids / weights:
+    optional [n_layers][T][K] forced routing."""
+    d = dims_struct(dims)
+    arr = (LayerPtrs * len(layers))(*[dl.ptrs for dl in layers])
+    _check("moe_stack_forward", load().moe_stack_forward(
+        ctypes.byref(d), arr, len(layers), _ptr(resid), resid.shape[0], ctypes.c_float(eps),
+        _ptr(ids), _ptr(weights), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
 def moe_decode_route(dims, layer: DeviceLayer, x, ws, forced: bool = False, stream=None):
     d = dims_struct(dims)
     _check("moe_decode_route", load().moe_decode_route(
@@ -280,7 +297,10 @@ def moe_layer_forward_static(dims, layer: DeviceLayer, x, out, ids=None, weights
         _ptr(weights), _ptr(shared_gate), _ptr(out), _stream(stream)))
 
 
-PROFILE_DECODE = ("k_route", "k_gate_up", "k_down")
+_PHASES = ("router_shared", "barrier_1", "select_bucket", "gate_up_first", "gate_up",
+           "barrier_2", "down", "combine")
+PROFILE_DECODE = (("k_moe_decode",) + _PHASES + tuple("max_" + p for p in _PHASES)
+                  + tuple("min_" + p for p in _PHASES) + ("cta_start_spread", "startup"))
 PROFILE_PREFILL = ("router_gemm", "select", "count", "scan", "scatter", "gather",
                    "gemm_gate_up", "gemm_down", "combine")
 

@@ -312,3 +312,69 @@ def test_stage_calls_equal_layer_forward(lib):
         torch.cuda.synchronize()
         assert torch.equal(out_a, out_b) and torch.equal(ids_a, ids_b)
         assert q.moe_get_device_status(ws2) == q.STRATA_OK
+
+
+def _oracle_stack_forced(dims, planes, r0):
+    """The oracle's stack with its own routing, and the routing as arrays."""
+    rref, recs = oracle.stack_forward(dims, planes, r0)
+    ids = np.stack([rec["ids"] for rec in recs]).astype(np.int32)
+    w = np.stack([rec["w"] for rec in recs]).astype(np.float32)
+    return rref, recs, ids, w
+
+
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_stack_one_kernel_forced(lib, T):
+    """moe_stack_forward (all layers in one persistent kernel) with the
+    oracle's routing forced at every layer: the final residual within
+    tolerance of the oracle's; the last layer's output too."""
+    dims = gen.QWEN
+    layers = [layer(dims, 20 + i) for i in range(4)]
+    planes = [p for p, _ in layers]
+    r0 = gen.draw_tokens(dims, T, 90 + T, "resid")
+    rref, recs, ids, w = _oracle_stack_forced(dims, planes, r0)
+    resid = G.f32(r0)
+    out = torch.empty((T, dims.hidden), dtype=torch.int16, device=G.dev())
+    ws = q.make_workspace(dims, T, G.dev())
+    q.moe_stack_forward(dims, [dl for _, dl in layers], resid, ws, eps=1e-6, ids=G.i32(ids),
+                        weights=G.f32(w), out=out)
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+    G.assert_close(resid.cpu().numpy() - r0, rref - r0, f"4-layer stack T={T}, forced")
+    G.assert_close(G.bf16_to_np(out), oracle.bf16_array_to_f32(recs[-1]["out_bf16"]),
+                   "last layer's output")
+
+
+def test_stack_one_kernel_own_routing(lib):
+    """Routed by the kernel: ids agree with the oracle's, and the residual
+    follows it, over the leading layers in which no token met a near tie."""
+    dims = gen.QWEN
+    layers = [layer(dims, 20 + i) for i in range(4)]
+    planes = [p for p, _ in layers]
+    T = 4
+    r0 = gen.draw_tokens(dims, T, 9, "resid")
+    rref, recs = oracle.stack_forward(dims, planes, r0)
+    n_ok = 0
+    while n_ok < len(recs) and np.all(recs[n_ok]["gap"] >= 3e-3):
+        n_ok += 1
+    assert n_ok >= 1, "pick another seed: the first layer already has a near tie"
+    resid = G.f32(r0)
+    ws = q.make_workspace(dims, T, G.dev())
+    q.moe_stack_forward(dims, [dl for _, dl in layers[:n_ok]], resid, ws, eps=1e-6)
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+    want = r0 + sum(oracle.bf16_array_to_f32(recs[i]["out_bf16"]) for i in range(n_ok))
+    G.assert_close(resid.cpu().numpy() - r0, want - r0, f"{n_ok}-layer stack, own routing")
+
+
+def test_layer_profile_phases(lib):
+    dims = gen.QWEN
+    _, dl = layer(dims, 0)
+    xb = qwen_x(1, 3)
+    ws = q.make_workspace(dims, 1, G.dev())
+    out = torch.empty((1, dims.hidden), dtype=torch.int16, device=G.dev())
+    prof = q.moe_layer_profile(dims, dl, G.u16(xb), out, ws)
+    assert list(prof) == list(q.PROFILE_DECODE)
+    phases = sum(prof[p] for p in q.strata_moe._PHASES)
+    assert 0 < phases <= prof["k_moe_decode"] * 1.05 + 1.0
+    for p in q.strata_moe._PHASES:
+        assert prof["min_" + p] <= prof[p] <= prof["max_" + p]

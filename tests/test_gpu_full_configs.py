@@ -43,12 +43,26 @@ def test_prefill_T2048_zipf_full_size():
         G.assert_close(G.bf16_to_np(out2), ref["out"], "prefill T=2048, forced routing")
 
 
+_STACK = {}
+
+
+def stack_layers(n):
+    """The stack workload's layers (seeds 0..39), and more with the next
+    seeds, drawn once per test session."""
+    dims = gen.QWEN
+    seeds = list(gen.CONFIGS["stack"].seeds)
+    seeds += list(range(seeds[-1] + 1, seeds[-1] + 1 + max(0, n - len(seeds))))
+    for s in seeds[:n]:
+        if s not in _STACK:
+            p = gen.draw_layer(dims, s)
+            _STACK[s] = (p, q.DeviceLayer(p, G.dev()))
+    return [_STACK[s][0] for s in seeds[:n]], [_STACK[s][1] for s in seeds[:n]]
+
+
 @pytest.mark.parametrize("T", [1, 4])
 def test_stack_40_layers(T):
     dims = gen.QWEN
-    cfg = gen.CONFIGS["stack"]
-    planes = [gen.draw_layer(dims, s) for s in cfg.seeds]
-    layers = [q.DeviceLayer(p, G.dev()) for p in planes]
+    planes, layers = stack_layers(40)
     r0 = gen.draw_tokens(dims, T, 1000 + T, "resid")
     rref, recs = oracle.stack_forward(dims, planes, r0)
     ws = q.make_workspace(dims, T, G.dev())
@@ -82,3 +96,52 @@ def test_stack_40_layers(T):
             compared += 1
         aligned = clear
     assert compared >= 5, compared
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_stack_40_layers_one_kernel(T):
+    """The 40-layer stack as the bench times it: one moe_stack_forward call
+    (one persistent kernel), with the oracle's routing forced at every layer,
+    and routed by itself over the leading layers free of near ties."""
+    dims = gen.QWEN
+    planes, layers = stack_layers(40)
+    r0 = gen.draw_tokens(dims, T, 1000 + T, "resid")
+    rref, recs = oracle.stack_forward(dims, planes, r0)
+    ids = np.stack([rec["ids"] for rec in recs]).astype(np.int32)
+    w = np.stack([rec["w"] for rec in recs]).astype(np.float32)
+    ws = q.make_workspace(dims, T, G.dev())
+    resid = G.f32(r0)
+    q.moe_stack_forward(dims, layers, resid, ws, eps=1e-6, ids=G.i32(ids), weights=G.f32(w))
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+    G.assert_close(resid.cpu().numpy() - r0, rref - r0, f"40-layer stack T={T}, one kernel")
+    n_ok = 0
+    while n_ok < len(recs) and np.all(recs[n_ok]["gap"] >= 3e-3):
+        n_ok += 1
+    if n_ok:
+        resid = G.f32(r0)
+        q.moe_stack_forward(dims, layers[:n_ok], resid, ws, eps=1e-6)
+        torch.cuda.synchronize()
+        want = r0 + sum(oracle.bf16_array_to_f32(recs[i]["out_bf16"]) for i in range(n_ok))
+        G.assert_close(resid.cpu().numpy() - r0, want - r0, f"{n_ok} layers, own routing")
+
+
+def test_stack_46_layers_two_launches():
+    """More layers than one launch of the persistent kernel takes (44): the
+    second launch continues from the first one's residual.  46 distinct
+    layers, the oracle's routing forced."""
+    dims = gen.QWEN
+    planes, layers = stack_layers(46)
+    T = 1
+    r0 = gen.draw_tokens(dims, T, 1046, "resid")
+    rref, recs = oracle.stack_forward(dims, planes, r0)
+    ids = np.stack([rec["ids"] for rec in recs]).astype(np.int32)
+    w = np.stack([rec["w"] for rec in recs]).astype(np.float32)
+    ws = q.make_workspace(dims, T, G.dev())
+    resid = G.f32(r0)
+    out = torch.empty((T, dims.hidden), dtype=torch.int16, device=G.dev())
+    q.moe_stack_forward(dims, layers, resid, ws, eps=1e-6, ids=G.i32(ids), weights=G.f32(w),
+                        out=out)
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+    G.assert_close(resid.cpu().numpy() - r0, rref - r0, "46-layer stack, two launches")
