@@ -14,8 +14,7 @@ inputs, bf16 activations):
   decode16  the same with T=16 (8 requests x 2 MTP tokens, cosine-0.9 pairs)
             and a Zipf(1.1) router bias.
   stack     one token (--tokens 1 or 4) through a 40-layer residual MoE stack
-            (one moe_stack_forward call: one persistent kernel for all 40
-            layers, 18.2 GB resident) as one CUDA graph.
+            (one moe_stack_forward call, 18.2 GB resident) as one CUDA graph.
 
 Printed: one JSON line (rank 0).  value = tokens per second through one MoE
 layer (decode1/decode16: layer-tokens / s; stack: tokens / s through all 40
@@ -329,21 +328,61 @@ def run_strata(args, rank, world, local, ctl):
     layer_bytes = mean_touched * expert_bytes(dims) + shared_bytes(dims) + router_bytes(dims)
     gbs = layer_bytes * nl / (ms_step / 1e3) / 1e9
 
-    # the decode layer is one kernel (k_moe_decode): its launches in the timed
-    # region above average ms_step / nl each, gaps between graph nodes
-    # included; the algorithmic bytes of one launch are the layer's touched
-    # experts, the shared expert and the router.  Its phases, from the
-    # kernel's own clock (moe_layer_profile), for the record.
-    dom = "k_moe_decode"
-    dom_us = ms_step * 1e3 / nl
-    dom_bytes = layer_bytes
+    # dominant decode kernel, timed alone: each stage over the 10 layers, with
+    # a workspace per layer so every call sees its own layer's plan
+    wss = [q.make_workspace(dims, T, dev) for _ in range(nl)]
+    v0 = 0
     with torch.cuda.stream(stream):
-        phases = {}
         for li in range(nl):
-            prof = q.moe_layer_profile(dims, layers[li], xs[0][li], outs[li], ws, stream=stream)
-            for k_, v_ in prof.items():
-                phases[k_] = phases.get(k_, 0.0) + v_ / nl
-        phases = {k_: v_ for k_, v_ in phases.items() if not k_.startswith("min_")}
+            q.moe_decode_route(dims, layers[li], xs[v0][li], wss[li], stream=stream)
+            q.moe_decode_gate_up(dims, layers[li], xs[v0][li], wss[li], stream=stream)
+            q.moe_decode_down_combine(dims, layers[li], T, outs[li], wss[li], stream=stream)
+        stream.synchronize()
+        # touched experts of variant 0 per layer (for per-stage bytes)
+        n_act = []
+        for li in range(nl):
+            q.moe_layer_forward(dims, layers[li], xs[v0][li], outs[li], ws, ids=ids_buf,
+                                stream=stream)
+            stream.synchronize()
+            n_act.append(len(np.unique(ids_buf.cpu().numpy())))
+        stages = {
+            "k_route": (lambda li: q.moe_decode_route(dims, layers[li], xs[v0][li], wss[li],
+                                                      stream=stream),
+                        lambda li: router_bytes(dims) + gu_bytes(dims, dims.shared_inter)),
+            "k_gate_up": (lambda li: q.moe_decode_gate_up(dims, layers[li], xs[v0][li], wss[li],
+                                                          stream=stream),
+                          lambda li: n_act[li] * gu_bytes(dims, dims.inter)),
+            "k_down": (lambda li: q.moe_decode_down_combine(dims, layers[li], T, outs[li],
+                                                            wss[li], stream=stream),
+                       lambda li: n_act[li] * dn_bytes(dims, dims.inter)
+                       + dn_bytes(dims, dims.shared_inter)),
+        }
+        # each stage captured as one graph of reps x 10 launches, so host-side
+        # call overhead does not leak into the per-launch time
+        per_stage = {}
+        reps = 50
+        for name, (fn, nbytes) in stages.items():
+            for li in range(nl):
+                fn(li)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for r in range(reps):
+                    for li in range(nl):
+                        fn(li)
+            g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(4):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (4 * reps * nl)
+            per_stage[name] = (us, sum(nbytes(li) for li in range(nl)) / nl)
+    dom = max(per_stage, key=lambda k: per_stage[k][0])
+    dom_us, dom_bytes = per_stage[dom]
     hbm_peak, _, peak_src = measured_peaks()
     achieved = dom_bytes / (dom_us / 1e6) / 1e9
 
@@ -408,15 +447,15 @@ def run_strata(args, rank, world, local, ctl):
             "peak": hbm_peak,
             "unit": "GB/s",
             "frac": achieved / hbm_peak,
-            "peak_source": f"{peak_src} (burst copy)",
+            "peak_source": f"{peak_src} (burst copy, kernel timed alone)",
             "traffic": kernel_traffic(dom),
             "us_per_launch": dom_us,
             "algorithmic_bytes_per_launch": dom_bytes,
-            "phases_us_serialised": {k: round(v, 3) for k, v in phases.items()},
+            "stages_us": {k: round(v[0], 3) for k, v in per_stage.items()},
         },
         "clocks": clocks.summary(),
         "e2e": e2e,
-        "gpu_launches": args.steps * nl,
+        "gpu_launches": args.steps * nl * 3,
     }
     return result, (dims, planes, xs, nl)
 
@@ -615,8 +654,8 @@ def run_stack_line(args, rank, world, local, ctl):
     step_bytes = touched * expert_bytes(dims) + nl * (shared_bytes(dims) + router_bytes(dims))
     gbs = step_bytes / (ms / 1e3) / 1e9
     hbm, _, src = measured_peaks()
-    # per step: the residual reset (a copy kernel) and the stack kernel(s)
-    launches = 1 + (1 if T <= 32 else nl * 11)
+    # per step: the residual reset (a copy kernel) and each layer's kernels
+    launches = 1 + nl * (4 if T <= 32 else 11)
     return {
         "metric": METRIC,
         "value": T * world / (ms / 1e3),

@@ -33,8 +33,7 @@
  *   - Kernels never trap.  A forced expert id outside [0, E) is skipped and
  *     latches STRATA_EBADROUTE in the workspace's error word; a bounded wait
  *     that runs out latches STRATA_ETIMEOUT.  moe_get_device_status reads and
- *     clears the word (and the decode kernel's grid-barrier word, which a
- *     wait that ran out can leave mid-way).
+ *     clears the word.
  *   - Results are deterministic: ids, permutations and every floating sum are
  *     computed in a fixed order, with no floating-point atomics.
  *
@@ -188,10 +187,9 @@ STRATA_API strata_status moe_combine(const strata_moe_dims* dims, const strata_m
                           size_t ws_bytes, void* stream);
 
 /* The whole layer: route, permute, experts, shared expert, combine.  For
- * T <= moe_decode_max_tokens() it is one persistent cooperative kernel (one
- * CTA per SM; router + shared gate/up, then selection, bucketing and routed
- * gate/up, then every down product + combine, with a grid barrier between
- * the phases); above, the tcgen05 prefill kernels.
+ * T <= moe_decode_max_tokens() it runs three decode kernels (router + shared
+ * gate/up in one; selection, bucketing and routed gate/up in one; every down
+ * product + combine in one); above, the tcgen05 prefill kernels.
  * ids_dev / weights_dev / shared_gate_dev receive the routing when non-NULL.
  * out_dev bf16 [T][H]. */
 STRATA_API strata_status moe_layer_forward(const strata_moe_dims* dims, const strata_moe_layer* layer,
@@ -223,13 +221,9 @@ STRATA_API strata_status moe_block_forward(const strata_moe_dims* dims, const st
  * read during the call only.  resid_dev fp32 [T][H] (in/out); ids_dev /
  * weights_dev: NULL to route every layer, or both int32 / fp32
  * [n_layers][T][K] to force the routing; out_dev: NULL or bf16 [T][H], the
- * last layer's output.  For T <= moe_decode_max_tokens()
- * up to 44 layers run as one persistent kernel (Strata, "Qwen3.6-35B-A3B:
- * pictures, several requests at once and speed", section "Speed": the
- * launches of a decode step are what the time goes to); above, one
- * moe_block_forward per layer.  The RMSNorm sums of squares of layers after
- * the first are summed per block of rows and then over the blocks, so an
- * input element may differ from moe_rmsnorm's by one bf16 ulp. */
+ * last layer's output.  One moe_block_forward per layer, all enqueued by
+ * this call ("qwen36: CUDA VRAM expert tier", section "Placement": a token's
+ * routed experts are 40 layers of top-8). */
 STRATA_API strata_status moe_stack_forward(const strata_moe_dims* dims,
                                            const strata_moe_layer* layers, int32_t n_layers,
                                            float* resid_dev, int32_t T, float eps,
@@ -237,8 +231,8 @@ STRATA_API strata_status moe_stack_forward(const strata_moe_dims* dims,
                                            void* out_dev, void* ws_dev, size_t ws_bytes,
                                            void* stream);
 
-/* The decode path (T <= moe_decode_max_tokens()) as three kernels and
- * separate calls, the same arithmetic as moe_layer_forward's single kernel.  They pass their
+/* The three kernels of the decode path (T <= moe_decode_max_tokens()), as
+ * separate calls; moe_layer_forward is the three in a row.  They pass their
  * state through the workspace (logits, the shared expert's SwiGLU vectors,
  * the routing, the bucketing and a plan of the touched experts, the routed
  * SwiGLU vectors), so they take the same workspace and T, in this order.
@@ -300,15 +294,9 @@ STRATA_API strata_status moe_layer_forward_static(const strata_moe_dims* dims,
  * every kernel launch, synchronises `stream`, and writes each kernel's
  * duration in microseconds to us[0..max_n) in launch order; *n_out gets the
  * number of kernels.  The events serialise the kernels, so each duration is
- * the kernel alone.  Decode (T <= moe_decode_max_tokens()): the one kernel,
- * then eight phases of it from the CTAs' clocks (%globaltimer): router and
- * shared gate/up, grid barrier, selection and bucketing, wait for the first
- * routed gate/up weights, routed gate/up, grid barrier, down products,
- * combine -- as CTA 0 saw them, then the slowest and the fastest CTA's
- * time for each -- then the spread of the CTAs' start times and CTA 0's
- * time from its start to its first phase; *n_out = 27.  Prefill: router
- * GEMM, top-K, count, scan, scatter, gather, gate/up GEMM, down GEMM,
- * combine. */
+ * the kernel alone.  Order: decode (T <= moe_decode_max_tokens()): route,
+ * gate/up, down+combine; prefill: router GEMM, top-K, count, scan, scatter,
+ * gather, gate/up GEMM, down GEMM, combine. */
 STRATA_API strata_status moe_layer_profile(const strata_moe_dims* dims,
                                            const strata_moe_layer* layer, const void* x_dev,
                                            int32_t T, void* out_dev, void* ws_dev,

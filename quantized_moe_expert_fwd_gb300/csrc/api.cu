@@ -3,7 +3,6 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
-#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -37,8 +36,6 @@ WsLayout ws_layout(const strata_moe_dims& d, int T) {
         L.plan = take((kPlanHeader + 3 * E + t * K) * 4);
         L.h = take(t * K * I * 4);
         L.hs = take(t * Is * 4);
-        L.ssq = take(size_t(kFxMaxGrid) * t * 4);
-        L.stamps = take((size_t(kFxMaxGrid) * kFxStampsPerLayer + 256) * 8);
     } else {
         const size_t nblk = (t + 31) / 32;
         const size_t max_mb = (t * K) / kBM + E + t / kBM + 2;
@@ -233,54 +230,17 @@ strata_status stage_down(const strata_moe_dims* d, const strata_moe_layer* L, in
     return cuda_status(launch_down_decode(dn, s));
 }
 
-// Layers on the persistent decode kernel (T <= kDecodeMaxTokens).  x: the
-// bf16 input of a single layer, or NULL with resid: every layer's input is
-// bf16(rmsnorm(resid, eps)) and resid += its output.  forced_ids/forced_w
-// and the routing copies apply to a single layer.  stamps: record the
-// kernel's phase clock of CTA 0 in the workspace.
-strata_status fused_layers(const strata_moe_dims* d, const strata_moe_layer* layers, int n,
-                           const void* x, float* resid, float eps, int T,
-                           const int32_t* forced_ids, const float* forced_w, int32_t* ids_user,
-                           float* w_user, float* sig_user, void* out, void* x_out, void* ws,
-                           cudaStream_t s, bool stamps) {
-    if (n < 1 || n > kFxMaxLayers) return STRATA_EINVAL;
-    const WsLayout W = ws_layout(*d, T);
-    FusedLaunch a{};
-    for (int l = 0; l < n; ++l) a.layers[l] = layers[l];
-    a.n_layers = n;
-    a.x = static_cast<const uint16_t*>(x);
-    a.resid = resid;
-    a.eps = eps;
-    a.forced_ids = forced_ids;
-    a.forced_w = forced_w;
-    a.ids_user = ids_user;
-    a.w_user = w_user;
-    a.sig_user = sig_user;
-    a.out = static_cast<uint16_t*>(out);
-    a.x_out = static_cast<uint16_t*>(x_out);
-    a.logits = at<float>(ws, W.logits);
-    a.hs = at<float>(ws, W.hs);
-    a.h = at<float>(ws, W.h);
-    a.ssq = at<float>(ws, W.ssq);
-    a.err = &at<Ctl>(ws, W.ctl)->err;
-    a.bar = &at<Ctl>(ws, W.ctl)->bar;
-    a.stamps = stamps ? at<unsigned long long>(ws, W.stamps) : nullptr;
-    a.T = T;
-    a.H = d->hidden;
-    a.E = d->n_experts;
-    a.K = d->top_k;
-    a.I = d->inter;
-    a.Is = d->shared_inter;
-    return cuda_status(launch_fused_decode(a, s));
-}
-
-// One layer on the decode kernel.  forced_ids/forced_w: NULL to route.
+// One layer on the decode kernels.  forced_ids/forced_w: NULL to route.
+// resid: NULL, or the residual that gets += the bf16 output.
 strata_status decode_layer(const strata_moe_dims* d, const strata_moe_layer* L, const void* x,
                            int T, const int32_t* forced_ids, const float* forced_w,
                            int32_t* ids_user, float* w_user, float* sig_user, void* out,
-                           void* ws, cudaStream_t s, bool stamps = false) {
-    return fused_layers(d, L, 1, x, nullptr, 0.0f, T, forced_ids, forced_w, ids_user, w_user,
-                        sig_user, out, nullptr, ws, s, stamps);
+                           float* resid, void* ws, cudaStream_t s) {
+    strata_status st = stage_route(d, L, x, T, forced_ids != nullptr, ws, s);
+    if (st != STRATA_OK) return st;
+    st = stage_gate_up(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, ws, s);
+    if (st != STRATA_OK) return st;
+    return stage_down(d, L, T, out, resid, ws, s);
 }
 
 // One layer on the prefill (tcgen05) kernels.
@@ -434,10 +394,9 @@ strata_status any_layer(const strata_moe_dims* d, const strata_moe_layer* L, con
                         const int32_t* forced_ids, const float* forced_w, int32_t* ids_user,
                         float* w_user, float* sig_user, void* out, float* resid, void* ws,
                         cudaStream_t s) {
-    if (T <= kDecodeMaxTokens && resid == nullptr)
+    if (T <= kDecodeMaxTokens)
         return decode_layer(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, out,
-                            ws, s);
-    if (T <= kDecodeMaxTokens) return STRATA_EINVAL;
+                            resid, ws, s);
     return prefill_layer(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, out, resid,
                          ws, s);
 }
@@ -757,9 +716,6 @@ strata_status moe_block_forward(const strata_moe_dims* dims, const strata_moe_la
         return STRATA_EINVAL;
     const WsLayout W = ws_layout(*dims, T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (T <= kDecodeMaxTokens)
-        return fused_layers(dims, layer, 1, nullptr, resid_dev, eps, T, ids_dev, weights_dev,
-                            nullptr, nullptr, nullptr, out_dev, x_out_dev, ws_dev, s, false);
     void* x = x_out_dev ? x_out_dev : at<void>(ws_dev, W.x);
     void* out = out_dev ? out_dev : at<void>(ws_dev, W.out);
     STRATA_TRY(launch_rmsnorm(resid_dev, T, dims->hidden, eps, static_cast<uint16_t*>(x), s));
@@ -780,24 +736,12 @@ strata_status moe_stack_forward(const strata_moe_dims* dims, const strata_moe_la
         (ids_dev == nullptr) != (weights_dev == nullptr) || !opt4(ids_dev) ||
         !opt4(weights_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t TK = size_t(T) * dims->top_k;
-    if (T > kDecodeMaxTokens) {
-        for (int l = 0; l < n_layers; ++l) {
-            const strata_status st = moe_block_forward(
-                dims, layers + l, resid_dev, T, eps, ids_dev ? ids_dev + l * TK : nullptr,
-                weights_dev ? weights_dev + l * TK : nullptr, nullptr,
-                l + 1 == n_layers ? out_dev : nullptr, ws_dev, ws_bytes, stream);
-            if (st != STRATA_OK) return st;
-        }
-        return STRATA_OK;
-    }
-    for (int l0 = 0; l0 < n_layers; l0 += kFxMaxLayers) {
-        const int n = n_layers - l0 < kFxMaxLayers ? n_layers - l0 : kFxMaxLayers;
-        const strata_status st = fused_layers(
-            dims, layers + l0, n, nullptr, resid_dev, eps, T, ids_dev ? ids_dev + l0 * TK : nullptr,
-            weights_dev ? weights_dev + l0 * TK : nullptr, nullptr, nullptr, nullptr,
-            l0 + n == n_layers ? out_dev : nullptr, nullptr, ws_dev, s, false);
+    for (int l = 0; l < n_layers; ++l) {
+        const strata_status st = moe_block_forward(
+            dims, layers + l, resid_dev, T, eps, ids_dev ? ids_dev + l * TK : nullptr,
+            weights_dev ? weights_dev + l * TK : nullptr, nullptr,
+            l + 1 == n_layers ? out_dev : nullptr, ws_dev, ws_bytes, stream);
         if (st != STRATA_OK) return st;
     }
     return STRATA_OK;
@@ -857,12 +801,8 @@ strata_status moe_layer_profile(const strata_moe_dims* dims, const strata_moe_la
     if (cudaEventCreate(&start) != cudaSuccess) return STRATA_ECUDA;
     cudaEventRecord(start, s);
     t_prof = &prof;
-    const bool dec = T <= kDecodeMaxTokens;
-    const strata_status st =
-        dec ? decode_layer(dims, layer, x_dev, T, nullptr, nullptr, nullptr, nullptr, nullptr,
-                           out_dev, ws_dev, s, true)
-            : any_layer(dims, layer, x_dev, T, nullptr, nullptr, nullptr, nullptr, nullptr,
-                        out_dev, nullptr, ws_dev, s);
+    const strata_status st = any_layer(dims, layer, x_dev, T, nullptr, nullptr, nullptr, nullptr,
+                                       nullptr, out_dev, nullptr, ws_dev, s);
     t_prof = nullptr;
     strata_status rc = st;
     if (cudaStreamSynchronize(s) != cudaSuccess) rc = STRATA_ECUDA;
@@ -875,53 +815,7 @@ strata_status moe_layer_profile(const strata_moe_dims* dims, const strata_moe_la
         if (n < max_n) us[n++] = ms * 1000.0f;
         prev = prof.ev[i];
     }
-    int total = prof.n;
-    if (dec && rc == STRATA_OK) {
-        // the decode kernel's phases from every CTA's clock: CTA 0's, the
-        // slowest CTA's and the fastest CTA's, then the spread of the CTAs'
-        // start times and CTA 0's start-up before its first phase
-        const int G = device_info().sms < kFxMaxGrid ? device_info().sms : kFxMaxGrid;
-        std::vector<unsigned long long> st(size_t(G) * kFxStampsPerLayer);
-        const WsLayout W = ws_layout(*dims, T);
-        if (cudaMemcpy(st.data(), at<unsigned long long>(ws_dev, W.stamps),
-                       st.size() * sizeof(unsigned long long),
-                       cudaMemcpyDeviceToHost) != cudaSuccess)
-            rc = STRATA_ECUDA;
-        // stamp order: 0 layer start, 1 A done, 2 barrier, 3 routed, 8 first
-        // gate/up chunk, 4 gate/up done, 5 barrier, 6 down done, 7 combined
-        static const int kOrder[9] = {0, 1, 2, 3, 8, 4, 5, 6, 7};
-        float ph[3][8];
-        for (int i = 0; i < 8; ++i) {
-            ph[0][i] = 0.0f;
-            ph[1][i] = 0.0f;
-            ph[2][i] = 3.4e38f;
-        }
-        unsigned long long s_min = ~0ull, s_max = 0;
-        for (int c = 0; c < G && rc == STRATA_OK; ++c) {
-            const unsigned long long* sc = st.data() + size_t(c) * kFxStampsPerLayer;
-            for (int i = 0; i < 8; ++i) {
-                const float d = float(double(sc[kOrder[i + 1]] - sc[kOrder[i]]) * 1e-3);
-                if (c == 0) ph[0][i] = d;
-                ph[1][i] = d > ph[1][i] ? d : ph[1][i];
-                ph[2][i] = d < ph[2][i] ? d : ph[2][i];
-            }
-            s_min = sc[9] < s_min ? sc[9] : s_min;
-            s_max = sc[9] > s_max ? sc[9] : s_max;
-        }
-        if (rc == STRATA_OK) {
-            for (int r = 0; r < 3; ++r)
-                for (int i = 0; i < 8; ++i) {
-                    if (n < max_n) us[n++] = ph[r][i];
-                    ++total;
-                }
-            const float extra[2] = {float(double(s_max - s_min) * 1e-3),
-                                    float(double(st[0] - st[9]) * 1e-3)};
-            for (int i = 0; i < 2; ++i) {
-                if (n < max_n) us[n++] = extra[i];
-                ++total;
-            }
-        }
-    }
+    const int total = prof.n;
     for (int i = 0; i < prof.n; ++i) cudaEventDestroy(prof.ev[i]);
     cudaEventDestroy(start);
     *n_out = total;
@@ -937,9 +831,6 @@ strata_status moe_get_device_status(void* ws_dev, void* stream) {
     if (cudaMemcpyAsync(&word, &ctl->err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return STRATA_ECUDA;
     if (cudaMemsetAsync(&ctl->err, 0, sizeof(uint32_t), s) != cudaSuccess) return STRATA_ECUDA;
-    // a wait that ran out may have left the grid barrier word mid-way; at rest
-    // its low bits are 0, so clearing it is always safe
-    if (cudaMemsetAsync(&ctl->bar, 0, sizeof(uint32_t), s) != cudaSuccess) return STRATA_ECUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return STRATA_ECUDA;
     return static_cast<strata_status>(word);
 }
@@ -1008,9 +899,9 @@ extern "C" strata_status moe_layer_forward_static(const strata_moe_dims* dims,
     void* ws = static_ws_address();
     if (ws == nullptr) return STRATA_ECUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the error and grid-barrier words must start at zero; every other
-    // region is written before it is read
+    // the error word must start at zero; every other region is written
+    // before it is read
     if (cudaMemsetAsync(ws, 0, sizeof(Ctl), s) != cudaSuccess) return STRATA_ECUDA;
     return decode_layer(dims, layer, x_dev, T, nullptr, nullptr, ids_dev, weights_dev,
-                        shared_gate_dev, out_dev, ws, s);
+                        shared_gate_dev, out_dev, nullptr, ws, s);
 }

@@ -12,8 +12,7 @@ constexpr int kWarp = 32;
 struct Ctl {
     uint32_t err;       // latched strata_status (first error wins)
     uint32_t where[7];  // first timed-out wait: site, block, warp, slot, round, item, 1
-    uint32_t bar;       // grid barrier of the persistent decode kernel (low 31 bits 0 at rest)
-    uint32_t pad[55];
+    uint32_t pad[56];
 };
 
 __device__ __forceinline__ void latch(uint32_t* err, uint32_t code) {
@@ -206,6 +205,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// Explicit shared-memory loads by 32-bit shared address: used where a
+// pointer reaches a non-inlined routine, which would otherwise read shared
+// memory through generic addressing.  volatile keeps them after the waits
+// that make the data ready.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ int lds_s32(uint32_t a) {
+    int v;
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
 // dst, src 16-byte aligned; bytes a multiple of 16
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {

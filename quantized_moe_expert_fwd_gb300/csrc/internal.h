@@ -43,7 +43,7 @@ struct MBlock {
 // prefill ones (per-block counts, row blocks, fp16 operands, bf16 outputs)
 // for larger T.
 struct WsLayout {
-    size_t ctl, logits, ids, w, sig, counts, offsets, perm, inv, plan, h, hs, x, out, ssq, stamps;
+    size_t ctl, logits, ids, w, sig, counts, offsets, perm, inv, plan, h, hs, x, out;
     size_t cnt_blk, base_blk, mblocks, n_mblocks, xg, h16, hs16, y, ysh;
     size_t total;
 };
@@ -113,30 +113,6 @@ struct DownLaunch {
     int stages;                       // set by the launcher
 };
 cudaError_t launch_down_decode(DownLaunch a, cudaStream_t s);
-
-// One persistent kernel for a decode-size layer, or for a stack of layers
-// with RMSNorm and the residual between them.
-constexpr int kFxMaxLayers = 44;      // keeps the launch's parameters within 4 KB
-constexpr int kFxMaxSlots = 16;
-constexpr int kFxMaxGrid = 1024;
-constexpr int kFxStampsPerLayer = 16;     // clock reads of one CTA (first layer)
-struct FusedLaunch {
-    strata_moe_layer layers[kFxMaxLayers];
-    int n_layers;
-    const uint16_t* x;                // bf16 [T][H] input of a single layer, or NULL
-    float* resid; float eps;          // NULL x: x = bf16(rmsnorm(resid)); resid += out each layer
-    const int32_t* forced_ids; const float* forced_w;   // [n_layers][T][K] or NULL
-    int32_t* ids_user; float* w_user; float* sig_user;  // single layer only
-    uint16_t* out;                    // bf16 [T][H] output of the last layer, or NULL
-    uint16_t* x_out;                  // bf16 [T][H] input of the first layer, or NULL
-    float* logits; float* hs; float* h; float* ssq;     // workspace
-    uint32_t* err; uint32_t* bar;
-    unsigned long long* stamps;       // NULL, or kFxStampsPerLayer clock reads per CTA
-    int T, H, E, K, I, Is;
-    // geometry, set by the launcher
-    int slots, slot_bytes, stage_q, pb, rr, uc, ub, og;
-};
-cudaError_t launch_fused_decode(FusedLaunch& a, cudaStream_t s);
 
 cudaError_t launch_plan(const int32_t* offsets, const int32_t* perm, int T, int K, int E,
                         int32_t* plan, uint32_t* err, cudaStream_t s);

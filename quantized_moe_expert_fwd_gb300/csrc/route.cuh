@@ -188,7 +188,16 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
 __device__ inline void select_topk_warp(const float* lg, int E, int K, float* L, float* ex,
                                         int* ids, float* w, int lane) {
     uint32_t* Lk = reinterpret_cast<uint32_t*>(L);
-    for (int e = lane; e < E; e += 32) Lk[e] = logit_key(__ldcg(lg + e));
+    // the logits come from L2: eight loads in flight a round trip
+#pragma unroll 1
+    for (int e0 = lane; e0 < E; e0 += 8 * 32) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = (e0 + 32 * j < E) ? __ldcg(lg + e0 + 32 * j) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (e0 + 32 * j < E) Lk[e0 + 32 * j] = logit_key(v[j]);
+    }
     __syncwarp();
     uint32_t bk = 0u, be = 0x7fffffffu;          // ascending ids: the first maximum stays
     for (int e = lane; e < E; e += 32) {

@@ -297,10 +297,7 @@ def moe_layer_forward_static(dims, layer: DeviceLayer, x, out, ids=None, weights
         _ptr(weights), _ptr(shared_gate), _ptr(out), _stream(stream)))
 
 
-_PHASES = ("router_shared", "barrier_1", "select_bucket", "gate_up_first", "gate_up",
-           "barrier_2", "down", "combine")
-PROFILE_DECODE = (("k_moe_decode",) + _PHASES + tuple("max_" + p for p in _PHASES)
-                  + tuple("min_" + p for p in _PHASES) + ("cta_start_spread", "startup"))
+PROFILE_DECODE = ("k_route", "k_gate_up", "k_down")
 PROFILE_PREFILL = ("router_gemm", "select", "count", "scan", "scatter", "gather",
                    "gemm_gate_up", "gemm_down", "combine")
 

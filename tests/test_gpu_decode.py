@@ -323,10 +323,10 @@ def _oracle_stack_forced(dims, planes, r0):
 
 
 @pytest.mark.parametrize("T", [1, 4, 16])
-def test_stack_one_kernel_forced(lib, T):
-    """moe_stack_forward (all layers in one persistent kernel) with the
-    oracle's routing forced at every layer: the final residual within
-    tolerance of the oracle's; the last layer's output too."""
+def test_stack_call_forced(lib, T):
+    """moe_stack_forward with the oracle's routing forced at every layer: the
+    final residual within tolerance of the oracle's; the last layer's output
+    too."""
     dims = gen.QWEN
     layers = [layer(dims, 20 + i) for i in range(4)]
     planes = [p for p, _ in layers]
@@ -344,7 +344,7 @@ def test_stack_one_kernel_forced(lib, T):
                    "last layer's output")
 
 
-def test_stack_one_kernel_own_routing(lib):
+def test_stack_call_own_routing(lib):
     """Routed by the kernel: ids agree with the oracle's, and the residual
     follows it, over the leading layers in which no token met a near tie."""
     dims = gen.QWEN
@@ -366,7 +366,7 @@ def test_stack_one_kernel_own_routing(lib):
     G.assert_close(resid.cpu().numpy() - r0, want - r0, f"{n_ok}-layer stack, own routing")
 
 
-def test_layer_profile_phases(lib):
+def test_layer_profile_kernels(lib):
     dims = gen.QWEN
     _, dl = layer(dims, 0)
     xb = qwen_x(1, 3)
@@ -374,7 +374,4 @@ def test_layer_profile_phases(lib):
     out = torch.empty((1, dims.hidden), dtype=torch.int16, device=G.dev())
     prof = q.moe_layer_profile(dims, dl, G.u16(xb), out, ws)
     assert list(prof) == list(q.PROFILE_DECODE)
-    phases = sum(prof[p] for p in q.strata_moe._PHASES)
-    assert 0 < phases <= prof["k_moe_decode"] * 1.05 + 1.0
-    for p in q.strata_moe._PHASES:
-        assert prof["min_" + p] <= prof[p] <= prof["max_" + p]
+    assert all(v > 0 for v in prof.values())
