@@ -926,105 +926,6 @@ cudaError_t launch_prefill_pack(const float* src, long long n, __half* dst, cuda
     return launch_pdl(k_pf_pack, int((n8 + 255) / 256), 256, 0, s, src, n8, dst);
 }
 
-cudaError_t launch_prefill_gate_up(const PfExperts& p, cudaStream_t s) {
-    const int T = p.T, K = p.K, H = p.H, I = p.I, Is = p.Is, E = p.E;
-    // A = xg [xg_rows][H]; B = interleaved gate/up rows.  A weight set the
-    // block list cannot name gets the other set's maps.
-    CUtensorMap ma, mq, ms, mq2, ms2;
-    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.xg, H, p.xg_rows, kBK, kBM, true))
-        return cudaErrorInvalidValue;
-    if (p.routed &&
-        (!make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.gu_q, H / 2, uint64_t(E) * 2 * I,
-                   kBK / 2, 256, false) ||
-         !make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.gu_s, H / 32, uint64_t(E) * 2 * I,
-                   H / 32, 256, false)))
-        return cudaErrorInvalidValue;
-    if (p.shared &&
-        (!make_map(&mq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_gu_q, H / 2, 2 * Is, kBK / 2, 256,
-                   false) ||
-         !make_map(&ms2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.sh_gu_s, H / 32, 2 * Is, H / 32, 256,
-                   false)))
-        return cudaErrorInvalidValue;
-    if (!p.routed) {
-        mq = mq2;
-        ms = ms2;
-    }
-    if (!p.shared) {
-        mq2 = mq;
-        ms2 = ms;
-    }
-    GemmLaunch g{};
-    g.BN = 256;
-    g.N = 2 * I;
-    g.N2 = 2 * Is;
-    g.K = H;
-    g.K2 = H;
-    g.K_max = H;
-    g.E = E;
-    g.mblocks = p.mblocks;
-    g.n_mblocks = p.n_mblocks;
-    g.nb_max = (2 * (I > Is ? I : Is)) / 256;
-    g.a_shared_row0 = p.xg_shared_row0;
-    g.out_f16 = p.h;
-    g.out_f32 = p.h_f32;
-    g.ldo = I;
-    g.out2_f16 = p.hs;
-    g.ld2 = Is;
-    g.err = p.err;
-    (void)T;
-    (void)K;
-    return run_gemm<kGemmGateUp>(g, ma, ma, mq, ms, mq2, ms2, s);
-}
-
-cudaError_t launch_prefill_down(const PfExperts& p, cudaStream_t s) {
-    const int T = p.T, K = p.K, H = p.H, I = p.I, Is = p.Is, E = p.E;
-    // A = h [T*K][I] (routed) or hs [T][Is] (shared); B = down rows
-    CUtensorMap da, da2, dq, ds, dq2, ds2;
-    if (p.routed &&
-        (!make_map(&da, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.h, I, uint64_t(T) * K, kBK, kBM,
-                   true) ||
-         !make_map(&dq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.dn_q, I / 2, uint64_t(E) * H, kBK / 2,
-                   256, false) ||
-         !make_map(&ds, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.dn_s, I / 32, uint64_t(E) * H, I / 32,
-                   256, false)))
-        return cudaErrorInvalidValue;
-    if (p.shared &&
-        (!make_map(&da2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.hs, Is, T, kBK, kBM, true) ||
-         !make_map(&dq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_dn_q, Is / 2, H, kBK / 2, 256,
-                   false) ||
-         !make_map(&ds2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.sh_dn_s, Is / 32, H, Is / 32, 256,
-                   false)))
-        return cudaErrorInvalidValue;
-    if (!p.routed) {
-        da = da2;
-        dq = dq2;
-        ds = ds2;
-    }
-    if (!p.shared) {
-        da2 = da;
-        dq2 = dq;
-        ds2 = ds;
-    }
-    GemmLaunch d{};
-    d.BN = 256;
-    d.N = H;
-    d.N2 = H;
-    d.K = I;
-    d.K2 = Is;
-    d.K_max = I > Is ? I : Is;
-    d.E = E;
-    d.mblocks = p.mblocks;
-    d.n_mblocks = p.n_mblocks;
-    d.nb_max = H / 256;
-    d.a_shared_row0 = 0;
-    d.out_f16 = p.y;
-    d.out_bf16 = p.y_bf16;
-    d.out2_f16 = p.ysh;
-    d.ldo = H;
-    d.err = p.err;
-    return run_gemm<kGemmDown>(d, da, da2, dq, ds, dq2, ds2, s);
-}
-
 cudaError_t launch_prefill_experts(const PfExperts& p, cudaStream_t s) {
     cudaError_t e = launch_prefill_gather(p.x, p.perm, p.T, p.K, p.H, p.xg, p.xg_rows, s);
     if (e != cudaSuccess) return e;

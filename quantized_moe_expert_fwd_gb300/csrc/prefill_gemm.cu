@@ -1,0 +1,534 @@
+// prefill_gemm.cu -- the prefill experts' grouped GEMMs with the weights as
+// the tensor cores' A operand in tensor memory (swap AB).
+//
+// Each tile is 128 weight rows (of one expert, or of the shared expert) by
+// the n <= 128 token rows of one block of that expert, over the full K:
+//   D[w][t] = sum_k W[w][k] X[t][k]         (fp32 in TMEM, 128 lanes x n cols)
+// The int4 weights are dequantised by four warps straight from the packed
+// bytes into registers and stored into tensor memory with tcgen05.st, where
+// the MMA reads them as its A operand: no dequantised tile goes through
+// shared memory, and N follows the expert's token count (rounded up to 16)
+// instead of padding every expert to 128 rows.  The activations (B) come by
+// TMA into 128-byte-swizzled shared memory, 32 rows a box, as many boxes as
+// the block has rows.
+//
+// Warps: 0 TMA producer; 1 TMEM allocation and (lane 0) the MMAs; 2..9
+// dequantisation, two sets of four taking alternate K blocks (warp w owns
+// TMEM lanes 32 (w % 4) .. +32: weight rows); 10..13 epilogue (the same lane
+// quarters): SwiGLU of gate/up row pairs (rows 2i, 2i+1 sit in neighbouring
+// lanes) or the down product's outputs.
+// Accumulators are double-buffered (2 x 128 columns) so a tile's epilogue
+// overlaps the next tile's MMAs; the dequantised A stages take 4 x 64
+// columns.  A pipeline stage is K = 128 (eight MMAs), so the per-stage
+// bookkeeping of the single-thread roles (waits, commits, TMA issue) is
+// spread over enough tensor work even for experts with few tokens.
+//
+// The pages found a fused dequantise + matrix-unit kernel losing to
+// dequantise-then-library-GEMM when the two did not overlap (Strata, "Strata
+// on an Intel Arc", section "The engine itself on Intel: the SYCL port");
+// here the dequantisation of stage k + 1 runs while the MMA eats stage k.
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace strata {
+
+constexpr int kSabThreads = 448;
+constexpr int kSabDeqSets = 2;           // dequantisation warp sets: K blocks alternate
+constexpr int kSabKS = 128;              // K of one pipeline stage: 8 MMAs of K = 16
+constexpr int kSabStages = 4;            // activation stages = dequantised A stages
+constexpr int kSabACols = kSabKS / 2;    // TMEM columns of one A stage (two fp16 a column)
+constexpr int kSabDCols = 128;           // one accumulator buffer: up to 128 token columns
+constexpr int kSabACol0 = 2 * kSabDCols; // first A column
+constexpr int kSabTmemCols = 512;
+constexpr int kSabBoxRows = 32;          // activation rows per TMA box
+constexpr uint32_t kSabSubBytes = kBM * 128u;          // 128 rows x 64 fp16 (one MMA K block)
+constexpr uint32_t kSabStageBytes = 2 * kSabSubBytes;  // K = 128: two 64-wide sub-blocks
+// Weight stages: 128 rows x 128 packed bytes = 256 inputs = 2 pipeline
+// stages, one TMA box with the 128-byte swizzle, so every row is read from
+// memory as a whole 128-byte line and a lane's 16-byte reads of its row are
+// spread over the banks.
+constexpr uint32_t kSabWBytes = kBM * 128u;
+constexpr int kSabWStages = 3;
+static_assert(kSabStages * kSabACols + kSabACol0 <= kSabTmemCols, "TMEM columns");
+
+__host__ __device__ inline uint32_t sab_scale_bytes(int K_max) {
+    return uint32_t(kBM) * uint32_t(K_max / 32) * 2u;
+}
+
+// 64 fp16 weights of one row for one K block: 32 packed bytes, two scales
+// -> 32 registers holding the MMA-order pairs, register c = K positions
+// (2c, 2c+1).  Within every 8 elements the positions hold elements
+// [0,4,1,5,2,6,3,7]: one LOP3 per pair (the activations are stored in the
+// same order, so the products are the natural ones).
+__device__ __forceinline__ void dequant_row_regs(const uint4& w0, const uint4& w1, uint32_t sc2,
+                                                 uint32_t (&r)[32]) {
+    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    const __half s0 = __ushort_as_half(uint16_t(sc2 & 0xffffu));
+    const __half s1 = __ushort_as_half(uint16_t(sc2 >> 16));
+    const __half2 sA = __halves2half2(s0, s0), sB = __halves2half2(s1, s1);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const __half2 s = (c < 4) ? sA : sB;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t b = ((words[c] >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
+            const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&b), off);   // exact
+            const __half2 v = __hmul2(q, s);
+            r[4 * c + j] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+    }
+}
+
+// Position of element e (within its group of 8) in the MMA order above.
+__device__ __forceinline__ int mma_pos(int i) {
+    const int e = i & 7;
+    return (i & ~7) | ((e & 3) * 2 + (e >> 2));
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kSabThreads, 1)
+    k_pf_gemm_sab(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_x2,
+                  const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_ws,
+                  const __grid_constant__ CUtensorMap map_w2,
+                  const __grid_constant__ CUtensorMap map_ws2, GemmLaunch a) {
+    extern __shared__ uint8_t sab_dyn[];
+    // full: activations of a stage landed; adeq: its A stage written; empty:
+    // its MMAs done (activations and A stage both free again)
+    __shared__ __align__(8) uint64_t full[kSabStages], adeq[kSabStages], empty[kSabStages];
+    __shared__ __align__(8) uint64_t wfull[kSabWStages], wempty[kSabWStages];
+    __shared__ __align__(8) uint64_t sc_full[2], sc_empty[2], acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_ntiles;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sab_dyn) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t scb = sab_scale_bytes(a.K_max);
+    uint8_t* w_base = base + size_t(kSabStages) * kSabStageBytes;   // weight stages
+    uint8_t* sc_base = w_base + size_t(kSabWStages) * kSabWBytes;   // two scale buffers
+
+    pdl_launch();
+    if (tid == 0) {
+        for (int i = 0; i < kSabStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&adeq[i], 128);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < kSabWStages; ++i) {
+            mbar_init(&wfull[i], 1);
+            mbar_init(&wempty[i], 128 * kSabDeqSets);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sc_full[i], 1);
+            mbar_init(&sc_empty[i], 128 * kSabDeqSets);
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 128);
+        }
+        mbar_fence_init();
+        tma_prefetch_map(&map_x);
+        tma_prefetch_map(&map_w);
+    }
+    if (wid == 1) {
+        tmem_alloc(&tmem_base, kSabTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait();
+    if (tid == 0) s_ntiles = __ldcg(a.n_mblocks) * a.nb_max;
+    __syncthreads();
+    const int n_tiles = s_ntiles;
+    const uint32_t tmem = tmem_base;
+
+    // tile -> (token block, 128-row weight tile); false when the weight tile
+    // does not exist for the block's group
+    auto tile_info = [&](int tile, int& g, int& row, int& nrows, int& mt, int& W, int& K) {
+        const int mb = tile / a.nb_max;
+        mt = tile % a.nb_max;
+        const MBlock m = a.mblocks[mb];
+        g = m.group;
+        row = m.row;
+        nrows = m.nrows;
+        const bool sh = g == a.E;
+        W = sh ? a.N2 : a.N;
+        K = sh ? a.K2 : a.K;
+        return mt * kBM < W && nrows > 0;
+    };
+
+    if (wid == 0) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t kst = 0, ti = 0;               // pipeline stages and tiles so far
+            uint32_t ws = 0, wph = 0;               // weight ring slot and phase
+            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+                int g, row, nrows, mt, W, K;
+                if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
+                const bool sh = g == a.E;
+                const CUtensorMap* mx = (sh && MODE == kGemmDown) ? &map_x2 : &map_x;
+                const CUtensorMap* mw = sh ? &map_w2 : &map_w;
+                const CUtensorMap* mws = sh ? &map_ws2 : &map_ws;
+                const int xrow = (sh && MODE == kGemmGateUp) ? a.a_shared_row0 + row : row;
+                const int wrow = (sh ? 0 : g * W) + mt * kBM;
+                const uint32_t buf = ti & 1u, sround = ti >> 1;
+                if (sround > 0 && !mbar_wait(&sc_empty[buf], (sround - 1) & 1))
+                    latch_timeout(a.err, 31, buf, sround, tile);
+                mbar_expect_tx(&sc_full[buf], uint32_t(kBM) * uint32_t(K / 32) * 2u);
+                tma_load_2d(sc_base + buf * scb, mws, 0, wrow, &sc_full[buf]);
+                const int nbox = (nrows + kSabBoxRows - 1) / kSabBoxRows;
+                const uint32_t xbytes = uint32_t(nbox) * (kSabBoxRows * 128u) * 2u;
+                const int nks = K / kSabKS;
+                for (int ks = 0; ks < nks; ++ks, ++kst) {
+                    if ((ks & 1) == 0) {
+                        // one weight stage: the next two pipeline stages
+                        if (kst >= 2u * kSabWStages && !mbar_wait(&wempty[ws], wph ^ 1u))
+                            latch_timeout(a.err, 30, ws, kst, tile);
+                        mbar_expect_tx(&wfull[ws], kSabWBytes);
+                        tma_load_2d(w_base + ws * kSabWBytes, mw, ks * (kSabKS / 2), wrow,
+                                    &wfull[ws]);
+                        if (++ws == uint32_t(kSabWStages)) {
+                            ws = 0;
+                            wph ^= 1u;
+                        }
+                    }
+                    const uint32_t s = kst & (kSabStages - 1), round = kst / kSabStages;
+                    if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1))
+                        latch_timeout(a.err, 32, s, round, tile);
+                    uint8_t* st = base + s * kSabStageBytes;
+                    mbar_expect_tx(&full[s], xbytes);
+                    for (int b = 0; b < nbox; ++b) {
+                        tma_load_2d(st + b * (kSabBoxRows * 128), mx, ks * kSabKS,
+                                    xrow + b * kSabBoxRows, &full[s]);
+                        tma_load_2d(st + kSabSubBytes + b * (kSabBoxRows * 128), mx,
+                                    ks * kSabKS + kBK, xrow + b * kSabBoxRows, &full[s]);
+                    }
+                }
+                ++ti;
+            }
+        }
+    } else if (wid == 1) {
+        // ----------------------------------------------------------- MMA
+        if (lane == 0) {
+            uint32_t kst = 0, ti = 0;
+            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+                int g, row, nrows, mt, W, K;
+                if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
+                const uint32_t dbuf = ti & 1u, dround = ti >> 1;
+                if (dround > 0 && !mbar_wait(&acc_empty[dbuf], (dround - 1) & 1))
+                    latch_timeout(a.err, 33, dbuf, dround, tile);
+                tc_fence_after();
+                const int npad = (nrows + 15) & ~15;
+                const uint32_t idesc = idesc_f16(kBM, npad, 0);
+                const uint32_t d_tmem = tmem + dbuf * kSabDCols;
+                const int nks = K / kSabKS;
+                for (int ks = 0; ks < nks; ++ks, ++kst) {
+                    const uint32_t s = kst & (kSabStages - 1), round = kst / kSabStages;
+                    if (!mbar_wait(&full[s], round & 1)) latch_timeout(a.err, 34, s, round, tile);
+                    if (!mbar_wait(&adeq[s], round & 1)) latch_timeout(a.err, 35, s, round, tile);
+                    tc_fence_after();
+                    const uint32_t bst = smem_u32(base + s * kSabStageBytes);
+                    const uint32_t a_tmem = tmem + uint32_t(kSabACol0) + s * kSabACols;
+#pragma unroll
+                    for (int j = 0; j < kSabKS / 16; ++j)
+                        umma_f16_tmem_a(d_tmem, a_tmem + uint32_t(8 * j),
+                                        sdesc_k_sw128(bst + (j >> 2) * kSabSubBytes +
+                                                      32u * (j & 3)),
+                                        idesc, (ks | j) != 0 ? 1u : 0u);
+                    umma_commit(&empty[s]);
+                }
+                umma_commit(&acc_full[dbuf]);
+                ++ti;
+            }
+        }
+    } else if (wid < 2 + 4 * kSabDeqSets) {
+        // ------------------------------------------------ dequantisation
+        const int q = wid & 3;                 // TMEM lane quarter
+        const int m = q * 32 + lane;           // weight row of the tile
+        const uint32_t set = uint32_t(wid - 2) >> 2;    // this set's stages: kst % 2 == set
+        uint32_t kst = 0, ti = 0;
+        uint32_t ws = 0, wph = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            int g, row, nrows, mt, W, K;
+            if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
+            const uint32_t buf = ti & 1u, sround = ti >> 1;
+            if (!mbar_wait(&sc_full[buf], sround & 1)) latch_timeout(a.err, 36, buf, sround, tile);
+            const uint32_t scrow = smem_u32(sc_base + buf * scb) + uint32_t(m * (K / 32) * 2);
+            const int nks = K / kSabKS;
+            for (int ks = 0; ks < nks; ++ks, ++kst) {
+                const uint32_t cws = ws, cwph = wph;
+                if (ks & 1) {
+                    if (++ws == uint32_t(kSabWStages)) {
+                        ws = 0;
+                        wph ^= 1u;
+                    }
+                }
+                if ((kst & 1u) != set) continue;
+                const uint32_t s = kst & (kSabStages - 1), round = kst / kSabStages;
+                if (!mbar_wait(&wfull[cws], cwph)) latch_timeout(a.err, 37, cws, kst, tile);
+                const uint32_t wrow_s = smem_u32(w_base + cws * kSabWBytes) + uint32_t(m * 128);
+                const uint2 sc4 = make_uint2(
+                    uint32_t(lds_u16(scrow + 8u * ks)) | (uint32_t(lds_u16(scrow + 8u * ks + 2u)) << 16),
+                    uint32_t(lds_u16(scrow + 8u * ks + 4u)) |
+                        (uint32_t(lds_u16(scrow + 8u * ks + 6u)) << 16));
+                if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1))
+                    latch_timeout(a.err, 38, s, round, tile);
+                tc_fence_after();
+#pragma unroll
+                for (int sb = 0; sb < 2; ++sb) {
+                    // 32 bytes of row m: 16-byte chunks c, c + 1 of the swizzled row
+                    const int c = (ks & 1) * 4 + sb * 2;
+                    const uint4 w0 = lds128(wrow_s + uint32_t(((c ^ (m & 7)) & 7) * 16));
+                    const uint4 w1 = lds128(wrow_s + uint32_t((((c + 1) ^ (m & 7)) & 7) * 16));
+                    uint32_t r[32];
+                    dequant_row_regs(w0, w1, sb ? sc4.y : sc4.x, r);
+                    tmem_st32(tmem + (uint32_t(q * 32) << 16) + uint32_t(kSabACol0) +
+                                  s * kSabACols + uint32_t(32 * sb),
+                              r);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&adeq[s]);
+                // each set has one of the weight stage's two pipeline stages
+                mbar_arrive(&wempty[cws]);
+            }
+            mbar_arrive(&sc_empty[buf]);
+            ++ti;
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q = wid & 3;
+        const int m = q * 32 + lane;           // weight row of the tile
+        uint32_t ti = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            int g, row, nrows, mt, W, K;
+            if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
+            const bool sh = g == a.E;
+            const uint32_t dbuf = ti & 1u, dround = ti >> 1;
+            if (!mbar_wait(&acc_full[dbuf], dround & 1))
+                latch_timeout(a.err, 39, dbuf, dround, tile);
+            tc_fence_after();
+            const uint32_t tl = tmem + (uint32_t(q * 32) << 16) + dbuf * kSabDCols;
+            for (int c0 = 0; c0 < nrows; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tl + uint32_t(c0), v);
+                tmem_ld_wait();
+                const int nv = min(32, nrows - c0);
+                if (MODE == kGemmGateUp) {
+                    // rows 2i (gate) and 2i + 1 (up) are lanes l and l + 1.  h is
+                    // rounded to fp16 for the down product, so the fast exp and
+                    // divide (relative error ~1e-6) cost nothing in accuracy.
+                    const int i = (mt * kBM + m) >> 1;       // SwiGLU index (even lanes)
+                    const int ld = sh ? a.ld2 : a.ldo;
+                    __half* hb = (sh ? a.out2_f16 : a.out_f16) + size_t(row + c0) * ld + mma_pos(i);
+                    float* hf = (!sh && a.out_f32 != nullptr)
+                                    ? a.out_f32 + size_t(row + c0) * ld + i : nullptr;
+                    const bool even = (lane & 1) == 0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float gt = __uint_as_float(v[j]);
+                        const float up = __shfl_down_sync(0xffffffffu, gt, 1);
+                        if (even && j < nv) {
+                            const float h = __fdividef(gt, 1.0f + __expf(-gt)) * up;
+                            hb[size_t(j) * ld] = __float2half_rn(h);
+                            if (hf != nullptr) hf[size_t(j) * ld] = h;
+                        }
+                    }
+                } else {
+                    const int o = mt * kBM + m;              // output feature
+                    const size_t ld = size_t(a.ldo);
+                    const size_t r0 = size_t(row + c0) * ld + o;
+                    if (!sh && a.out_bf16 != nullptr) {
+                        uint16_t* yb = a.out_bf16 + r0;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nv) yb[j * ld] = f32_to_bf16(__uint_as_float(v[j]));
+                    } else {
+                        __half* yh = (sh ? a.out2_f16 : a.out_f16) + r0;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nv) yh[j * ld] = __float2half_rn(__uint_as_float(v[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[dbuf]);
+            ++ti;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (wid == 1) tmem_dealloc(tmem, kSabTmemCols);
+}
+
+// ------------------------------------------------------------------ host
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 sab_encode_fn() {
+    static std::mutex mu;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (fn == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D map over a row-major [rows][inner] array (inner in elements).
+bool sab_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+             uint64_t rows, uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+    auto fn = sab_encode_fn();
+    if (fn == nullptr || base == nullptr) return false;
+    const cuuint64_t gdim[2] = {inner, rows};
+    const cuuint64_t gstride[1] = {inner * uint64_t(esize)};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r =
+        fn(m, dt, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE,
+           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t run_sab(GemmLaunch g, const CUtensorMap& mx, const CUtensorMap& mx2,
+                    const CUtensorMap& mw, const CUtensorMap& mws, const CUtensorMap& mw2,
+                    const CUtensorMap& mws2, cudaStream_t s) {
+    const Dev d = device_info();
+    const size_t dyn = size_t(kSabStages) * kSabStageBytes + size_t(kSabWStages) * kSabWBytes +
+                       2 * size_t(sab_scale_bytes(g.K_max)) + 1024;
+    if (dyn > kPfSmemBudget || g.K % 256 != 0 || g.K2 % 256 != 0) return cudaErrorInvalidValue;
+    g.stages = kSabStages;
+    cudaError_t e = cudaFuncSetAttribute(k_pf_gemm_sab<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(d.sms);
+    cfg.blockDim = dim3(kSabThreads);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_pf_gemm_sab<MODE>, mx, mx2, mw, mws, mw2, mws2, g);
+    if (e == cudaSuccess) prof_after_launch(s);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_gate_up(const PfExperts& p, cudaStream_t s) {
+    const int H = p.H, I = p.I, Is = p.Is, E = p.E;
+    // activations xg [xg_rows][H] in 32-row boxes; weights: packed rows and
+    // their scales in 128-row boxes.  A weight set the block list cannot name
+    // gets the other set's maps.
+    CUtensorMap mx, mq, ms, mq2, ms2;
+    if (!sab_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.xg, H, p.xg_rows, kBK, kSabBoxRows,
+                 true))
+        return cudaErrorInvalidValue;
+    if (p.routed &&
+        (!sab_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.gu_q, H / 2, uint64_t(E) * 2 * I,
+                  kSabKS, kBM, true) ||
+         !sab_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.gu_s, H / 32, uint64_t(E) * 2 * I,
+                  H / 32, kBM, false)))
+        return cudaErrorInvalidValue;
+    if (p.shared &&
+        (!sab_map(&mq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_gu_q, H / 2, 2 * Is,
+                  kSabKS, kBM, true) ||
+         !sab_map(&ms2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.sh_gu_s, H / 32, 2 * Is, H / 32,
+                  kBM, false)))
+        return cudaErrorInvalidValue;
+    if (!p.routed) {
+        mq = mq2;
+        ms = ms2;
+    }
+    if (!p.shared) {
+        mq2 = mq;
+        ms2 = ms;
+    }
+    GemmLaunch g{};
+    g.N = 2 * I;
+    g.N2 = 2 * Is;
+    g.K = H;
+    g.K2 = H;
+    g.K_max = H;
+    g.E = E;
+    g.mblocks = p.mblocks;
+    g.n_mblocks = p.n_mblocks;
+    g.nb_max = (2 * (I > Is ? I : Is)) / kBM;
+    g.a_shared_row0 = p.xg_shared_row0;
+    g.out_f16 = p.h;
+    g.out_f32 = p.h_f32;
+    g.ldo = I;
+    g.out2_f16 = p.hs;
+    g.ld2 = Is;
+    g.err = p.err;
+    return run_sab<kGemmGateUp>(g, mx, mx, mq, ms, mq2, ms2, s);
+}
+
+cudaError_t launch_prefill_down(const PfExperts& p, cudaStream_t s) {
+    const int T = p.T, K = p.K, H = p.H, I = p.I, Is = p.Is, E = p.E;
+    // activations h [T*K][I] (routed) or hs [T][Is] (shared)
+    CUtensorMap mx, mx2, mq, ms, mq2, ms2;
+    if (p.routed &&
+        (!sab_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.h, I, uint64_t(T) * K, kBK,
+                  kSabBoxRows, true) ||
+         !sab_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.dn_q, I / 2, uint64_t(E) * H,
+                  kSabKS, kBM, true) ||
+         !sab_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.dn_s, I / 32, uint64_t(E) * H, I / 32,
+                  kBM, false)))
+        return cudaErrorInvalidValue;
+    if (p.shared &&
+        (!sab_map(&mx2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.hs, Is, T, kBK, kSabBoxRows, true) ||
+         !sab_map(&mq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_dn_q, Is / 2, H,
+                  kSabKS, kBM, true) ||
+         !sab_map(&ms2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.sh_dn_s, Is / 32, H, Is / 32, kBM,
+                  false)))
+        return cudaErrorInvalidValue;
+    if (!p.routed) {
+        mx = mx2;
+        mq = mq2;
+        ms = ms2;
+    }
+    if (!p.shared) {
+        mx2 = mx;
+        mq2 = mq;
+        ms2 = ms;
+    }
+    GemmLaunch d{};
+    d.N = H;
+    d.N2 = H;
+    d.K = I;
+    d.K2 = Is;
+    d.K_max = I > Is ? I : Is;
+    d.E = E;
+    d.mblocks = p.mblocks;
+    d.n_mblocks = p.n_mblocks;
+    d.nb_max = H / kBM;
+    d.a_shared_row0 = 0;
+    d.out_f16 = p.y;
+    d.out_bf16 = p.y_bf16;
+    d.out2_f16 = p.ysh;
+    d.ldo = H;
+    d.err = p.err;
+    return run_sab<kGemmDown>(d, mx, mx2, mq, ms, mq2, ms2, s);
+}
+
+}  // namespace strata
