@@ -12,11 +12,15 @@
 // TMA into 128-byte-swizzled shared memory, 32 rows a box, as many boxes as
 // the block has rows.
 //
-// Warps: 0 TMA producer; 1 TMEM allocation and (lane 0) the MMAs; 2..9
-// dequantisation, two sets of four taking alternate K blocks (warp w owns
-// TMEM lanes 32 (w % 4) .. +32: weight rows); 10..13 epilogue (the same lane
-// quarters): SwiGLU of gate/up row pairs (rows 2i, 2i+1 sit in neighbouring
-// lanes) or the down product's outputs.
+// Warps: 0 TMA producer; 1 and 2 the MMAs (lane 0; warp 1 also allocates
+// the TMEM); 3..10 dequantisation, two sets of four taking alternate K
+// blocks (warp w owns TMEM lanes 32 (w % 4) .. +32: weight rows); 11..14
+// epilogue (the same lane quarters): SwiGLU of gate/up row pairs (rows 2i,
+// 2i+1 sit in neighbouring lanes) or the down product's outputs.
+// One thread issues a tcgen05.mma about every 54 cycles however small N is,
+// while the tensor pipe needs only N / 2 cycles for a 128 x N x 16 product:
+// a tile of at most 64 tokens therefore splits its K steps between the two
+// MMA warps, each into an accumulator of its own, which the epilogue adds.
 // Accumulators are double-buffered (2 x 128 columns) so a tile's epilogue
 // overlaps the next tile's MMAs; the dequantised A stages take 4 x 64
 // columns.  A pipeline stage is K = 128 (eight MMAs), so the per-stage
@@ -41,7 +45,9 @@
 
 namespace strata {
 
-constexpr int kSabThreads = 448;
+constexpr int kSabThreads = 480;
+constexpr int kSabMmaWarps = 2;          // MMA issuing warps (1, 2)
+constexpr int kSabDeq0 = 1 + kSabMmaWarps;   // first dequantisation warp
 constexpr int kSabDeqSets = 2;           // dequantisation warp sets: K blocks alternate
 constexpr int kSabKS = 128;              // K of one pipeline stage: 8 MMAs of K = 16
 constexpr int kSabStages = 4;            // activation stages = dequantised A stages
@@ -67,26 +73,60 @@ __host__ __device__ inline uint32_t sab_scale_bytes(int K_max) {
 // 64 fp16 weights of one row for one K block: 32 packed bytes, two scales
 // -> 32 registers holding the MMA-order pairs, register c = K positions
 // (2c, 2c+1).  Within every 8 elements the positions hold elements
-// [0,4,1,5,2,6,3,7]: one LOP3 per pair (the activations are stored in the
-// same order, so the products are the natural ones).
+// [0,4,1,5,2,6,3,7], so a pair is one nibble position of the word's two
+// 16-bit halves (the activations are stored in the same order, so the
+// products are the natural ones).  A nibble n is or-ed into the mantissa of
+// 1024.0: at bits 0-3 that reads 1024 + n and a subtraction of 1032 gives
+// n - 8; at bits 4-7 it reads 1024 + 16 n and a fused multiply-add with 1/16
+// and -72 gives n - 8; both exact.  One shift by 8 brings the upper byte's
+// nibbles down, so a word of four pairs costs one shift and four masks on the
+// integer pipe, the rest is half2 arithmetic.  The product with the scale is
+// the single rounding.
 __device__ __forceinline__ void dequant_row_regs(const uint4& w0, const uint4& w1, uint32_t sc2,
                                                  uint32_t (&r)[32]) {
     const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2c00), __ushort_as_half(0x2c00));
+    const __half2 m72 = __halves2half2(__ushort_as_half(0xd480), __ushort_as_half(0xd480));
     const __half s0 = __ushort_as_half(uint16_t(sc2 & 0xffffu));
     const __half s1 = __ushort_as_half(uint16_t(sc2 >> 16));
     const __half2 sA = __halves2half2(s0, s0), sB = __halves2half2(s1, s1);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
         const __half2 s = (c < 4) ? sA : sB;
+        const uint32_t w = words[c], wh = w >> 8;
+        const uint32_t b[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x64006400u,
+                               (wh & 0x000F000Fu) | 0x64006400u, (wh & 0x00F000F0u) | 0x64006400u};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t b = ((words[c] >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
-            const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&b), off);   // exact
+            const __half2 h = *reinterpret_cast<const __half2*>(&b[j]);
+            const __half2 q = (j & 1) ? __hfma2(h, sixteenth, m72) : __hsub2(h, off);   // exact
             const __half2 v = __hmul2(q, s);
             r[4 * c + j] = *reinterpret_cast<const uint32_t*>(&v);
         }
     }
+}
+
+// Descriptor step (16-byte units) from a stage's first K step to step j:
+// sub-block j / 4, 32 (j % 4) bytes into its 128-byte rows.
+__device__ __forceinline__ uint64_t sab_boff(int j) {
+    return uint64_t((uint32_t(j >> 2) * kSabSubBytes + 32u * uint32_t(j & 3)) >> 4);
+}
+
+// Accumulators of a tile with npad token columns: two (one per MMA warp,
+// alternate K steps) when both fit one 128-column buffer, else one.
+__host__ __device__ inline int sab_accumulators(int npad) { return npad <= 64 ? 2 : 1; }
+
+// Bounded wait that also gives up early once a timed-out wait has been
+// latched (STRATA_ETIMEOUT), so one failed wait in the grid does not leave
+// every later wait to run out its full limit.
+__device__ __forceinline__ bool sab_wait(uint64_t* bar, uint32_t parity, const uint32_t* err) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *reinterpret_cast<const volatile uint32_t*>(err) == 4u)
+            return false;
+    }
+    return false;
 }
 
 // Position of element e (within its group of 8) in the MMA order above.
@@ -107,6 +147,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
     __shared__ __align__(8) uint64_t full[kSabStages], adeq[kSabStages], empty[kSabStages];
     __shared__ __align__(8) uint64_t wfull[kSabWStages], wempty[kSabWStages];
     __shared__ __align__(8) uint64_t sc_full[2], sc_empty[2], acc_full[2], acc_empty[2];
+    __shared__ __align__(8) uint64_t mma_done;
     __shared__ uint32_t tmem_base;
     __shared__ int s_ntiles;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -121,7 +162,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         for (int i = 0; i < kSabStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&adeq[i], 128);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], kSabMmaWarps);
         }
         for (int i = 0; i < kSabWStages; ++i) {
             mbar_init(&wfull[i], 1);
@@ -130,9 +171,10 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sc_full[i], 1);
             mbar_init(&sc_empty[i], 128 * kSabDeqSets);
-            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_full[i], kSabMmaWarps);
             mbar_init(&acc_empty[i], 128);
         }
+        mbar_init(&mma_done, kSabMmaWarps);
         mbar_fence_init();
         tma_prefetch_map(&map_x);
         tma_prefetch_map(&map_w);
@@ -170,6 +212,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         if (lane == 0) {
             uint32_t kst = 0, ti = 0;               // pipeline stages and tiles so far
             uint32_t ws = 0, wph = 0;               // weight ring slot and phase
+            uint32_t wcount = 0;                     // weight stages so far
             for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
                 int g, row, nrows, mt, W, K;
                 if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
@@ -180,7 +223,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                 const int xrow = (sh && MODE == kGemmGateUp) ? a.a_shared_row0 + row : row;
                 const int wrow = (sh ? 0 : g * W) + mt * kBM;
                 const uint32_t buf = ti & 1u, sround = ti >> 1;
-                if (sround > 0 && !mbar_wait(&sc_empty[buf], (sround - 1) & 1))
+                if (sround > 0 && !sab_wait(&sc_empty[buf], (sround - 1) & 1, a.err))
                     latch_timeout(a.err, 31, buf, sround, tile);
                 mbar_expect_tx(&sc_full[buf], uint32_t(kBM) * uint32_t(K / 32) * 2u);
                 tma_load_2d(sc_base + buf * scb, mws, 0, wrow, &sc_full[buf]);
@@ -190,18 +233,19 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                 for (int ks = 0; ks < nks; ++ks, ++kst) {
                     if ((ks & 1) == 0) {
                         // one weight stage: the next two pipeline stages
-                        if (kst >= 2u * kSabWStages && !mbar_wait(&wempty[ws], wph ^ 1u))
+                        if (kst >= 2u * kSabWStages && !sab_wait(&wempty[ws], wph ^ 1u, a.err))
                             latch_timeout(a.err, 30, ws, kst, tile);
                         mbar_expect_tx(&wfull[ws], kSabWBytes);
                         tma_load_2d(w_base + ws * kSabWBytes, mw, ks * (kSabKS / 2), wrow,
                                     &wfull[ws]);
+                        ++wcount;
                         if (++ws == uint32_t(kSabWStages)) {
                             ws = 0;
                             wph ^= 1u;
                         }
                     }
                     const uint32_t s = kst & (kSabStages - 1), round = kst / kSabStages;
-                    if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1))
+                    if (round > 0 && !sab_wait(&empty[s], (round - 1) & 1, a.err))
                         latch_timeout(a.err, 32, s, round, tile);
                     uint8_t* st = base + s * kSabStageBytes;
                     mbar_expect_tx(&full[s], xbytes);
@@ -214,53 +258,87 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                 }
                 ++ti;
             }
+            // Every copy has landed before the CTA exits, also when a wait
+            // gave up: the last round of each slot (completed long ago when
+            // nothing failed).
+            for (uint32_t i = 0; i < uint32_t(kSabStages) && i < kst; ++i) {
+                const uint32_t k = kst - 1 - i;
+                mbar_wait(&full[k % kSabStages], (k / kSabStages) & 1);
+            }
+            for (uint32_t i = 0; i < uint32_t(kSabWStages) && i < wcount; ++i) {
+                const uint32_t k = wcount - 1 - i;
+                mbar_wait(&wfull[k % kSabWStages], (k / kSabWStages) & 1);
+            }
+            for (uint32_t i = 0; i < 2u && i < ti; ++i) {
+                const uint32_t t = ti - 1 - i;
+                mbar_wait(&sc_full[t & 1u], (t >> 1) & 1);
+            }
         }
-    } else if (wid == 1) {
+    } else if (wid <= kSabMmaWarps) {
         // ----------------------------------------------------------- MMA
         if (lane == 0) {
+            const int mw = wid - 1;          // with two accumulators: K steps j % 2 == mw
             uint32_t kst = 0, ti = 0;
             for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
                 int g, row, nrows, mt, W, K;
                 if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
                 const uint32_t dbuf = ti & 1u, dround = ti >> 1;
-                if (dround > 0 && !mbar_wait(&acc_empty[dbuf], (dround - 1) & 1))
+                if (dround > 0 && !sab_wait(&acc_empty[dbuf], (dround - 1) & 1, a.err))
                     latch_timeout(a.err, 33, dbuf, dround, tile);
                 tc_fence_after();
                 const int npad = (nrows + 15) & ~15;
+                const int nacc = sab_accumulators(npad);
                 const uint32_t idesc = idesc_f16(kBM, npad, 0);
-                const uint32_t d_tmem = tmem + dbuf * kSabDCols;
+                const uint32_t d_tmem = tmem + dbuf * kSabDCols + uint32_t(mw * (kSabDCols / 2));
                 const int nks = K / kSabKS;
                 for (int ks = 0; ks < nks; ++ks, ++kst) {
                     const uint32_t s = kst & (kSabStages - 1), round = kst / kSabStages;
-                    if (!mbar_wait(&full[s], round & 1)) latch_timeout(a.err, 34, s, round, tile);
-                    if (!mbar_wait(&adeq[s], round & 1)) latch_timeout(a.err, 35, s, round, tile);
+                    if (!sab_wait(&full[s], round & 1, a.err))
+                        latch_timeout(a.err, 34, s, round, tile);
+                    if (!sab_wait(&adeq[s], round & 1, a.err))
+                        latch_timeout(a.err, 35, s, round, tile);
                     tc_fence_after();
-                    const uint32_t bst = smem_u32(base + s * kSabStageBytes);
-                    const uint32_t a_tmem = tmem + uint32_t(kSabACol0) + s * kSabACols;
+                    // the stage's first K step; step j is sub-block j / 4 of B,
+                    // 32 (j % 4) bytes into its rows, and A columns 8 j on
+                    const uint64_t b0 = sdesc_k_sw128(smem_u32(base + s * kSabStageBytes));
+                    const uint32_t a0 = tmem + uint32_t(kSabACol0) + s * kSabACols;
+                    if (nacc == 1) {
+                        if (mw == 0) {
 #pragma unroll
-                    for (int j = 0; j < kSabKS / 16; ++j)
-                        umma_f16_tmem_a(d_tmem, a_tmem + uint32_t(8 * j),
-                                        sdesc_k_sw128(bst + (j >> 2) * kSabSubBytes +
-                                                      32u * (j & 3)),
-                                        idesc, (ks | j) != 0 ? 1u : 0u);
+                            for (int j = 0; j < kSabKS / 16; ++j)
+                                umma_f16_tmem_a(d_tmem, a0 + uint32_t(8 * j), b0 + sab_boff(j),
+                                                idesc, (ks | j) != 0 ? 1u : 0u);
+                        }
+                    } else {
+                        const uint64_t bm = b0 + uint64_t(2 * mw);     // + 32 bytes on odd steps
+                        const uint32_t am = a0 + uint32_t(8 * mw);
+#pragma unroll
+                        for (int jj = 0; jj < kSabKS / 32; ++jj)
+                            umma_f16_tmem_a(d_tmem, am + uint32_t(16 * jj), bm + sab_boff(2 * jj),
+                                            idesc, (ks | jj) != 0 ? 1u : 0u);
+                    }
                     umma_commit(&empty[s]);
                 }
                 umma_commit(&acc_full[dbuf]);
                 ++ti;
             }
+            // no product may still be writing the TMEM when it is freed
+            umma_commit(&mma_done);
+            mbar_wait(&mma_done, 0);
         }
-    } else if (wid < 2 + 4 * kSabDeqSets) {
+    } else if (wid < kSabDeq0 + 4 * kSabDeqSets) {
         // ------------------------------------------------ dequantisation
         const int q = wid & 3;                 // TMEM lane quarter
         const int m = q * 32 + lane;           // weight row of the tile
-        const uint32_t set = uint32_t(wid - 2) >> 2;    // this set's stages: kst % 2 == set
+        const uint32_t set = uint32_t(wid - kSabDeq0) >> 2;   // this set's stages: kst % 2 == set
         uint32_t kst = 0, ti = 0;
         uint32_t ws = 0, wph = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
             int g, row, nrows, mt, W, K;
             if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
             const uint32_t buf = ti & 1u, sround = ti >> 1;
-            if (!mbar_wait(&sc_full[buf], sround & 1)) latch_timeout(a.err, 36, buf, sround, tile);
+            if (!sab_wait(&sc_full[buf], sround & 1, a.err))
+                latch_timeout(a.err, 36, buf, sround, tile);
             const uint32_t scrow = smem_u32(sc_base + buf * scb) + uint32_t(m * (K / 32) * 2);
             const int nks = K / kSabKS;
             for (int ks = 0; ks < nks; ++ks, ++kst) {
@@ -273,13 +351,13 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                 }
                 if ((kst & 1u) != set) continue;
                 const uint32_t s = kst & (kSabStages - 1), round = kst / kSabStages;
-                if (!mbar_wait(&wfull[cws], cwph)) latch_timeout(a.err, 37, cws, kst, tile);
+                if (!sab_wait(&wfull[cws], cwph, a.err)) latch_timeout(a.err, 37, cws, kst, tile);
                 const uint32_t wrow_s = smem_u32(w_base + cws * kSabWBytes) + uint32_t(m * 128);
                 const uint2 sc4 = make_uint2(
                     uint32_t(lds_u16(scrow + 8u * ks)) | (uint32_t(lds_u16(scrow + 8u * ks + 2u)) << 16),
                     uint32_t(lds_u16(scrow + 8u * ks + 4u)) |
                         (uint32_t(lds_u16(scrow + 8u * ks + 6u)) << 16));
-                if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1))
+                if (round > 0 && !sab_wait(&empty[s], (round - 1) & 1, a.err))
                     latch_timeout(a.err, 38, s, round, tile);
                 tc_fence_after();
 #pragma unroll
@@ -313,30 +391,46 @@ __global__ void __launch_bounds__(kSabThreads, 1)
             if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
             const bool sh = g == a.E;
             const uint32_t dbuf = ti & 1u, dround = ti >> 1;
-            if (!mbar_wait(&acc_full[dbuf], dround & 1))
+            if (!sab_wait(&acc_full[dbuf], dround & 1, a.err))
                 latch_timeout(a.err, 39, dbuf, dround, tile);
             tc_fence_after();
             const uint32_t tl = tmem + (uint32_t(q * 32) << 16) + dbuf * kSabDCols;
+            const bool two = sab_accumulators((nrows + 15) & ~15) == 2;
             for (int c0 = 0; c0 < nrows; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tl + uint32_t(c0), v);
-                tmem_ld_wait();
+                if (two) {
+                    // the odd K steps' accumulator, 64 columns on
+                    uint32_t v1[32];
+                    tmem_ld32(tl + uint32_t(kSabDCols / 2 + c0), v1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+                } else {
+                    tmem_ld_wait();
+                }
                 const int nv = min(32, nrows - c0);
                 if (MODE == kGemmGateUp) {
-                    // rows 2i (gate) and 2i + 1 (up) are lanes l and l + 1.  h is
-                    // rounded to fp16 for the down product, so the fast exp and
-                    // divide (relative error ~1e-6) cost nothing in accuracy.
-                    const int i = (mt * kBM + m) >> 1;       // SwiGLU index (even lanes)
+                    // rows 2i (gate) and 2i + 1 (up) are lanes l and l + 1, each
+                    // with every token.  One exchange per token pair gives the
+                    // even lane token j's (gate, up) and the odd lane token
+                    // j + 1's, so every lane computes a SwiGLU.  h is rounded to
+                    // fp16 for the down product, so the fast exp and divide
+                    // (relative error ~1e-6) cost nothing in accuracy.
+                    const int odd = lane & 1;
+                    const int i = (mt * kBM + m) >> 1;       // SwiGLU index of the pair
                     const int ld = sh ? a.ld2 : a.ldo;
-                    __half* hb = (sh ? a.out2_f16 : a.out_f16) + size_t(row + c0) * ld + mma_pos(i);
-                    float* hf = (!sh && a.out_f32 != nullptr)
-                                    ? a.out_f32 + size_t(row + c0) * ld + i : nullptr;
-                    const bool even = (lane & 1) == 0;
+                    const size_t r0 = size_t(row + c0 + odd) * ld;
+                    __half* hb = (sh ? a.out2_f16 : a.out_f16) + r0 + mma_pos(i);
+                    float* hf = (!sh && a.out_f32 != nullptr) ? a.out_f32 + r0 + i : nullptr;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float gt = __uint_as_float(v[j]);
-                        const float up = __shfl_down_sync(0xffffffffu, gt, 1);
-                        if (even && j < nv) {
+                    for (int j = 0; j < 32; j += 2) {
+                        const float keep = __uint_as_float(odd ? v[j + 1] : v[j]);
+                        const float send = __uint_as_float(odd ? v[j] : v[j + 1]);
+                        const float other = __shfl_xor_sync(0xffffffffu, send, 1);
+                        const float gt = odd ? other : keep, up = odd ? keep : other;
+                        if (j + odd < nv) {
                             const float h = __fdividef(gt, 1.0f + __expf(-gt)) * up;
                             hb[size_t(j) * ld] = __float2half_rn(h);
                             if (hf != nullptr) hf[size_t(j) * ld] = h;
