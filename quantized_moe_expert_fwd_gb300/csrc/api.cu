@@ -43,6 +43,7 @@ WsLayout ws_layout(const strata_moe_dims& d, int T) {
         L.base_blk = take(nblk * E * 4);
         L.mblocks = take(max_mb * sizeof(MBlock));
         L.n_mblocks = take(16);
+        L.lgp = take(size_t(kRouterSplitMax) * t * (E + 1) * 4);
         L.xg = take((t * K + t) * H * 2);
         L.h16 = take(t * K * I * 2);
         L.hs16 = take(t * Is * 2);
@@ -254,7 +255,7 @@ strata_status prefill_layer(const strata_moe_dims* d, const strata_moe_layer* L,
     PfRoute r{};
     r.x = static_cast<const uint16_t*>(x);
     r.router = static_cast<const uint16_t*>(L->router_dev);
-    r.logits = at<float>(ws, W.logits);
+    r.part = at<float>(ws, W.lgp);
     r.forced_ids = forced_ids;
     r.forced_w = forced_w;
     r.ids = at<int32_t>(ws, W.ids);
@@ -441,7 +442,7 @@ strata_status moe_route(const strata_moe_dims* dims, const strata_moe_layer* lay
         r.x = static_cast<const uint16_t*>(x_dev);
         r.router = static_cast<const uint16_t*>(layer->router_dev);
         r.bias = layer->router_bias_dev;
-        r.logits = at<float>(ws_dev, W.logits);
+        r.part = at<float>(ws_dev, W.lgp);
         r.logits_user = logits_dev;
         r.ids = at<int32_t>(ws_dev, W.ids);
         r.w = at<float>(ws_dev, W.w);

@@ -26,9 +26,9 @@ constexpr int kPlanHeader = 4;
 // prefill (T > kDecodeMaxTokens) tiles: 128 rows x 64 K per stage
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kPfMaxStages = 6;
 constexpr size_t kPfSmemBudget = 225280;
-enum GemmMode { kGemmRouter = 0, kGemmGateUp = 1, kGemmDown = 2 };
+constexpr int kRouterSplitMax = 8;       // K slices of the prefill router GEMM
+enum GemmMode { kGemmGateUp = 1, kGemmDown = 2 };
 
 // One block of up to 128 rows of one group (a routed expert, or the shared
 // expert as group E) for the prefill GEMMs.  row: first row of the group's
@@ -44,7 +44,7 @@ struct MBlock {
 // for larger T.
 struct WsLayout {
     size_t ctl, logits, ids, w, sig, counts, offsets, perm, inv, plan, h, hs, x, out;
-    size_t cnt_blk, base_blk, mblocks, n_mblocks, xg, h16, hs16, y, ysh;
+    size_t cnt_blk, base_blk, mblocks, n_mblocks, lgp, xg, h16, hs16, y, ysh;
     size_t total;
 };
 
@@ -123,7 +123,8 @@ cudaError_t launch_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x,
 
 // ---------------------------------------------------------------- prefill
 struct PfSelectLaunch {
-    const float* logits; float* logits_user;
+    const float* part; int nsplit;    // router GEMM K slices [nsplit][T][E + 1]
+    const float* bias; float* logits_user;
     const int32_t* forced_ids; const float* forced_w;
     int32_t* ids; float* w; float* sig;
     int32_t* ids_user; float* w_user; float* sig_user;
@@ -138,10 +139,9 @@ struct PfScanLaunch {
 };
 struct GemmLaunch {
     const MBlock* mblocks; const int32_t* n_mblocks;
-    int router_mblocks, M;             // router: rows of A
-    int N, N2, N_valid, K, K2, K_max;   // N, K of routed groups; N2, K2 of the shared group
-    int BN, nb_max, E, a_shared_row0, stages;
-    float* out_f32; const float* bias;   // router: logits (+ bias on the first E columns)
+    int N, N2, K, K2, K_max;      // N, K of routed groups; N2, K2 of the shared group
+    int nb_max, E, a_shared_row0;
+    float* out_f32;               // gate/up: routed h also in fp32 (or NULL)
     __half* out_f16; __half* out2_f16;
     uint16_t* out_bf16; uint16_t* out2_bf16;
     int ldo, ld2;
@@ -149,7 +149,7 @@ struct GemmLaunch {
 };
 struct PfRoute {
     const uint16_t* x; const uint16_t* router; const float* bias;
-    float* logits; float* logits_user;
+    float* part; float* logits_user;    // part: kRouterSplitMax * T * (E + 1) floats
     const int32_t* forced_ids; const float* forced_w;
     int32_t* ids; float* w; float* sig;
     int32_t* ids_user; float* w_user; float* sig_user;

@@ -1,15 +1,17 @@
 // prefill.cu -- the large-T (prefill) path of the routed MoE FFN on the
-// 5th-generation tensor cores.
+// 5th-generation tensor cores: routing, bucketing, gathering and the
+// combine (the expert GEMMs are in prefill_gemm.cu).
 //
 // The pages found the prompt path bound by "dequantize each expert to FP16
 // and call oneMKL" (Strata, "Strata on an Intel Arc", section "The engine
 // itself on Intel: the SYCL port") and by per-layer host grouping; a fused
 // dequant + matrix-unit kernel lost there because it did not overlap the
-// two.  Here every step runs on the GPU and the dequantisation feeds the
-// tensor cores through shared memory while they run:
+// two.  Here every step runs on the GPU:
 //
-//   router GEMM     logits = x * router^T (bf16 x bf16 -> fp32, tcgen05)
-//   k_pf_select     top-K, softmax weights, sigmoid gate: one warp a token
+//   k_pf_router     K slices of logits = x * router^T (bf16 x bf16 -> fp32,
+//                   tcgen05), one CTA a (expert tile, token tile, slice)
+//   k_pf_select     slices added in order + bias; top-K, softmax weights,
+//                   sigmoid gate: one warp a token
 //   k_pf_count / k_pf_scan / k_pf_scatter
 //                   stable counting sort of the (token, k) pairs by expert
 //                   and the list of 128-row blocks of every expert ("a
@@ -18,18 +20,14 @@
 //                   section "What was tuned"); the shared expert is one more
 //                   group whose rows are all tokens
 //   k_pf_gather     activations of every slot, fp16, in the operand order
-//   gate/up GEMM    persistent tcgen05 kernel: A (activations) by TMA, B =
-//                   int4 rows by TMA, dequantised by four warps into the
-//                   128-byte-swizzled fp16 tile, fp32 accumulator in TMEM,
-//                   SwiGLU in the epilogue -> h (fp16)
-//   down GEMM       the same with A = h -> y (bf16)
+//   gate/up, down   grouped GEMMs with the dequantised int4 weights in TMEM
+//                   (prefill_gemm.cu) -> h (fp16), y (fp16 or bf16)
 //   k_pf_combine    out = sum_k w y + sigma(gate) S, in a fixed order
 //
-// Operand order inside each group of 8 along K: [0,4,1,5,2,6,3,7].  One
-// LOP3 on a packed int4 word, (w >> 4j) & 0x000F000F | 0x64006400, yields
-// the fp16 pair (1024 + u_j, 1024 + u_{j+4}); writing the activations (A)
-// in the same order makes the products the natural ones, since the MMA sums
-// over K in any consistent order.
+// Operand order inside each group of 8 along K: [0,4,1,5,2,6,3,7], the
+// order in which the weight dequantisation yields its fp16 pairs; writing
+// the activations in the same order makes the products the natural ones,
+// since the MMA sums over K in any consistent order.
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -40,14 +38,16 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "route.cuh"
 #include "tc.cuh"
 
 namespace strata {
 
 // ------------------------------------------------------------- selection
-// One warp a token: top-K (ties to the lower id), ids ascending,
-// renormalised softmax weights, sigmoid of the shared-gate logit; or the
-// forced ids/weights.  The same arithmetic as the decode path.
+// One warp a token: the logits are the router GEMM's K slices added in slice
+// order plus the bias; then top-K (ties to the lower id), ids ascending,
+// renormalised softmax weights and the sigmoid of the shared-gate logit, by
+// the decode path's selection; or the forced ids/weights.
 __global__ void __launch_bounds__(256) k_pf_select(PfSelectLaunch a) {
     extern __shared__ float s_dyn[];
     pdl_launch();
@@ -55,11 +55,43 @@ __global__ void __launch_bounds__(256) k_pf_select(PfSelectLaunch a) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int t = blockIdx.x * (blockDim.x >> 5) + wid;
     if (t >= a.T) return;
-    const int E = a.E, K = a.K;
-    const float* lg = a.logits + size_t(t) * (E + 1);
+    const int E = a.E, K = a.K, S = a.nsplit;
+    const size_t ld = size_t(E) + 1, sstride = size_t(a.T) * ld;
+    const float* p = a.part + size_t(t) * ld;
     float* L = s_dyn + size_t(wid) * (E + 16);
+    uint32_t* Lk = reinterpret_cast<uint32_t*>(L);
     __shared__ int s_ids[8][kMaxTopK];
     __shared__ float s_w[8][kMaxTopK];
+    __shared__ float s_gate[8];
+    // logits e = lane, lane + 32, ... and the gate (e = E): four of them,
+    // times the slices, loads in flight at once
+#pragma unroll 1
+    for (int e0 = lane; e0 <= E; e0 += 4 * 32) {
+        float u[kRouterSplitMax][4];
+#pragma unroll
+        for (int sl = 0; sl < kRouterSplitMax; ++sl)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                u[sl][j] = (sl < S && e0 + 32 * j <= E) ? __ldcg(p + sl * sstride + e0 + 32 * j)
+                                                        : 0.0f;
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int sl = 0; sl < kRouterSplitMax; ++sl)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] += u[sl][j];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + 32 * j;
+            if (e < E) {
+                const float l = a.bias != nullptr ? v[j] + __ldg(a.bias + e) : v[j];
+                Lk[e] = logit_key(l);
+                if (a.logits_user) a.logits_user[size_t(t) * E + e] = l;
+            } else if (e == E) {
+                s_gate[wid] = v[j];
+            }
+        }
+    }
+    __syncwarp();
     if (a.forced_ids) {
         for (int k = lane; k < K; k += 32) {
             const int id = __ldg(a.forced_ids + size_t(t) * K + k);
@@ -69,67 +101,8 @@ __global__ void __launch_bounds__(256) k_pf_select(PfSelectLaunch a) {
         }
         __syncwarp();
     } else {
-        // top-K of the E logits, as in the decode path
-        for (int e = lane; e < E; e += 32) L[e] = __ldcg(lg + e);
-        __syncwarp();
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
-        for (int e = lane; e < E; e += 32) {
-            const float v = L[e];
-            if (v > bv || (v == bv && e < be)) {
-                bv = v;
-                be = e;
-            }
-        }
-        float myv = 0.0f;
-        int mye = 0x7fffffff;
-        for (int k = 0; k < K; ++k) {
-            float wv = bv;
-            int we = be;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, we, o);
-                if (ov > wv || (ov == wv && oe < we)) {
-                    wv = ov;
-                    we = oe;
-                }
-            }
-            if (lane == k) {
-                myv = wv;
-                mye = we;
-            }
-            if (we < E && (we & 31) == lane) {
-                L[we] = __int_as_float(0x7fc00000);
-                bv = -INFINITY;
-                be = 0x7fffffff;
-                for (int e = lane; e < E; e += 32) {
-                    const float v = L[e];
-                    if (v > bv || (v == bv && e < be)) {
-                        bv = v;
-                        be = e;
-                    }
-                }
-            }
-        }
-        const float m = __shfl_sync(0xffffffffu, myv, 0);
-        int rank = 0;
-        for (int j = 0; j < K; ++j) rank += (__shfl_sync(0xffffffffu, mye, j) < mye) ? 1 : 0;
-        float* ex = L + E;
-        float e_k = 0.0f;
-        if (lane < K) {
-            e_k = expf(myv - m);
-            ex[rank] = e_k;
-            s_ids[wid][rank] = mye;
-        }
-        __syncwarp();
-        float sum = 0.0f;
-        for (int r = 0; r < K; ++r) sum += ex[r];
-        if (lane < K) s_w[wid][rank] = e_k / sum;
-        __syncwarp();
+        select_topk_keys(E, K, Lk, L + E, s_ids[wid], s_w[wid], lane);
     }
-    if (a.logits_user)
-        for (int e = lane; e < E; e += 32) a.logits_user[size_t(t) * E + e] = __ldcg(lg + e);
     for (int k = lane; k < K; k += 32) {
         const size_t o = size_t(t) * K + k;
         a.ids[o] = s_ids[wid][k];
@@ -138,9 +111,9 @@ __global__ void __launch_bounds__(256) k_pf_select(PfSelectLaunch a) {
         if (a.w_user) a.w_user[o] = s_w[wid][k];
     }
     if (lane == 0) {
-        const float s = 1.0f / (1.0f + expf(-__ldcg(lg + E)));
-        a.sig[t] = s;
-        if (a.sig_user) a.sig_user[t] = s;
+        const float sg = 1.0f / (1.0f + expf(-s_gate[wid]));
+        a.sig[t] = sg;
+        if (a.sig_user) a.sig_user[t] = sg;
     }
 }
 
@@ -455,312 +428,123 @@ __global__ void k_pf_combine(const void* y, const __half* y_sh, const int32_t* i
     }
 }
 
-// ------------------------------------------------------------------ GEMM
-// Persistent grouped GEMM, one CTA per SM, six warps:
-//   warp 0      TMA producer (A and B stages; the tile's scales)
-//   warp 1      TMEM allocation; lane 0 issues the MMAs
-//   warps 2..5  dequantise B into the swizzled fp16 tile, then read the
-//               accumulator out of TMEM (warp w owns TMEM lanes
-//               32 (w % 4) .. +32) and store the tile
-// A tile: 128 rows x 64 K (fp16 or bf16), B tile: BN rows x 64 K; the MMA is
-// M = 128, N = BN, K = 16, four per stage.
-constexpr int kPfThreads = 192;
-constexpr int kTmemCols = 256;
+// ------------------------------------------------------------ router GEMM
+// K slices of logits^T = router * x^T on the tensor cores.  A = 128 router
+// rows (experts; the tile past the last expert holds the shared-gate row and
+// the TMA's zero fill), B = 256 tokens, both bf16, K-major, 64-wide K blocks
+// by TMA with the 128-byte swizzle; fp32 accumulator in TMEM.  With the
+// experts along the TMEM lanes a warp's store writes 32 consecutive logits of
+// one token.  One CTA takes one (expert tile, token tile, K slice) and writes
+// its partial products; the selection adds the slices in slice order, so the
+// result does not depend on scheduling.
+constexpr int kRtThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kRtBN = 256;               // tokens per tile
+constexpr int kRtStages = 4;
+constexpr uint32_t kRtABytes = kBM * 128u;
+constexpr uint32_t kRtStageBytes = kRtABytes + kRtBN * 128u;
 
-struct GemmSmem {
-    uint32_t stage_bytes, a_off, b_off, pk_off, sc_off, total;
+struct RouterLaunch {
+    float* part;               // [S][T][E + 1]
+    uint32_t* err;
+    int T, E, S, kbt, n_ttiles;
 };
 
-__host__ __device__ inline GemmSmem gemm_smem(int mode, int BN, int K, int stages) {
-    GemmSmem s{};
-    s.a_off = 0;
-    s.b_off = kBM * 128;
-    s.pk_off = s.b_off + uint32_t(BN) * 128;
-    s.stage_bytes = s.pk_off + (mode == kGemmRouter ? 0u : uint32_t(BN) * 32u);
-    s.sc_off = uint32_t(stages) * s.stage_bytes;
-    s.total = s.sc_off + (mode == kGemmRouter ? 0u : uint32_t(BN) * uint32_t(K / 32) * 2u);
-    return s;
-}
-
-// Dequantise one 64-wide K slice of one B row: 32 packed bytes and two
-// scales -> 64 fp16 in the operand order, 8 chunks of 16 bytes stored with
-// the 128-byte swizzle (chunk c of row r at (c ^ (r & 7)) * 16).
-__device__ __forceinline__ void dequant_row64(const uint8_t* pk, const uint16_t* sc2,
-                                              uint8_t* brow, int r) {
-    const uint4 w0 = *reinterpret_cast<const uint4*>(pk);
-    const uint4 w1 = *reinterpret_cast<const uint4*>(pk + 16);
-    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    const __half2 s0 = __halves2half2(__ushort_as_half(sc2[0]), __ushort_as_half(sc2[0]));
-    const __half2 s1 = __halves2half2(__ushort_as_half(sc2[1]), __ushort_as_half(sc2[1]));
-    const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const __half2 s = (c < 4) ? s0 : s1;
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t b = ((words[c] >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
-            const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&b), off);  // exact
-            const __half2 v = __hmul2(q, s);
-            o[j] = *reinterpret_cast<const uint32_t*>(&v);
-        }
-        *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(kPfThreads, 1)
-    k_pf_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a2,
-              const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_bs,
-              const __grid_constant__ CUtensorMap map_b2, const __grid_constant__ CUtensorMap map_bs2,
-              GemmLaunch a) {
-    extern __shared__ uint8_t pf_dyn[];
-    __shared__ __align__(8) uint64_t full[kPfMaxStages], deq[kPfMaxStages], empty[kPfMaxStages];
-    __shared__ __align__(8) uint64_t acc_full, acc_empty, sc_full, sc_empty;
+__global__ void __launch_bounds__(kRtThreads, 1)
+    k_pf_router(const __grid_constant__ CUtensorMap map_r, const __grid_constant__ CUtensorMap map_x,
+                RouterLaunch a) {
+    extern __shared__ uint8_t rt_dyn[];
+    __shared__ __align__(8) uint64_t full[kRtStages], empty[kRtStages];
+    __shared__ __align__(8) uint64_t acc_full;
     __shared__ uint32_t tmem_base;
-    __shared__ int s_ntiles;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int S = a.stages, BN = a.BN;
-    const bool int4b = MODE != kGemmRouter;
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pf_dyn) + 1023) &
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rt_dyn) + 1023) &
                                                ~uintptr_t(1023));
-    const GemmSmem L = gemm_smem(MODE, BN, a.K_max, S);
+    const int item = blockIdx.x;
+    const int sl = item % a.S, nt = (item / a.S) % a.n_ttiles, mt = item / (a.S * a.n_ttiles);
+    const int kb0 = sl * a.kbt / a.S, nkb = (sl + 1) * a.kbt / a.S - kb0;   // S <= kbt: nkb >= 1
 
     pdl_launch();
     if (tid == 0) {
-        for (int i = 0; i < S; ++i) {
+        for (int i = 0; i < kRtStages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&deq[i], 128);
             mbar_init(&empty[i], 1);
         }
         mbar_init(&acc_full, 1);
-        mbar_init(&acc_empty, 128);
-        mbar_init(&sc_full, 1);
-        mbar_init(&sc_empty, 128);
         mbar_fence_init();
-        tma_prefetch_map(&map_a);
-        tma_prefetch_map(&map_b);
+        tma_prefetch_map(&map_r);
+        tma_prefetch_map(&map_x);
     }
     if (wid == 1) {
-        tmem_alloc(&tmem_base, kTmemCols);
+        tmem_alloc(&tmem_base, kRtBN);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     pdl_wait();
-    if (tid == 0) s_ntiles = (MODE == kGemmRouter ? a.router_mblocks : __ldcg(a.n_mblocks)) * a.nb_max;
-    __syncthreads();
-    const int n_tiles = s_ntiles;
     const uint32_t tmem = tmem_base;
-    const uint32_t idesc_full = idesc_f16(kBM, BN, MODE == kGemmRouter ? 1 : 0);
-
-    // tile -> (m-block, n-block); returns false when the n-block does not
-    // exist for the m-block's group
-    auto tile_info = [&](int tile, int& group, int& row, int& nrows, int& n0, int& N, int& K) {
-        const int mb = tile / a.nb_max, nb = tile % a.nb_max;
-        if (MODE == kGemmRouter) {
-            group = 0;
-            row = mb * kBM;
-            nrows = min(kBM, a.M - row);
-            N = a.N;
-            K = a.K;
-        } else {
-            const MBlock m = a.mblocks[mb];
-            group = m.group;
-            row = m.row;
-            nrows = m.nrows;
-            const bool sh = group == a.E;
-            N = sh ? a.N2 : a.N;
-            K = sh ? a.K2 : a.K;
-        }
-        n0 = nb * BN;
-        return n0 < N;
-    };
 
     if (wid == 0) {
-        // ------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t kbt = 0, ti = 0;
-            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-                int g, row, nrows, n0, N, K;
-                if (!tile_info(tile, g, row, nrows, n0, N, K)) continue;
-                const bool sh = int4b && g == a.E;
-                const CUtensorMap* ma = (sh && MODE == kGemmDown) ? &map_a2 : &map_a;
-                const CUtensorMap* mbq = sh ? &map_b2 : &map_b;
-                const CUtensorMap* mbs = sh ? &map_bs2 : &map_bs;
-                const int arow = (sh && MODE == kGemmGateUp) ? a.a_shared_row0 + row : row;
-                const int brow = (int4b && !sh) ? g * N + n0 : n0;
-                if (int4b) {
-                    if (ti > 0 && !mbar_wait(&sc_empty, (ti - 1) & 1))
-                        latch_timeout(a.err, 11, 0, ti, tile);
-                    mbar_expect_tx(&sc_full, uint32_t(BN) * uint32_t(K / 32) * 2u);
-                    tma_load_2d(base + L.sc_off, mbs, 0, brow, &sc_full);
-                }
-                const int kbn = K / kBK;
-                for (int kb = 0; kb < kbn; ++kb, ++kbt) {
-                    const int s = int(kbt % S);
-                    const uint32_t round = kbt / S;
-                    if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1))
-                        latch_timeout(a.err, 12, s, round, tile);
-                    uint8_t* st = base + size_t(s) * L.stage_bytes;
-                    const uint32_t bbytes = int4b ? uint32_t(BN) * 32u : uint32_t(BN) * 128u;
-                    mbar_expect_tx(&full[s], uint32_t(kBM) * 128u + bbytes);
-                    tma_load_2d(st + L.a_off, ma, kb * kBK, arow, &full[s]);
-                    if (int4b)
-                        tma_load_2d(st + L.pk_off, mbq, kb * (kBK / 2), brow, &full[s]);
-                    else
-                        tma_load_2d(st + L.b_off, mbq, kb * kBK, brow, &full[s]);
-                }
-                ++ti;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kRtStages, round = kb / kRtStages;
+                if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1))
+                    latch_timeout(a.err, 50, s, round, item);
+                uint8_t* st = base + size_t(s) * kRtStageBytes;
+                mbar_expect_tx(&full[s], kRtStageBytes);
+                tma_load_2d(st, &map_r, (kb0 + kb) * kBK, mt * kBM, &full[s]);
+                tma_load_2d(st + kRtABytes, &map_x, (kb0 + kb) * kBK, nt * kRtBN, &full[s]);
+            }
+            // every copy has landed before the CTA exits
+            for (int i = 0; i < kRtStages && i < nkb; ++i) {
+                const int kb = nkb - 1 - i;
+                mbar_wait(&full[kb % kRtStages], (kb / kRtStages) & 1);
             }
         }
     } else if (wid == 1) {
-        // ----------------------------------------------------------- MMA
         if (lane == 0) {
-            uint32_t kbt = 0, ti = 0;
-            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-                int g, row, nrows, n0, N, K;
-                if (!tile_info(tile, g, row, nrows, n0, N, K)) continue;
-                if (ti > 0 && !mbar_wait(&acc_empty, (ti - 1) & 1))
-                    latch_timeout(a.err, 13, 0, ti, tile);
+            const uint32_t idesc = idesc_f16(kBM, kRtBN, 1);
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kRtStages, round = kb / kRtStages;
+                if (!mbar_wait(&full[s], round & 1)) latch_timeout(a.err, 51, s, round, item);
                 tc_fence_after();
-                const int kbn = K / kBK;
-                for (int kb = 0; kb < kbn; ++kb, ++kbt) {
-                    const int s = int(kbt % S);
-                    const uint32_t round = kbt / S;
-                    if (!mbar_wait(int4b ? &deq[s] : &full[s], round & 1))
-                        latch_timeout(a.err, 14, s, round, tile);
-                    tc_fence_after();
-                    const uint32_t st = smem_u32(base + size_t(s) * L.stage_bytes);
+                const uint32_t st = smem_u32(base + size_t(s) * kRtStageBytes);
+                const uint64_t ad = sdesc_k_sw128(st), bd = sdesc_k_sw128(st + kRtABytes);
 #pragma unroll
-                    for (int j = 0; j < kBK / 16; ++j) {
-                        const uint64_t ad = sdesc_k_sw128(st + L.a_off + 32u * j);
-                        const uint64_t bd = sdesc_k_sw128(st + L.b_off + 32u * j);
-                        umma_f16(tmem, ad, bd, idesc_full, (kb | j) != 0 ? 1u : 0u);
-                    }
-                    umma_commit(&empty[s]);
-                }
-                umma_commit(&acc_full);
-                ++ti;
+                for (int j = 0; j < kBK / 16; ++j)      // + 32 bytes a K step
+                    umma_f16(tmem, ad + uint64_t(2 * j), bd + uint64_t(2 * j), idesc,
+                             (kb | j) != 0 ? 1u : 0u);
+                umma_commit(&empty[s]);
             }
+            umma_commit(&acc_full);
+            mbar_wait(&acc_full, 0);
         }
     } else {
-        // ---------------------------------------- dequant + epilogue
-        const int dq = tid - 64;                 // 0..127
-        const int q = wid & 3;                   // TMEM lane quarter of this warp
-        const int m = q * 32 + lane;             // accumulator row of this thread
-        uint32_t kbt = 0, ti = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-            int g, row, nrows, n0, N, K;
-            if (!tile_info(tile, g, row, nrows, n0, N, K)) continue;
-            const bool sh = int4b && g == a.E;
-            const int kbn = K / kBK;
-            if (int4b && !mbar_wait(&sc_full, ti & 1)) latch_timeout(a.err, 15, 0, ti, tile);
-            const uint16_t* sct = reinterpret_cast<const uint16_t*>(base + L.sc_off);
-            for (int kb = 0; kb < kbn; ++kb, ++kbt) {
-                const int s = int(kbt % S);
-                const uint32_t round = kbt / S;
-                if (int4b) {
-                    if (!mbar_wait(&full[s], round & 1)) latch_timeout(a.err, 16, s, round, tile);
-                    uint8_t* st = base + size_t(s) * L.stage_bytes;
-                    for (int r = dq; r < BN; r += 128)
-                        dequant_row64(st + L.pk_off + r * 32, sct + size_t(r) * (K / 32) + 2 * kb,
-                                      st + L.b_off + r * 128, r);
-                    fence_proxy_async_smem();
-                    mbar_arrive(&deq[s]);
+        // warp w reads TMEM lanes 32 (w % 4) .. +32: router rows (logit columns)
+        const int q = wid & 3;
+        const int r = mt * kBM + q * 32 + lane;
+        const size_t ld = size_t(a.E) + 1;
+        float* out = a.part + size_t(sl) * size_t(a.T) * ld + r;
+        if (!mbar_wait(&acc_full, 0)) latch_timeout(a.err, 52, 0, 0, item);
+        tc_fence_after();
+        const int t0 = nt * kRtBN;
+        for (int c = 0; c < kRtBN / 32 && t0 + 32 * c < a.T; ++c) {    // warp-uniform
+            uint32_t v[32];
+            tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(32 * c), v);
+            tmem_ld_wait();
+            if (r <= a.E) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int t = t0 + 32 * c + j;
+                    if (t < a.T) out[size_t(t) * ld] = __uint_as_float(v[j]);
                 }
             }
-            if (int4b) mbar_arrive(&sc_empty);
-
-            // epilogue
-            if (!mbar_wait(&acc_full, ti & 1)) latch_timeout(a.err, 17, 0, ti, tile);
-            tc_fence_after();
-            const bool valid = m < nrows;
-            const uint32_t tl = tmem + (uint32_t(q * 32) << 16);
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tl + uint32_t(c * 32), v);
-                tmem_ld_wait();
-                if (!valid) continue;
-                const int col0 = n0 + c * 32;
-                if (MODE == kGemmRouter) {
-                    float* o = a.out_f32 + size_t(row + m) * a.ldo;
-                    for (int j = 0; j < 32; ++j) {
-                        const int n = col0 + j;
-                        if (n < a.N_valid)
-                            o[n] = __uint_as_float(v[j]) +
-                                   ((a.bias != nullptr && n < a.E) ? __ldg(a.bias + n) : 0.0f);
-                    }
-                } else if (MODE == kGemmGateUp) {
-                    // h_i = silu(gate) * up for 16 pairs, stored in the operand order
-                    float hv[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        hv[i] = silu_mul(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                    const int ld = sh ? a.ld2 : a.ldo;
-                    if (!sh && a.out_f32 != nullptr) {
-                        // natural order, fp32 (the h of the stage-wise calls)
-                        float4* h32 = reinterpret_cast<float4*>(a.out_f32 + size_t(row + m) * ld +
-                                                                col0 / 2);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            h32[j] = make_float4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2],
-                                                 hv[4 * j + 3]);
-                    }
-                    __half* hrow = (sh ? a.out2_f16 : a.out_f16) + size_t(row + m) * ld + col0 / 2;
-#pragma unroll
-                    for (int gq = 0; gq < 2; ++gq) {
-                        const float* f = hv + 8 * gq;
-                        const __half2 h0 = __floats2half2_rn(f[0], f[4]);
-                        const __half2 h1 = __floats2half2_rn(f[1], f[5]);
-                        const __half2 h2 = __floats2half2_rn(f[2], f[6]);
-                        const __half2 h3 = __floats2half2_rn(f[3], f[7]);
-                        *reinterpret_cast<uint4*>(hrow + 8 * gq) =
-                            make_uint4(*reinterpret_cast<const uint32_t*>(&h0),
-                                       *reinterpret_cast<const uint32_t*>(&h1),
-                                       *reinterpret_cast<const uint32_t*>(&h2),
-                                       *reinterpret_cast<const uint32_t*>(&h3));
-                    }
-                } else if (!sh && a.out_bf16 != nullptr) {
-                    // y in bf16 (the stage-wise calls' format)
-                    uint16_t* yrow = a.out_bf16 + size_t(row + m) * a.ldo + col0;
-#pragma unroll
-                    for (int gq = 0; gq < 4; ++gq) {
-                        uint32_t o[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            o[j] = uint32_t(f32_to_bf16(__uint_as_float(v[8 * gq + 2 * j]))) |
-                                   (uint32_t(f32_to_bf16(__uint_as_float(v[8 * gq + 2 * j + 1])))
-                                    << 16);
-                        *reinterpret_cast<uint4*>(yrow + 8 * gq) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                } else {
-                    // y in fp16: the combine sums several of them before the
-                    // output's own rounding
-                    __half* yrow = (sh ? a.out2_f16 : a.out_f16) + size_t(row + m) * a.ldo + col0;
-#pragma unroll
-                    for (int gq = 0; gq < 4; ++gq) {
-                        uint32_t o[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const __half2 hv2 = __floats2half2_rn(__uint_as_float(v[8 * gq + 2 * j]),
-                                                                  __uint_as_float(v[8 * gq + 2 * j + 1]));
-                            o[j] = *reinterpret_cast<const uint32_t*>(&hv2);
-                        }
-                        *reinterpret_cast<uint4*>(yrow + 8 * gq) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&acc_empty);
-            ++ti;
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (wid == 1) tmem_dealloc(tmem, kTmemCols);
+    if (wid == 1) tmem_dealloc(tmem, kRtBN);
 }
 
 // ------------------------------------------------------------------ host
@@ -816,28 +600,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t sme
     return e;
 }
 
-int pick_stages(int mode, int BN, int K) {
-    for (int S = kPfMaxStages; S >= 2; --S) {
-        const GemmSmem L = gemm_smem(mode, BN, K, S);
-        if (L.total + 1024 <= kPfSmemBudget) return S;
-    }
-    return 0;
-}
-
-template <int MODE>
-cudaError_t run_gemm(GemmLaunch g, const CUtensorMap& ma, const CUtensorMap& ma2,
-                     const CUtensorMap& mb, const CUtensorMap& mbs, const CUtensorMap& mb2,
-                     const CUtensorMap& mbs2, cudaStream_t s) {
-    const Dev d = device_info();
-    g.stages = pick_stages(MODE, g.BN, g.K_max);
-    if (g.stages < 2) return cudaErrorInvalidValue;
-    const size_t dyn = gemm_smem(MODE, g.BN, g.K_max, g.stages).total + 1024;
-    cudaError_t e = cudaFuncSetAttribute(k_pf_gemm<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn));
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k_pf_gemm<MODE>, d.sms, kPfThreads, dyn, s, ma, ma2, mb, mbs, mb2, mbs2, g);
-}
-
 }  // namespace
 
 bool prefill_supported(const strata_moe_dims& d) {
@@ -847,29 +609,27 @@ bool prefill_supported(const strata_moe_dims& d) {
 }
 
 cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s) {
-    // logits = x * router^T
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, r.x, r.H, r.T, kBK, kBM, true) ||
-        !make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, r.router, r.H, r.E + 1, kBK, 128, true))
+    // logit slices: router rows in 128-row boxes, tokens in 256-row boxes
+    CUtensorMap mr, mx;
+    if (!make_map(&mr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, r.router, r.H, r.E + 1, kBK, kBM, true) ||
+        !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, r.x, r.H, r.T, kBK, kRtBN, true))
         return cudaErrorInvalidValue;
-    GemmLaunch g{};
-    g.BN = 128;
-    g.N = r.E + 1;
-    g.N_valid = r.E + 1;
-    g.K = r.H;
-    g.K_max = r.H;
-    g.M = r.T;
-    g.router_mblocks = (r.T + kBM - 1) / kBM;
-    g.nb_max = (r.E + 1 + 127) / 128;
-    g.out_f32 = r.logits;
-    g.bias = r.bias;
-    g.E = r.E;
-    g.ldo = r.E + 1;
-    g.err = r.err;
-    cudaError_t e = run_gemm<kGemmRouter>(g, ma, ma, mb, mb, mb, mb, s);
+    const int n_mt = (r.E + 1 + kBM - 1) / kBM, n_tt = (r.T + kRtBN - 1) / kRtBN, kbt = r.H / kBK;
+    // enough K slices to give every SM one tile
+    int S = device_info().sms / (n_mt * n_tt);
+    S = S < 1 ? 1 : (S > kRouterSplitMax ? kRouterSplitMax : S);
+    S = S > kbt ? kbt : S;
+    RouterLaunch g{r.part, r.err, r.T, r.E, S, kbt, n_tt};
+    const size_t dyn = size_t(kRtStages) * kRtStageBytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(k_pf_router, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(dyn));
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(k_pf_router, n_mt * n_tt * S, kRtThreads, dyn, s, mr, mx, g);
     if (e != cudaSuccess) return e;
     PfSelectLaunch sl{};
-    sl.logits = r.logits;
+    sl.part = r.part;
+    sl.nsplit = S;
+    sl.bias = r.bias;
     sl.logits_user = r.logits_user;
     sl.forced_ids = r.forced_ids;
     sl.forced_w = r.forced_w;
@@ -883,8 +643,8 @@ cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s) {
     sl.T = r.T;
     sl.E = r.E;
     sl.K = r.K;
-    const size_t dyn = size_t(8) * (r.E + 16) * sizeof(float);
-    return launch_pdl(k_pf_select, (r.T + 7) / 8, 256, dyn, s, sl);
+    const size_t sdyn = size_t(8) * (r.E + 16) * sizeof(float);
+    return launch_pdl(k_pf_select, (r.T + 7) / 8, 256, sdyn, s, sl);
 }
 
 cudaError_t launch_prefill_bucket(const PfBucket& b, cudaStream_t s) {

@@ -9,8 +9,9 @@
 // the MMA reads them as its A operand: no dequantised tile goes through
 // shared memory, and N follows the expert's token count (rounded up to 16)
 // instead of padding every expert to 128 rows.  The activations (B) come by
-// TMA into 128-byte-swizzled shared memory, 32 rows a box, as many boxes as
-// the block has rows.
+// TMA into 128-byte-swizzled shared memory, one 3-D box a pipeline stage:
+// the block's rows rounded up to 32 (one tensor map per height) by the
+// stage's two 64-wide K blocks.
 //
 // Warps: 0 TMA producer; 1 and 2 the MMAs (lane 0; warp 1 also allocates
 // the TMEM); 3..10 dequantisation, two sets of four taking alternate K
@@ -55,9 +56,16 @@ constexpr int kSabACols = kSabKS / 2;    // TMEM columns of one A stage (two fp1
 constexpr int kSabDCols = 128;           // one accumulator buffer: up to 128 token columns
 constexpr int kSabACol0 = 2 * kSabDCols; // first A column
 constexpr int kSabTmemCols = 512;
-constexpr int kSabBoxRows = 32;          // activation rows per TMA box
+constexpr int kSabBoxRows = 32;          // activation box heights: 32, 64, 96, 128 rows
+constexpr int kSabXMaps = kBM / kSabBoxRows;
 constexpr uint32_t kSabSubBytes = kBM * 128u;          // 128 rows x 64 fp16 (one MMA K block)
 constexpr uint32_t kSabStageBytes = 2 * kSabSubBytes;  // K = 128: two 64-wide sub-blocks
+
+// Activation maps of one operand, one per box height (rows 32 (i + 1)).
+// The box of map i lands as [2 K blocks][32 (i + 1) rows][64 fp16].
+struct SabXMaps {
+    CUtensorMap m[kSabXMaps];
+};
 // Weight stages: 128 rows x 128 packed bytes = 256 inputs = 2 pipeline
 // stages, one TMA box with the 128-byte swizzle, so every row is read from
 // memory as a whole 128-byte line and a lane's 16-byte reads of its row are
@@ -66,6 +74,10 @@ constexpr uint32_t kSabWBytes = kBM * 128u;
 constexpr int kSabWStages = 3;
 static_assert(kSabStages * kSabACols + kSabACol0 <= kSabTmemCols, "TMEM columns");
 
+// A tile's scales land as [K / 256][128 rows][8 fp16]: the 8 scales of a
+// row for 256 inputs (two pipeline stages) side by side, so a stage's read
+// of 8 bytes per row by 32 consecutive rows spans only a few wavefronts
+// (row-major [128][K / 32] put all 32 rows of a warp in one bank).
 __host__ __device__ inline uint32_t sab_scale_bytes(int K_max) {
     return uint32_t(kBM) * uint32_t(K_max / 32) * 2u;
 }
@@ -108,9 +120,10 @@ __device__ __forceinline__ void dequant_row_regs(const uint4& w0, const uint4& w
 }
 
 // Descriptor step (16-byte units) from a stage's first K step to step j:
-// sub-block j / 4, 32 (j % 4) bytes into its 128-byte rows.
-__device__ __forceinline__ uint64_t sab_boff(int j) {
-    return uint64_t((uint32_t(j >> 2) * kSabSubBytes + 32u * uint32_t(j & 3)) >> 4);
+// K block j / 4 (bsub: its size in 16-byte units), 32 (j % 4) bytes into
+// its 128-byte rows.
+__device__ __forceinline__ uint64_t sab_boff(int j, uint32_t bsub) {
+    return uint64_t(uint32_t(j >> 2) * bsub + 2u * uint32_t(j & 3));
 }
 
 // Accumulators of a tile with npad token columns: two (one per MMA warp,
@@ -137,7 +150,7 @@ __device__ __forceinline__ int mma_pos(int i) {
 
 template <int MODE>
 __global__ void __launch_bounds__(kSabThreads, 1)
-    k_pf_gemm_sab(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_x2,
+    k_pf_gemm_sab(const __grid_constant__ SabXMaps map_x, const __grid_constant__ SabXMaps map_x2,
                   const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_ws,
                   const __grid_constant__ CUtensorMap map_w2,
                   const __grid_constant__ CUtensorMap map_ws2, GemmLaunch a) {
@@ -176,7 +189,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         }
         mbar_init(&mma_done, kSabMmaWarps);
         mbar_fence_init();
-        tma_prefetch_map(&map_x);
+        for (int i = 0; i < kSabXMaps; ++i) tma_prefetch_map(&map_x.m[i]);
         tma_prefetch_map(&map_w);
     }
     if (wid == 1) {
@@ -194,10 +207,19 @@ __global__ void __launch_bounds__(kSabThreads, 1)
 
     // tile -> (token block, 128-row weight tile); false when the weight tile
     // does not exist for the block's group
-    auto tile_info = [&](int tile, int& g, int& row, int& nrows, int& mt, int& W, int& K) {
-        const int mb = tile / a.nb_max;
+    // Every role reads the next tile's block entry one tile ahead, so its L2
+    // round trip overlaps the current tile.
+    auto fetch = [&](int tile) {
+        MBlock m{0, 0, 0, 0};
+        if (tile < n_tiles) {
+            const int4 v = __ldcg(reinterpret_cast<const int4*>(a.mblocks) + tile / a.nb_max);
+            m = MBlock{v.x, v.y, v.z, v.w};
+        }
+        return m;
+    };
+    auto tile_info = [&](int tile, const MBlock& m, int& g, int& row, int& nrows, int& mt, int& W,
+                         int& K) {
         mt = tile % a.nb_max;
-        const MBlock m = a.mblocks[mb];
         g = m.group;
         row = m.row;
         nrows = m.nrows;
@@ -213,11 +235,15 @@ __global__ void __launch_bounds__(kSabThreads, 1)
             uint32_t kst = 0, ti = 0;               // pipeline stages and tiles so far
             uint32_t ws = 0, wph = 0;               // weight ring slot and phase
             uint32_t wcount = 0;                     // weight stages so far
+            MBlock mb_next = fetch(blockIdx.x);
             for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+                const MBlock mb = mb_next;
+                mb_next = fetch(tile + int(gridDim.x));
                 int g, row, nrows, mt, W, K;
-                if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
+                if (!tile_info(tile, mb, g, row, nrows, mt, W, K)) continue;
                 const bool sh = g == a.E;
-                const CUtensorMap* mx = (sh && MODE == kGemmDown) ? &map_x2 : &map_x;
+                const int nbox = (nrows + kSabBoxRows - 1) / kSabBoxRows;
+                const CUtensorMap* mx = &((sh && MODE == kGemmDown) ? map_x2 : map_x).m[nbox - 1];
                 const CUtensorMap* mw = sh ? &map_w2 : &map_w;
                 const CUtensorMap* mws = sh ? &map_ws2 : &map_ws;
                 const int xrow = (sh && MODE == kGemmGateUp) ? a.a_shared_row0 + row : row;
@@ -226,8 +252,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                 if (sround > 0 && !sab_wait(&sc_empty[buf], (sround - 1) & 1, a.err))
                     latch_timeout(a.err, 31, buf, sround, tile);
                 mbar_expect_tx(&sc_full[buf], uint32_t(kBM) * uint32_t(K / 32) * 2u);
-                tma_load_2d(sc_base + buf * scb, mws, 0, wrow, &sc_full[buf]);
-                const int nbox = (nrows + kSabBoxRows - 1) / kSabBoxRows;
+                tma_load_3d(sc_base + buf * scb, mws, 0, wrow, 0, &sc_full[buf]);
                 const uint32_t xbytes = uint32_t(nbox) * (kSabBoxRows * 128u) * 2u;
                 const int nks = K / kSabKS;
                 for (int ks = 0; ks < nks; ++ks, ++kst) {
@@ -249,12 +274,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                         latch_timeout(a.err, 32, s, round, tile);
                     uint8_t* st = base + s * kSabStageBytes;
                     mbar_expect_tx(&full[s], xbytes);
-                    for (int b = 0; b < nbox; ++b) {
-                        tma_load_2d(st + b * (kSabBoxRows * 128), mx, ks * kSabKS,
-                                    xrow + b * kSabBoxRows, &full[s]);
-                        tma_load_2d(st + kSabSubBytes + b * (kSabBoxRows * 128), mx,
-                                    ks * kSabKS + kBK, xrow + b * kSabBoxRows, &full[s]);
-                    }
+                    tma_load_3d(st, mx, 0, xrow, 2 * ks, &full[s]);
                 }
                 ++ti;
             }
@@ -279,9 +299,12 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         if (lane == 0) {
             const int mw = wid - 1;          // with two accumulators: K steps j % 2 == mw
             uint32_t kst = 0, ti = 0;
+            MBlock mb_next = fetch(blockIdx.x);
             for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+                const MBlock mb = mb_next;
+                mb_next = fetch(tile + int(gridDim.x));
                 int g, row, nrows, mt, W, K;
-                if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
+                if (!tile_info(tile, mb, g, row, nrows, mt, W, K)) continue;
                 const uint32_t dbuf = ti & 1u, dround = ti >> 1;
                 if (dround > 0 && !sab_wait(&acc_empty[dbuf], (dround - 1) & 1, a.err))
                     latch_timeout(a.err, 33, dbuf, dround, tile);
@@ -289,6 +312,9 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                 const int npad = (nrows + 15) & ~15;
                 const int nacc = sab_accumulators(npad);
                 const uint32_t idesc = idesc_f16(kBM, npad, 0);
+                // the stage's second K block follows the first's box rows
+                const uint32_t bsub = uint32_t((nrows + kSabBoxRows - 1) / kSabBoxRows) *
+                                      (kSabBoxRows * 128u / 16u);
                 const uint32_t d_tmem = tmem + dbuf * kSabDCols + uint32_t(mw * (kSabDCols / 2));
                 const int nks = K / kSabKS;
                 for (int ks = 0; ks < nks; ++ks, ++kst) {
@@ -306,7 +332,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                         if (mw == 0) {
 #pragma unroll
                             for (int j = 0; j < kSabKS / 16; ++j)
-                                umma_f16_tmem_a(d_tmem, a0 + uint32_t(8 * j), b0 + sab_boff(j),
+                                umma_f16_tmem_a(d_tmem, a0 + uint32_t(8 * j), b0 + sab_boff(j, bsub),
                                                 idesc, (ks | j) != 0 ? 1u : 0u);
                         }
                     } else {
@@ -314,7 +340,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                         const uint32_t am = a0 + uint32_t(8 * mw);
 #pragma unroll
                         for (int jj = 0; jj < kSabKS / 32; ++jj)
-                            umma_f16_tmem_a(d_tmem, am + uint32_t(16 * jj), bm + sab_boff(2 * jj),
+                            umma_f16_tmem_a(d_tmem, am + uint32_t(16 * jj), bm + sab_boff(2 * jj, bsub),
                                             idesc, (ks | jj) != 0 ? 1u : 0u);
                     }
                     umma_commit(&empty[s]);
@@ -333,13 +359,16 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         const uint32_t set = uint32_t(wid - kSabDeq0) >> 2;   // this set's stages: kst % 2 == set
         uint32_t kst = 0, ti = 0;
         uint32_t ws = 0, wph = 0;
+        MBlock mb_next = fetch(blockIdx.x);
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            const MBlock mb = mb_next;
+            mb_next = fetch(tile + int(gridDim.x));
             int g, row, nrows, mt, W, K;
-            if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
+            if (!tile_info(tile, mb, g, row, nrows, mt, W, K)) continue;
             const uint32_t buf = ti & 1u, sround = ti >> 1;
             if (!sab_wait(&sc_full[buf], sround & 1, a.err))
                 latch_timeout(a.err, 36, buf, sround, tile);
-            const uint32_t scrow = smem_u32(sc_base + buf * scb) + uint32_t(m * (K / 32) * 2);
+            const uint32_t scrow = smem_u32(sc_base + buf * scb) + uint32_t(m * 16);
             const int nks = K / kSabKS;
             for (int ks = 0; ks < nks; ++ks, ++kst) {
                 const uint32_t cws = ws, cwph = wph;
@@ -353,10 +382,9 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                 const uint32_t s = kst & (kSabStages - 1), round = kst / kSabStages;
                 if (!sab_wait(&wfull[cws], cwph, a.err)) latch_timeout(a.err, 37, cws, kst, tile);
                 const uint32_t wrow_s = smem_u32(w_base + cws * kSabWBytes) + uint32_t(m * 128);
-                const uint2 sc4 = make_uint2(
-                    uint32_t(lds_u16(scrow + 8u * ks)) | (uint32_t(lds_u16(scrow + 8u * ks + 2u)) << 16),
-                    uint32_t(lds_u16(scrow + 8u * ks + 4u)) |
-                        (uint32_t(lds_u16(scrow + 8u * ks + 6u)) << 16));
+                // the stage's 4 scales: group ks / 2, half ks % 2
+                const uint2 sc4 =
+                    lds_u2(scrow + uint32_t(ks >> 1) * (kBM * 16u) + uint32_t(ks & 1) * 8u);
                 if (round > 0 && !sab_wait(&empty[s], (round - 1) & 1, a.err))
                     latch_timeout(a.err, 38, s, round, tile);
                 tc_fence_after();
@@ -386,9 +414,12 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         const int q = wid & 3;
         const int m = q * 32 + lane;           // weight row of the tile
         uint32_t ti = 0;
+        MBlock mb_next = fetch(blockIdx.x);
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            const MBlock mb = mb_next;
+            mb_next = fetch(tile + int(gridDim.x));
             int g, row, nrows, mt, W, K;
-            if (!tile_info(tile, g, row, nrows, mt, W, K)) continue;
+            if (!tile_info(tile, mb, g, row, nrows, mt, W, K)) continue;
             const bool sh = g == a.E;
             const uint32_t dbuf = ti & 1u, dround = ti >> 1;
             if (!sab_wait(&acc_full[dbuf], dround & 1, a.err))
@@ -499,15 +530,48 @@ bool sab_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base
     return r == CUDA_SUCCESS;
 }
 
+// Scale map of a row-major [rows][K / 32] fp16 array viewed as (8 scales,
+// rows, K / 256 groups); the box (8, 128, K / 256) is one tile's scales.
+bool sab_scale_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
+    auto fn = sab_encode_fn();
+    if (fn == nullptr || base == nullptr) return false;
+    const cuuint64_t gdim[3] = {8, rows, K / 256};
+    const cuuint64_t gstride[2] = {K / 16, 16};
+    const cuuint32_t box[3] = {8, cuuint32_t(kBM), cuuint32_t(K / 256)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), gdim, gstride, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Activation maps of a row-major [rows][K] fp16 array viewed as (64
+// elements, rows, K / 64 blocks): the box (64, 32 (i + 1), 2) lands as two
+// 64-wide K blocks one after the other, each with the 128-byte swizzle.
+bool sab_xmaps(SabXMaps* m, const void* base, uint64_t K, uint64_t rows) {
+    auto fn = sab_encode_fn();
+    if (fn == nullptr || base == nullptr) return false;
+    const cuuint64_t gdim[3] = {uint64_t(kBK), rows, K / kBK};
+    const cuuint64_t gstride[2] = {K * 2, uint64_t(kBK) * 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    for (int i = 0; i < kSabXMaps; ++i) {
+        const cuuint32_t box[3] = {cuuint32_t(kBK), cuuint32_t(kSabBoxRows * (i + 1)), 2};
+        if (fn(&m->m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), gdim,
+               gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
 template <int MODE>
-cudaError_t run_sab(GemmLaunch g, const CUtensorMap& mx, const CUtensorMap& mx2,
+cudaError_t run_sab(GemmLaunch g, const SabXMaps& mx, const SabXMaps& mx2,
                     const CUtensorMap& mw, const CUtensorMap& mws, const CUtensorMap& mw2,
                     const CUtensorMap& mws2, cudaStream_t s) {
     const Dev d = device_info();
     const size_t dyn = size_t(kSabStages) * kSabStageBytes + size_t(kSabWStages) * kSabWBytes +
                        2 * size_t(sab_scale_bytes(g.K_max)) + 1024;
     if (dyn > kPfSmemBudget || g.K % 256 != 0 || g.K2 % 256 != 0) return cudaErrorInvalidValue;
-    g.stages = kSabStages;
     cudaError_t e = cudaFuncSetAttribute(k_pf_gemm_sab<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn));
     if (e != cudaSuccess) return e;
@@ -530,24 +594,21 @@ cudaError_t run_sab(GemmLaunch g, const CUtensorMap& mx, const CUtensorMap& mx2,
 
 cudaError_t launch_prefill_gate_up(const PfExperts& p, cudaStream_t s) {
     const int H = p.H, I = p.I, Is = p.Is, E = p.E;
-    // activations xg [xg_rows][H] in 32-row boxes; weights: packed rows and
-    // their scales in 128-row boxes.  A weight set the block list cannot name
-    // gets the other set's maps.
-    CUtensorMap mx, mq, ms, mq2, ms2;
-    if (!sab_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.xg, H, p.xg_rows, kBK, kSabBoxRows,
-                 true))
-        return cudaErrorInvalidValue;
+    // activations xg [xg_rows][H]; weights: packed rows and their scales in
+    // 128-row boxes.  A weight set the block list cannot name gets the other
+    // set's maps.
+    SabXMaps mx;
+    CUtensorMap mq, ms, mq2, ms2;
+    if (!sab_xmaps(&mx, p.xg, H, p.xg_rows)) return cudaErrorInvalidValue;
     if (p.routed &&
         (!sab_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.gu_q, H / 2, uint64_t(E) * 2 * I,
                   kSabKS, kBM, true) ||
-         !sab_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.gu_s, H / 32, uint64_t(E) * 2 * I,
-                  H / 32, kBM, false)))
+         !sab_scale_map(&ms, p.gu_s, H, uint64_t(E) * 2 * I)))
         return cudaErrorInvalidValue;
     if (p.shared &&
         (!sab_map(&mq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_gu_q, H / 2, 2 * Is,
                   kSabKS, kBM, true) ||
-         !sab_map(&ms2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.sh_gu_s, H / 32, 2 * Is, H / 32,
-                  kBM, false)))
+         !sab_scale_map(&ms2, p.sh_gu_s, H, 2 * Is)))
         return cudaErrorInvalidValue;
     if (!p.routed) {
         mq = mq2;
@@ -580,21 +641,19 @@ cudaError_t launch_prefill_gate_up(const PfExperts& p, cudaStream_t s) {
 cudaError_t launch_prefill_down(const PfExperts& p, cudaStream_t s) {
     const int T = p.T, K = p.K, H = p.H, I = p.I, Is = p.Is, E = p.E;
     // activations h [T*K][I] (routed) or hs [T][Is] (shared)
-    CUtensorMap mx, mx2, mq, ms, mq2, ms2;
+    SabXMaps mx, mx2;
+    CUtensorMap mq, ms, mq2, ms2;
     if (p.routed &&
-        (!sab_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.h, I, uint64_t(T) * K, kBK,
-                  kSabBoxRows, true) ||
+        (!sab_xmaps(&mx, p.h, I, uint64_t(T) * K) ||
          !sab_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.dn_q, I / 2, uint64_t(E) * H,
                   kSabKS, kBM, true) ||
-         !sab_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.dn_s, I / 32, uint64_t(E) * H, I / 32,
-                  kBM, false)))
+         !sab_scale_map(&ms, p.dn_s, I, uint64_t(E) * H)))
         return cudaErrorInvalidValue;
     if (p.shared &&
-        (!sab_map(&mx2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.hs, Is, T, kBK, kSabBoxRows, true) ||
+        (!sab_xmaps(&mx2, p.hs, Is, T) ||
          !sab_map(&mq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_dn_q, Is / 2, H,
                   kSabKS, kBM, true) ||
-         !sab_map(&ms2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.sh_dn_s, Is / 32, H, Is / 32, kBM,
-                  false)))
+         !sab_scale_map(&ms2, p.sh_dn_s, Is, H)))
         return cudaErrorInvalidValue;
     if (!p.routed) {
         mx = mx2;

@@ -185,6 +185,9 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
 // A lane keeps the best key of its own logits (ids lane, lane+32, ...); each
 // pick is a warp maximum of the lanes' bests (redux), then the lowest id
 // holding it, after which only the winning lane rescans its own logits.
+__device__ inline void select_topk_keys(int E, int K, uint32_t* Lk, float* ex, int* ids, float* w,
+                                        int lane);
+
 __device__ inline void select_topk_warp(const float* lg, int E, int K, float* L, float* ex,
                                         int* ids, float* w, int lane) {
     uint32_t* Lk = reinterpret_cast<uint32_t*>(L);
@@ -198,6 +201,14 @@ __device__ inline void select_topk_warp(const float* lg, int E, int K, float* L,
         for (int j = 0; j < 8; ++j)
             if (e0 + 32 * j < E) Lk[e0 + 32 * j] = logit_key(v[j]);
     }
+    select_topk_keys(E, K, Lk, ex, ids, w, lane);
+}
+
+// The selection itself on the order-preserving keys Lk[0..E) already in
+// this warp's shared scratch (lane-strided writes; consumed, i.e. picked
+// entries are zeroed).
+__device__ inline void select_topk_keys(int E, int K, uint32_t* Lk, float* ex, int* ids, float* w,
+                                        int lane) {
     __syncwarp();
     uint32_t bk = 0u, be = 0x7fffffffu;          // ascending ids: the first maximum stays
     for (int e = lane; e < E; e += 32) {
