@@ -155,9 +155,12 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                   const __grid_constant__ CUtensorMap map_w2,
                   const __grid_constant__ CUtensorMap map_ws2, GemmLaunch a) {
     extern __shared__ uint8_t sab_dyn[];
-    // full: activations of a stage landed; adeq: its A stage written; empty:
-    // its MMAs done (activations and A stage both free again)
-    __shared__ __align__(8) uint64_t full[kSabStages], adeq[kSabStages], empty[kSabStages];
+    // full: a stage's activations landed (the producer's arrival with the
+    // transaction bytes) and its A stage written (128 dequantisation
+    // arrivals); empty: its MMAs done (activations and A stage both free
+    // again).  Every waiter of a barrier waits for each of its phases in
+    // turn: the parity waits below are only sound that way.
+    __shared__ __align__(8) uint64_t full[kSabStages], empty[kSabStages];
     __shared__ __align__(8) uint64_t wfull[kSabWStages], wempty[kSabWStages];
     __shared__ __align__(8) uint64_t sc_full[2], sc_empty[2], acc_full[2], acc_empty[2];
     __shared__ __align__(8) uint64_t mma_done;
@@ -173,8 +176,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
     pdl_launch();
     if (tid == 0) {
         for (int i = 0; i < kSabStages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&adeq[i], 128);
+            mbar_init(&full[i], 1 + 128);
             mbar_init(&empty[i], kSabMmaWarps);
         }
         for (int i = 0; i < kSabWStages; ++i) {
@@ -321,8 +323,6 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                     const uint32_t s = kst & (kSabStages - 1), round = kst / kSabStages;
                     if (!sab_wait(&full[s], round & 1, a.err))
                         latch_timeout(a.err, 34, s, round, tile);
-                    if (!sab_wait(&adeq[s], round & 1, a.err))
-                        latch_timeout(a.err, 35, s, round, tile);
                     tc_fence_after();
                     // the stage's first K step; step j is sub-block j / 4 of B,
                     // 32 (j % 4) bytes into its rows, and A columns 8 j on
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&adeq[s]);
+                mbar_arrive(&full[s]);
                 // each set has one of the weight stage's two pipeline stages
                 mbar_arrive(&wempty[cws]);
             }
