@@ -64,6 +64,82 @@ struct BucketOut {
     int32_t* plan;
 };
 
+// bucket_cta for at most 32 pairs: warp 0 holds pair p in lane p and ranks
+// it by (expert, p) with shuffles -- the same slots as the counting sort --
+// while the per-expert arrays wait for one barrier.  s_cnt zeroed, s_inv -1
+// on entry.
+template <typename Sync>
+__device__ void bucket_warp(const int* s_ids, int TK, int K, int E, int* s_cnt, int* s_off,
+                            SPlan& P, int* s_inv, const BucketOut& g, int tid, int nthr,
+                            Sync sync) {
+    const int lane = tid & 31;
+    if (tid < 32) {
+        const int p = lane;
+        const int e = p < TK ? s_ids[p] : -1;
+        const bool ok = e >= 0 && e < E;
+        const int key = ok ? e : 0x7fffffff;          // no slot: ranked after every valid pair
+        int rank = 0, before = 0, cnt = 0;
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int kj = __shfl_sync(0xffffffffu, key, j);
+            rank += (kj < key || (kj == key && j < p)) ? 1 : 0;
+            before += (kj == key && j < p) ? 1 : 0;
+            cnt += kj == key ? 1 : 0;
+        }
+        const bool first = ok && before == 0;        // its expert's first pair
+        const unsigned fm = __ballot_sync(0xffffffffu, first);
+        int uidx = 0;                                // touched experts below this one
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int kj = __shfl_sync(0xffffffffu, key, j);
+            uidx += (((fm >> j) & 1u) != 0u && kj < key) ? 1 : 0;
+        }
+        const int nvalid = __popc(__ballot_sync(0xffffffffu, ok));
+        if (ok) {
+            s_inv[p] = rank;
+            P.tok[rank] = p / K;
+            if (g.perm) g.perm[rank] = p;
+        }
+        if (first) {
+            P.e[uidx] = key;
+            P.off[uidx] = rank;
+            P.cnt[uidx] = cnt;
+            s_cnt[key] = cnt;
+        }
+        if (nvalid + lane < TK) P.tok[nvalid + lane] = -1;
+        if (lane == 0) {
+            P.n = __popc(fm);
+            s_off[E] = nvalid;
+        }
+    }
+    sync();
+    #pragma unroll 1
+    for (int e = tid; e < E; e += nthr) {
+        int off = 0;
+        #pragma unroll 1
+        for (int u = 0; u < P.n; ++u) off += P.e[u] < e ? P.cnt[u] : 0;
+        s_off[e] = off;
+        if (g.counts) g.counts[e] = s_cnt[e];
+        if (g.offsets) g.offsets[e] = off;
+    }
+    if (tid == 0 && g.offsets) g.offsets[E] = s_off[E];
+    if (g.inv)
+        #pragma unroll 1
+        for (int p = tid; p < TK; p += nthr) g.inv[p] = s_inv[p];
+    if (g.plan) {
+        if (tid == 0) g.plan[0] = P.n;
+        #pragma unroll 1
+        for (int i = tid; i < P.n; i += nthr) {
+            g.plan[kPlanHeader + i] = P.e[i];
+            g.plan[kPlanHeader + E + i] = P.off[i];
+            g.plan[kPlanHeader + 2 * E + i] = P.cnt[i];
+        }
+        #pragma unroll 1
+        for (int s = tid; s < TK; s += nthr) g.plan[kPlanHeader + 3 * E + s] = P.tok[s];
+    }
+    sync();
+}
+
 // Stable counting sort of the T*K (token, k) pairs by expert, by one CTA.
 // s_ids: the pairs' expert ids; an out-of-range id gets no slot (inv -1).
 // Fills P and s_inv in shared memory and, when given, the global copies:
@@ -80,6 +156,10 @@ __device__ void bucket_cta(const int* s_ids, int T, int K, int E, int* s_cnt, in
     #pragma unroll 1
     for (int p = tid; p < TK; p += nthr) s_inv[p] = -1;
     sync();
+    if (TK <= 32) {
+        bucket_warp(s_ids, TK, K, E, s_cnt, s_off, P, s_inv, g, tid, nthr, sync);
+        return;
+    }
     #pragma unroll 1
     for (int p = tid; p < TK; p += nthr) {
         const int e = s_ids[p];
@@ -205,16 +285,22 @@ __device__ inline void select_topk_warp(const float* lg, int E, int K, float* L,
 }
 
 // The selection itself on the order-preserving keys Lk[0..E) already in
-// this warp's shared scratch (lane-strided writes; consumed, i.e. picked
-// entries are zeroed).
-__device__ inline void select_topk_keys(int E, int K, uint32_t* Lk, float* ex, int* ids, float* w,
-                                        int lane) {
+// this warp's shared scratch (lane-strided writes).  Each lane copies its
+// keys (ids lane, lane + 32, ...) into registers, so after a pick only the
+// winning lane rescans, in registers.  KPL: keys a lane, >= E / 32.
+template <int KPL>
+__device__ inline void select_topk_reg(int E, int K, const uint32_t* Lk, float* ex, int* ids,
+                                       float* w, int lane) {
     __syncwarp();
+    uint32_t key[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) key[i] = lane + 32 * i < E ? Lk[lane + 32 * i] : 0u;
     uint32_t bk = 0u, be = 0x7fffffffu;          // ascending ids: the first maximum stays
-    for (int e = lane; e < E; e += 32) {
-        const uint32_t k = Lk[e];
-        if (be == 0x7fffffffu || k > bk) {
-            bk = k;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && (be == 0x7fffffffu || key[i] > bk)) {
+            bk = key[i];
             be = uint32_t(e);
         }
     }
@@ -227,13 +313,15 @@ __device__ inline void select_topk_keys(int E, int K, uint32_t* Lk, float* ex, i
             mye = emin;
         }
         if (emin < uint32_t(E) && int(emin & 31u) == lane) {
-            Lk[emin] = 0u;
+            // the pick is taken (key 0 never wins); rescan this lane's keys
             bk = 0u;
             be = 0x7fffffffu;
-            for (int e = lane; e < E; e += 32) {
-                const uint32_t kk = Lk[e];
-                if (be == 0x7fffffffu || kk > bk) {
-                    bk = kk;
+#pragma unroll
+            for (int i = 0; i < KPL; ++i) {
+                const int e = lane + 32 * i;
+                if (uint32_t(e) == emin) key[i] = 0u;
+                if (e < E && (be == 0x7fffffffu || key[i] > bk)) {
+                    bk = key[i];
                     be = uint32_t(e);
                 }
             }
@@ -256,6 +344,22 @@ __device__ inline void select_topk_keys(int E, int K, uint32_t* Lk, float* ex, i
     __syncwarp();
 }
 
+__device__ inline void select_topk_keys(int E, int K, uint32_t* Lk, float* ex, int* ids, float* w,
+                                        int lane) {
+    if (E <= 32)
+        select_topk_reg<1>(E, K, Lk, ex, ids, w, lane);
+    else if (E <= 64)
+        select_topk_reg<2>(E, K, Lk, ex, ids, w, lane);
+    else if (E <= 128)
+        select_topk_reg<4>(E, K, Lk, ex, ids, w, lane);
+    else if (E <= 256)
+        select_topk_reg<8>(E, K, Lk, ex, ids, w, lane);
+    else if (E <= 512)
+        select_topk_reg<16>(E, K, Lk, ex, ids, w, lane);
+    else
+        select_topk_reg<32>(E, K, Lk, ex, ids, w, lane);
+}
+
 // Routing of all T tokens by one CTA into shared memory: s_ids, s_w [T*K],
 // s_sig [T].  forced_ids / forced_w replace the selection when given.
 // scratch: (nthr / 32) * (E + 16) floats.
@@ -276,11 +380,14 @@ __device__ void route_cta(const float* logits, int T, int E, int K, const int32_
                 s_ids[t * K + k] = id;
                 s_w[t * K + k] = __ldg(forced_w + t * K + k);
             }
+            if (lane == 0) s_sig[t] = 1.0f / (1.0f + expf(-__ldcg(lg + E)));
         } else {
+            // the gate logit is requested with the others
+            const float gl = lane == 0 ? __ldcg(lg + E) : 0.0f;
             float* L = scratch + size_t(wid) * (E + 16);
             select_topk_warp(lg, E, K, L, L + E, s_ids + t * K, s_w + t * K, lane);
+            if (lane == 0) s_sig[t] = 1.0f / (1.0f + expf(-gl));
         }
-        if (lane == 0) s_sig[t] = 1.0f / (1.0f + expf(-__ldcg(lg + E)));
     }
     sync();
 }
