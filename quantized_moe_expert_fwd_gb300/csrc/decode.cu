@@ -361,10 +361,22 @@ __global__ void __launch_bounds__(kGuThreads, 1) k_gate_up(GuLaunch a) {
         __syncthreads();
     }
 
-    // this CTA's contiguous share of the touched experts' row pairs
-    const long long RP = (long long)P.n * I;
-    const long long beg = (long long)blockIdx.x * RP / gridDim.x;
-    const long long end = (long long)(blockIdx.x + 1) * RP / gridDim.x;
+    // this CTA's contiguous share of the touched experts' row pairs, cut by
+    // cost: a row pair of expert j costs its tokens plus one (the read of
+    // its rows), so CTAs on an expert with many tokens take fewer of its rows
+    auto rp_at = [&](long long x) {
+        long long cum = 0;
+        for (int j = 0; j < P.n; ++j) {
+            const long long w = (long long)P.cnt[j] + 1, cj = w * I;
+            if (x < cum + cj) return (long long)j * I + (x - cum) / w;
+            cum += cj;
+        }
+        return (long long)P.n * I;
+    };
+    long long cost = 0;
+    for (int j = 0; j < P.n; ++j) cost += ((long long)P.cnt[j] + 1) * I;
+    const long long beg = rp_at((long long)blockIdx.x * cost / gridDim.x);
+    const long long end = rp_at((long long)(blockIdx.x + 1) * cost / gridDim.x);
     const size_t qrow = size_t(H) >> 1, srow = size_t(H) >> 5;   // bytes, scales per row
     const size_t qexp = size_t(2) * I * qrow, sexp = size_t(2) * I * srow;
     const uint32_t stage_q = uint32_t(kGuRowPairs * 2 * qrow);
@@ -393,11 +405,28 @@ __global__ void __launch_bounds__(kGuThreads, 1) k_gate_up(GuLaunch a) {
         return;
     }
 
-    // consumers
+    // consumers: first (x_smem) every token's activations into shared memory
+    // after the ring, chunk-interleaved, while the producer's first copies fly
     const int cw = wid - 1;
     const int NC = H >> 5;
     uint64_t x2[MC][16];
     float X[MC];
+    uint4* xs = reinterpret_cast<uint4*>(g_ring + size_t(S) * stage_bytes);
+    if (a.x_smem) {
+        for (int i = tid - 32; i < T * 4 * NC; i += kGuConsumers * 32) {
+            const int t = i / (4 * NC), r = i - t * 4 * NC, c = r >> 2, v = r & 3;
+            xs[size_t(t) * 4 * NC + v * NC + c] =
+                ldg_keep(reinterpret_cast<const uint4*>(a.x + size_t(t) * H) + 4 * c + v);
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kGuConsumers * 32) : "memory");
+    }
+    // token t's activations into x2 / X
+    auto get_x = [&](int t) {
+        if (a.x_smem)
+            load_x_smem<MC>(xs + size_t(t) * 4 * NC, NC, lane, x2, X);
+        else
+            load_x<MC>(a.x + size_t(t) * H, NC, lane, x2, X);
+    };
     int xt = -1;              // token whose activations x2 holds
     int i = 0;
     for (long long rp = beg; rp < end; ++i) {
@@ -407,7 +436,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) k_gate_up(GuLaunch a) {
         const int s0 = P.off[j], scount = P.cnt[j];
         if (scount > 0 && P.tok[s0] != xt && P.tok[s0] >= 0 && P.tok[s0] < T) {
             xt = P.tok[s0];
-            load_x<MC>(a.x + size_t(xt) * H, NC, lane, x2, X);      // overlaps the copy
+            get_x(xt);                 // overlaps the copy
         }
         if (!mbar_wait(&full[slot], round & 1)) latch_timeout(a.err, 2, slot, round, i);
         const uint8_t* sq = g_ring + size_t(slot) * stage_bytes;
@@ -418,7 +447,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) k_gate_up(GuLaunch a) {
             if (t < 0 || t >= T) continue;
             if (t != xt) {
                 xt = t;
-                load_x<MC>(a.x + size_t(t) * H, NC, lane, x2, X);
+                get_x(t);
             }
 #pragma unroll
             for (int pp = 0; pp < kGuRowPairs / kGuConsumers; ++pp) {
@@ -689,18 +718,26 @@ cudaError_t launch_select(const SelectLaunch& a, cudaStream_t s) {
     return launch_pdl(k_select, 1, 256, dyn, s, a);
 }
 
-int gate_up_stages(int H) {
+// Ring stages of k_gate_up: as many as kGuRingBytes holds, fewer when the T
+// tokens' activations (T * H bf16 after the ring, x_smem) would not fit
+// beside them; with fewer than two stages left the activations stay in
+// global memory.
+int gate_up_stages(int H, int T, int* x_smem) {
     const size_t stage = size_t(kGuRowPairs) * 2 * (size_t(H) / 2 + size_t(H) / 16);
-    int S = int(kGuRingBytes / stage);
+    const size_t xbytes = size_t(T) * H * 2;
+    size_t room = kGuSmemBytes > xbytes ? kGuSmemBytes - xbytes : 0;
+    *x_smem = room >= 2 * stage ? 1 : 0;
+    if (!*x_smem || room > kGuRingBytes) room = kGuRingBytes;
+    const int S = int(room / stage);
     return S < kGuMaxStages ? S : kGuMaxStages;
 }
 
 cudaError_t launch_gate_up_decode(GuLaunch a, cudaStream_t s) {
     const Dev d = device_info();
     const int mc = (a.H + 1023) / 1024;
-    a.stages = gate_up_stages(a.H);
+    a.stages = gate_up_stages(a.H, a.T, &a.x_smem);
     const size_t stage = size_t(kGuRowPairs) * 2 * (size_t(a.H) / 2 + size_t(a.H) / 16);
-    size_t dyn = size_t(a.stages) * stage;
+    size_t dyn = size_t(a.stages) * stage + (a.x_smem ? size_t(a.T) * a.H * 2 : 0);
     const size_t sel = size_t(kGuConsumers + 1) * (a.E + 16) * sizeof(float);
     if (dyn < sel) dyn = sel;
     cudaError_t err;

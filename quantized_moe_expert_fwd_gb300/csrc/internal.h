@@ -18,6 +18,7 @@ constexpr int kDownRowsPerCta = 16;
 // shared-memory rings of the decode expert kernels
 constexpr int kGuMaxStages = 8;
 constexpr size_t kGuRingBytes = 147456;   // 4 stages of 16 gate/up row pairs at H = 2048
+constexpr size_t kGuSmemBytes = 196608;   // ring + the tokens' activations (dynamic part)
 constexpr int kDnMaxStages = 24;
 constexpr size_t kDnRingBytes = 114688;
 // plan: [0] touched experts, header pad, then e[E], off[E], cnt[E], tok[T*K]
@@ -94,7 +95,7 @@ struct GuLaunch {
     uint32_t* err;
     int T, H, I, E, K;
     int mode;
-    int stages;                       // set by the launcher
+    int stages, x_smem;               // set by the launcher
 };
 cudaError_t launch_gate_up_decode(GuLaunch a, cudaStream_t s);
 

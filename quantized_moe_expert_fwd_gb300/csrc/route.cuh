@@ -423,4 +423,34 @@ __device__ __forceinline__ void load_x(const uint16_t* xrow, int NC, int lane,
     }
 }
 
+// The same from shared memory: a token's row stored chunk-interleaved, the
+// 16-byte piece v of chunk c at piece index v * NC + c, so the 32 lanes of a
+// warp read 32 consecutive pieces.  Same values and sums as load_x.
+template <int MC>
+__device__ __forceinline__ void load_x_smem(const uint4* xs, int NC, int lane,
+                                            uint64_t (&x2)[MC][16], float (&X)[MC]) {
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+        const int c = lane + 32 * m;
+        float sum = 0.0f;
+        if (c < NC) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint4 u = xs[v * NC + c];
+                const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float lo = bf16_lo(wv[i]), hi = bf16_hi(wv[i]);
+                    x2[m][4 * v + i] = pk(lo, hi);
+                    sum += lo + hi;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x2[m][j] = 0ull;
+        }
+        X[m] = sum;
+    }
+}
+
 }  // namespace strata
