@@ -244,6 +244,90 @@ def build_decode(args, dev):
     return dims, T, planes, layers, xs, outs, cfg
 
 
+def _touched_per_layer(q, dims, layers, xs, outs, ws, stream, ids_buf, nl, v0=0):
+    n_act = []
+    for li in range(nl):
+        q.moe_layer_forward(dims, layers[li], xs[v0][li], outs[li], ws, ids=ids_buf,
+                            stream=stream)
+        stream.synchronize()
+        n_act.append(len(np.unique(ids_buf.cpu().numpy())))
+    return n_act
+
+
+def decode_stages(q, dims, layers, xs, outs, ws, stream, ids_buf, nl, T, dev):
+    """The three decode kernels, each timed alone over the layers: one graph
+    of reps x layers launches a stage, a workspace per layer so every call
+    sees its own layer's plan.  {name: (us a launch, weight bytes)}."""
+    import torch
+    wss = [q.make_workspace(dims, T, dev) for _ in range(nl)]
+    v0 = 0
+    with torch.cuda.stream(stream):
+        for li in range(nl):
+            q.moe_decode_route(dims, layers[li], xs[v0][li], wss[li], stream=stream)
+            q.moe_decode_gate_up(dims, layers[li], xs[v0][li], wss[li], stream=stream)
+            q.moe_decode_down_combine(dims, layers[li], T, outs[li], wss[li], stream=stream)
+        stream.synchronize()
+        n_act = _touched_per_layer(q, dims, layers, xs, outs, ws, stream, ids_buf, nl)
+        stages = {
+            "k_route": (lambda li: q.moe_decode_route(dims, layers[li], xs[v0][li], wss[li],
+                                                      stream=stream),
+                        lambda li: router_bytes(dims) + gu_bytes(dims, dims.shared_inter)),
+            "k_gate_up": (lambda li: q.moe_decode_gate_up(dims, layers[li], xs[v0][li], wss[li],
+                                                          stream=stream),
+                          lambda li: n_act[li] * gu_bytes(dims, dims.inter)),
+            "k_down": (lambda li: q.moe_decode_down_combine(dims, layers[li], T, outs[li],
+                                                            wss[li], stream=stream),
+                       lambda li: n_act[li] * dn_bytes(dims, dims.inter)
+                       + dn_bytes(dims, dims.shared_inter)),
+        }
+        # each stage captured as one graph of reps x 10 launches, so host-side
+        # call overhead does not leak into the per-launch time
+        per_stage = {}
+        reps = 50
+        for name, (fn, nbytes) in stages.items():
+            for li in range(nl):
+                fn(li)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for r in range(reps):
+                    for li in range(nl):
+                        fn(li)
+            g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(4):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (4 * reps * nl)
+            per_stage[name] = (us, sum(nbytes(li) for li in range(nl)) / nl)
+    return per_stage, {k: round(v[0], 3) for k, v in per_stage.items()}
+
+
+def tc_layer_stages(q, dims, layers, xs, outs, ws, stream, ids_buf, nl, reps=5):
+    """Per-kernel durations of the tcgen05 layer (moe_layer_profile, events
+    between the launches), averaged over the layers and reps; the weight-
+    streaming kernels carry their weight bytes.  {name: (us, bytes)}."""
+    n_act = _touched_per_layer(q, dims, layers, xs, outs, ws, stream, ids_buf, nl)
+    acc = {}
+    for _ in range(reps):
+        for li in range(nl):
+            prof = q.moe_layer_profile(dims, layers[li], xs[0][li], outs[li], ws, stream=stream)
+            for k, v in prof.items():
+                acc[k] = acc.get(k, 0.0) + v / (reps * nl)
+    mean_act = sum(n_act) / nl
+    weight_bytes = {
+        "router_gemm": router_bytes(dims),
+        "gemm_gate_up": mean_act * gu_bytes(dims, dims.inter) + gu_bytes(dims, dims.shared_inter),
+        "gemm_down": mean_act * dn_bytes(dims, dims.inter) + dn_bytes(dims, dims.shared_inter),
+    }
+    per_stage = {k: (acc[k], b) for k, b in weight_bytes.items() if k in acc}
+    return per_stage, {k: round(v, 3) for k, v in acc.items()}
+
+
 def run_strata(args, rank, world, local, ctl):
     import torch
     import quantized_moe_expert_fwd_gb300 as q
@@ -328,63 +412,17 @@ def run_strata(args, rank, world, local, ctl):
     layer_bytes = mean_touched * expert_bytes(dims) + shared_bytes(dims) + router_bytes(dims)
     gbs = layer_bytes * nl / (ms_step / 1e3) / 1e9
 
-    # dominant decode kernel, timed alone: each stage over the 10 layers, with
-    # a workspace per layer so every call sees its own layer's plan
-    wss = [q.make_workspace(dims, T, dev) for _ in range(nl)]
-    v0 = 0
-    with torch.cuda.stream(stream):
-        for li in range(nl):
-            q.moe_decode_route(dims, layers[li], xs[v0][li], wss[li], stream=stream)
-            q.moe_decode_gate_up(dims, layers[li], xs[v0][li], wss[li], stream=stream)
-            q.moe_decode_down_combine(dims, layers[li], T, outs[li], wss[li], stream=stream)
-        stream.synchronize()
-        # touched experts of variant 0 per layer (for per-stage bytes)
-        n_act = []
-        for li in range(nl):
-            q.moe_layer_forward(dims, layers[li], xs[v0][li], outs[li], ws, ids=ids_buf,
-                                stream=stream)
-            stream.synchronize()
-            n_act.append(len(np.unique(ids_buf.cpu().numpy())))
-        stages = {
-            "k_route": (lambda li: q.moe_decode_route(dims, layers[li], xs[v0][li], wss[li],
-                                                      stream=stream),
-                        lambda li: router_bytes(dims) + gu_bytes(dims, dims.shared_inter)),
-            "k_gate_up": (lambda li: q.moe_decode_gate_up(dims, layers[li], xs[v0][li], wss[li],
-                                                          stream=stream),
-                          lambda li: n_act[li] * gu_bytes(dims, dims.inter)),
-            "k_down": (lambda li: q.moe_decode_down_combine(dims, layers[li], T, outs[li],
-                                                            wss[li], stream=stream),
-                       lambda li: n_act[li] * dn_bytes(dims, dims.inter)
-                       + dn_bytes(dims, dims.shared_inter)),
-        }
-        # each stage captured as one graph of reps x 10 launches, so host-side
-        # call overhead does not leak into the per-launch time
-        per_stage = {}
-        reps = 50
-        for name, (fn, nbytes) in stages.items():
-            for li in range(nl):
-                fn(li)
-            stream.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for r in range(reps):
-                    for li in range(nl):
-                        fn(li)
-            g.replay()
-            stream.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(4):
-                g.replay()
-            e1.record(stream)
-            e1.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / (4 * reps * nl)
-            per_stage[name] = (us, sum(nbytes(li) for li in range(nl)) / nl)
+    tc_path = T > q.moe_layer_decode_max_tokens()
+    if tc_path:
+        per_stage, kernels_us = tc_layer_stages(q, dims, layers, xs, outs, ws, stream, ids_buf, nl)
+    else:
+        per_stage, kernels_us = decode_stages(q, dims, layers, xs, outs, ws, stream, ids_buf, nl,
+                                              T, dev)
     dom = max(per_stage, key=lambda k: per_stage[k][0])
     dom_us, dom_bytes = per_stage[dom]
     hbm_peak, _, peak_src = measured_peaks()
     achieved = dom_bytes / (dom_us / 1e6) / 1e9
+    launches_per_layer = 9 if tc_path else 3
 
     # end to end through the public API with host buffers
     e2e = None
@@ -453,9 +491,12 @@ def run_strata(args, rank, world, local, ctl):
             "algorithmic_bytes_per_launch": dom_bytes,
             "stages_us": {k: round(v[0], 3) for k, v in per_stage.items()},
         },
+        "kernels": ("tcgen05 grouped GEMMs (T above the whole-layer decode switch)"
+                    if tc_path else "decode kernels"),
+        "kernels_us": kernels_us,
         "clocks": clocks.summary(),
         "e2e": e2e,
-        "gpu_launches": args.steps * nl * 3,
+        "gpu_launches": args.steps * nl * launches_per_layer,
     }
     return result, (dims, planes, xs, nl)
 
@@ -655,7 +696,8 @@ def run_stack_line(args, rank, world, local, ctl):
     gbs = step_bytes / (ms / 1e3) / 1e9
     hbm, _, src = measured_peaks()
     # per step: the residual reset (a copy kernel) and each layer's kernels
-    launches = 1 + nl * (4 if T <= 32 else 11)
+    # (rmsnorm + 3 decode kernels, or rmsnorm + 9 tcgen05-path kernels)
+    launches = 1 + nl * (4 if T <= q.moe_layer_decode_max_tokens() else 10)
     return {
         "metric": METRIC,
         "value": T * world / (ms / 1e3),

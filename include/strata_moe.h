@@ -104,9 +104,20 @@ typedef struct {
  * layer of shape *dims; 0 when the shape is unsupported or max_tokens < 1. */
 STRATA_API size_t moe_workspace_bytes(const strata_moe_dims* dims, int32_t max_tokens);
 
-/* The T at and below which the calls take the decode (GEMV) kernels; above
- * it they take the tcgen05 grouped-GEMM (prefill) kernels. */
+/* The T at and below which the stage calls (moe_route ... moe_combine), the
+ * moe_decode_* calls and moe_layer_forward_static take the decode (GEMV)
+ * kernels; above it they take the tcgen05 grouped-GEMM (prefill) kernels. */
 STRATA_API int32_t moe_decode_max_tokens(void);
+
+/* The T at and below which the whole-layer calls (moe_layer_forward,
+ * moe_layer_forward_routed, moe_block_forward, moe_stack_forward) take the
+ * decode kernels; above it they take the tcgen05 kernels, unless the shape
+ * does not allow those (hidden % 256 != 0 or an intermediate size below 256),
+ * when the decode kernels serve up to moe_decode_max_tokens().  Measured on
+ * GB300 at the 2048-hidden, 256-expert, top-8 shape: the decode kernels' layer
+ * time grows by ~16 us a token from ~32 us at T = 1, the tcgen05 kernels' by
+ * ~2 us a token from ~45 us, about equal at T = 2. */
+STRATA_API int32_t moe_layer_decode_max_tokens(void);
 
 /* Input RMSNorm, unit weight:  x[t][h] = bf16( r[t][h] / sqrt(mean_h r^2 + eps) ).
  * Strata "Speed": "add+norm+q8_1 in one launch" is the norm in front of the
@@ -187,9 +198,9 @@ STRATA_API strata_status moe_combine(const strata_moe_dims* dims, const strata_m
                           size_t ws_bytes, void* stream);
 
 /* The whole layer: route, permute, experts, shared expert, combine.  For
- * T <= moe_decode_max_tokens() it runs three decode kernels (router + shared
- * gate/up in one; selection, bucketing and routed gate/up in one; every down
- * product + combine in one); above, the tcgen05 prefill kernels.
+ * T <= moe_layer_decode_max_tokens() it runs three decode kernels (router +
+ * shared gate/up in one; selection, bucketing and routed gate/up in one;
+ * every down product + combine in one); above, the tcgen05 prefill kernels.
  * ids_dev / weights_dev / shared_gate_dev receive the routing when non-NULL.
  * out_dev bf16 [T][H]. */
 STRATA_API strata_status moe_layer_forward(const strata_moe_dims* dims, const strata_moe_layer* layer,
@@ -270,7 +281,8 @@ STRATA_API strata_status moe_decode_down_combine(const strata_moe_dims* dims,
  * cudaMalloc.  The workspace is a fixed 2 MiB array inside the library: every
  * GPU that loads the library holds it until the process exits, and every call
  * of this function on a device uses the same array.
- *   - Limits: T <= moe_decode_max_tokens() and moe_workspace_bytes(dims, T)
+ *   - Runs the decode kernels at every T it takes.  Limits: T <=
+ *     moe_decode_max_tokens() and the decode kernels' part of the workspace
  *     <= 2 MiB (every decode T of the 2048-hidden, 256-expert, top-8 shape
  *     fits); a larger request returns STRATA_EINVAL with nothing launched.
  *   - The first call on each device looks up the array's device address
@@ -294,9 +306,10 @@ STRATA_API strata_status moe_layer_forward_static(const strata_moe_dims* dims,
  * every kernel launch, synchronises `stream`, and writes each kernel's
  * duration in microseconds to us[0..max_n) in launch order; *n_out gets the
  * number of kernels.  The events serialise the kernels, so each duration is
- * the kernel alone.  Order: decode (T <= moe_decode_max_tokens()): route,
- * gate/up, down+combine; prefill: router GEMM, top-K, count, scan, scatter,
- * gather, gate/up GEMM, down GEMM, combine. */
+ * the kernel alone.  Order: decode kernels (T <= moe_layer_decode_max_tokens(),
+ * three of them): route, gate/up, down+combine; tcgen05 kernels (nine):
+ * router GEMM, top-K, count, scan, scatter, gather, gate/up GEMM, down GEMM,
+ * combine. */
 STRATA_API strata_status moe_layer_profile(const strata_moe_dims* dims,
                                            const strata_moe_layer* layer, const void* x_dev,
                                            int32_t T, void* out_dev, void* ws_dev,

@@ -36,7 +36,9 @@ WsLayout ws_layout(const strata_moe_dims& d, int T) {
         L.plan = take((kPlanHeader + 3 * E + t * K) * 4);
         L.h = take(t * K * I * 4);
         L.hs = take(t * Is * 4);
-    } else {
+    }
+    L.decode_end = o;
+    if (T > kLayerDecodeMaxTokens) {
         const size_t nblk = (t + 31) / 32;
         const size_t max_mb = (t * K) / kBM + E + t / kBM + 2;
         L.cnt_blk = take(nblk * E * 4);
@@ -390,12 +392,14 @@ strata_status pf_down(const strata_moe_dims* d, const strata_moe_layer* L, int T
     return STRATA_OK;
 }
 
-// The layer at any T: decode kernels up to kDecodeMaxTokens, prefill above.
+// The layer at any T: decode kernels up to kLayerDecodeMaxTokens (or up to
+// kDecodeMaxTokens when the shape does not allow the tensor-core kernels),
+// the tensor-core (prefill) kernels above.
 strata_status any_layer(const strata_moe_dims* d, const strata_moe_layer* L, const void* x, int T,
                         const int32_t* forced_ids, const float* forced_w, int32_t* ids_user,
                         float* w_user, float* sig_user, void* out, float* resid, void* ws,
                         cudaStream_t s) {
-    if (T <= kDecodeMaxTokens)
+    if (T <= kLayerDecodeMaxTokens || (T <= kDecodeMaxTokens && !prefill_supported(*d)))
         return decode_layer(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, out,
                             resid, ws, s);
     return prefill_layer(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, out, resid,
@@ -415,6 +419,8 @@ size_t moe_workspace_bytes(const strata_moe_dims* dims, int32_t max_tokens) {
 }
 
 int32_t moe_decode_max_tokens(void) { return kDecodeMaxTokens; }
+
+int32_t moe_layer_decode_max_tokens(void) { return kLayerDecodeMaxTokens; }
 
 strata_status moe_rmsnorm(const float* r_dev, int32_t T, int32_t H, float eps, void* x_dev,
                           void* stream) {
@@ -896,7 +902,8 @@ extern "C" strata_status moe_layer_forward_static(const strata_moe_dims* dims,
     if (!al16(x_dev) || !opt4(ids_dev) || !opt4(weights_dev) || !opt4(shared_gate_dev) ||
         !al16(out_dev))
         return STRATA_EINVAL;
-    if (T > kDecodeMaxTokens || ws_layout(*dims, T).total > kStaticWsBytes) return STRATA_EINVAL;
+    if (T > kDecodeMaxTokens || ws_layout(*dims, T).decode_end > kStaticWsBytes)
+        return STRATA_EINVAL;
     void* ws = static_ws_address();
     if (ws == nullptr) return STRATA_ECUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

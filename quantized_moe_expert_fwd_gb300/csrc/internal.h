@@ -11,7 +11,12 @@
 
 namespace strata {
 
-constexpr int kDecodeMaxTokens = 32;
+constexpr int kDecodeMaxTokens = 32;       // the decode kernels take up to this many tokens
+// A whole layer (layer, block and stack calls) runs on the decode kernels up
+// to this many tokens and on the tensor-core kernels above, when the layer's
+// shape allows them: measured on GB300, the decode kernels' cost grows by
+// ~16 us a token, the tensor-core path's by ~2 us on a ~45 us base, equal at 2.
+constexpr int kLayerDecodeMaxTokens = 2;
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kDownRowsPerCta = 16;
@@ -40,13 +45,13 @@ struct MBlock {
 
 // Byte offsets of the workspace regions for a call with T tokens.  Every
 // region starts on a 256-byte boundary; the control block is at 0.  The
-// decode regions (plan, h, hs as fp32) exist for T <= kDecodeMaxTokens, the
-// prefill ones (per-block counts, row blocks, fp16 operands, bf16 outputs)
-// for larger T.
+// decode regions (plan, h, hs as fp32) exist for T <= kDecodeMaxTokens and
+// end at decode_end; the prefill ones (per-block counts, row blocks, fp16
+// operands, bf16 outputs) follow for T > kLayerDecodeMaxTokens.
 struct WsLayout {
     size_t ctl, logits, ids, w, sig, counts, offsets, perm, inv, plan, h, hs, x, out;
     size_t cnt_blk, base_blk, mblocks, n_mblocks, lgp, xg, h16, hs16, y, ysh;
-    size_t total;
+    size_t decode_end, total;
 };
 
 WsLayout ws_layout(const strata_moe_dims& d, int T);
@@ -182,6 +187,8 @@ struct PfExperts {
     int T, K, H, I, Is, E;
 };
 bool prefill_supported(const strata_moe_dims& d);
+// the expert GEMMs' shared memory (stages and a tile's scales) fits at this K
+bool prefill_gemm_fits(int K_max);
 cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s);
 cudaError_t launch_prefill_bucket(const PfBucket& b, cudaStream_t s);
 // block list of the routed slots from caller offsets (offsets NULL: none)

@@ -603,9 +603,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t sme
 }  // namespace
 
 bool prefill_supported(const strata_moe_dims& d) {
-    // tile and box rules: K multiples of 64 with >= 16 bytes of scales per
-    // row (K >= 256), N multiples of 128, and at most 1024 experts
-    return d.inter >= 256 && d.shared_inter >= 256 && d.hidden % 256 == 0;
+    // tile and box rules: K multiples of 256 (two pipeline stages a weight
+    // box, >= 16 bytes of scales per row), N multiples of 128, at most 1024
+    // experts, and the GEMMs' shared memory at the largest K
+    const int kmax = d.hidden > d.inter ? (d.hidden > d.shared_inter ? d.hidden : d.shared_inter)
+                                        : (d.inter > d.shared_inter ? d.inter : d.shared_inter);
+    return d.inter >= 256 && d.shared_inter >= 256 && d.hidden % 256 == 0 &&
+           d.inter % 256 == 0 && d.shared_inter % 256 == 0 && prefill_gemm_fits(kmax);
 }
 
 cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s) {

@@ -82,6 +82,13 @@ __host__ __device__ inline uint32_t sab_scale_bytes(int K_max) {
     return uint32_t(kBM) * uint32_t(K_max / 32) * 2u;
 }
 
+// Dynamic shared memory of the expert GEMM: activation stages, weight
+// stages, two scale buffers and the 1024-byte alignment slack.
+inline size_t sab_smem_bytes(int K_max) {
+    return size_t(kSabStages) * kSabStageBytes + size_t(kSabWStages) * kSabWBytes +
+           2 * size_t(sab_scale_bytes(K_max)) + 1024;
+}
+
 // 64 fp16 weights of one row for one K block: 32 packed bytes, two scales
 // -> 32 registers holding the MMA-order pairs, register c = K positions
 // (2c, 2c+1).  Within every 8 elements the positions hold elements
@@ -496,6 +503,8 @@ __global__ void __launch_bounds__(kSabThreads, 1)
 }
 
 // ------------------------------------------------------------------ host
+bool prefill_gemm_fits(int K_max) { return sab_smem_bytes(K_max) <= kPfSmemBudget; }
+
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 sab_encode_fn() {
@@ -569,8 +578,7 @@ cudaError_t run_sab(GemmLaunch g, const SabXMaps& mx, const SabXMaps& mx2,
                     const CUtensorMap& mw, const CUtensorMap& mws, const CUtensorMap& mw2,
                     const CUtensorMap& mws2, cudaStream_t s) {
     const Dev d = device_info();
-    const size_t dyn = size_t(kSabStages) * kSabStageBytes + size_t(kSabWStages) * kSabWBytes +
-                       2 * size_t(sab_scale_bytes(g.K_max)) + 1024;
+    const size_t dyn = sab_smem_bytes(g.K_max);
     if (dyn > kPfSmemBudget || g.K % 256 != 0 || g.K2 % 256 != 0) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_pf_gemm_sab<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn));

@@ -66,6 +66,7 @@ def load() -> ctypes.CDLL:
         sigs = {
             "moe_workspace_bytes": (SZ, [D, I32]),
             "moe_decode_max_tokens": (I32, []),
+            "moe_layer_decode_max_tokens": (I32, []),
             "moe_rmsnorm": (I32, [P, I32, I32, ctypes.c_float, P, P]),
             "moe_route": (I32, [D, L, P, I32, P, P, P, P, P, SZ, P]),
             "moe_permute": (I32, [D, P, I32, P, P, P, P, P, SZ, P]),
@@ -94,7 +95,8 @@ def load() -> ctypes.CDLL:
         return lib
 
 
-EXPORTED = ("moe_workspace_bytes", "moe_decode_max_tokens", "moe_rmsnorm", "moe_route",
+EXPORTED = ("moe_workspace_bytes", "moe_decode_max_tokens", "moe_layer_decode_max_tokens",
+            "moe_rmsnorm", "moe_route",
             "moe_permute", "moe_expert_gate_up", "moe_expert_down", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_routed",
             "moe_block_forward", "moe_stack_forward", "moe_decode_route", "moe_decode_gate_up",
@@ -173,6 +175,10 @@ def moe_workspace_bytes(dims, max_tokens: int) -> int:
 
 def moe_decode_max_tokens() -> int:
     return int(load().moe_decode_max_tokens())
+
+
+def moe_layer_decode_max_tokens() -> int:
+    return int(load().moe_layer_decode_max_tokens())
 
 
 def moe_rmsnorm(r, x, eps: float = 1e-6, stream=None):
@@ -310,7 +316,8 @@ def moe_layer_profile(dims, layer: DeviceLayer, x, out, ws, stream=None):
     _check("moe_layer_profile", load().moe_layer_profile(
         ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(x), x.shape[0], _ptr(out), _ptr(ws),
         ws.numel(), _stream(stream), us, 64, ctypes.byref(n)))
-    names = PROFILE_DECODE if x.shape[0] <= moe_decode_max_tokens() else PROFILE_PREFILL
+    # which kernels ran: the decode path launches three, the tensor-core path nine
+    names = PROFILE_DECODE if n.value == len(PROFILE_DECODE) else PROFILE_PREFILL
     return {names[i] if i < len(names) else f"k{i}": float(us[i]) for i in range(n.value)}
 
 

@@ -1,6 +1,11 @@
-"""Parity of the decode kernels (T <= 32) against the CPU oracle, through the
-C ABI.  Ids and permutations bit-exact (near ties excepted, see gpu_util);
-floats within rel-L2 5e-3 and max-abs 2e-2 * rms(ref)."""
+"""Parity of decode-size layers (T <= 32) against the CPU oracle, through the
+C ABI: the whole-layer calls (decode kernels up to
+moe_layer_decode_max_tokens(), tcgen05 kernels above when the shape allows)
+and the decode kernels themselves at every T through the stage calls.  Ids
+and permutations bit-exact (near ties excepted, see gpu_util); floats within
+rel-L2 5e-3 and max-abs 2e-2 * rms(ref)."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -291,27 +296,75 @@ def test_block_forward_stack(lib):
         G.assert_close(resid.cpu().numpy(), rref, "4-block stack, own routing")
 
 
-def test_stage_calls_equal_layer_forward(lib):
+def _static(lib, dims, dl, x, out, ids=None):
+    d = q.dims_struct(dims)
+    return lib.moe_layer_forward_static(ctypes.byref(d), ctypes.byref(dl.ptrs),
+                                        ctypes.c_void_p(x.data_ptr()), x.shape[0],
+                                        None if ids is None else ctypes.c_void_p(ids.data_ptr()),
+                                        None, None, ctypes.c_void_p(out.data_ptr()), None)
+
+
+def _stage_calls(dims, dl, x, ws, forced=None, ids=None):
+    T = x.shape[0]
+    out = torch.full((T, dims.hidden), -1, dtype=torch.int16, device=G.dev())
+    if forced is None:
+        q.moe_decode_route(dims, dl, x, ws)
+        q.moe_decode_gate_up(dims, dl, x, ws, ids=ids)
+    else:
+        q.moe_decode_route(dims, dl, x, ws, forced=True)
+        q.moe_decode_gate_up(dims, dl, x, ws, forced_ids=G.i32(forced[0]),
+                             forced_weights=G.f32(forced[1]), ids=ids)
+    q.moe_decode_down_combine(dims, dl, T, out, ws)
+    return out
+
+
+def test_stage_calls_equal_static_layer(lib):
     """moe_decode_route -> moe_decode_gate_up -> moe_decode_down_combine is
-    moe_layer_forward, bit for bit, and publishes the same routing."""
+    the decode-kernel layer (moe_layer_forward_static), bit for bit, and
+    publishes the same routing; at T = 1 moe_layer_forward is that layer
+    too."""
     dims = gen.QWEN
     planes, dl = layer(dims, 8)
     for T in (1, 9):
         xb = qwen_x(T, 80 + T)
         x = G.u16(xb)
-        ws = q.make_workspace(dims, T, G.dev())
         out_a = torch.empty((T, dims.hidden), dtype=torch.int16, device=G.dev())
         ids_a = torch.empty((T, dims.top_k), dtype=torch.int32, device=G.dev())
-        q.moe_layer_forward(dims, dl, x, out_a, ws, ids=ids_a)
-        out_b = torch.empty_like(out_a)
+        assert _static(lib, dims, dl, x, out_a, ids_a) == q.STRATA_OK
         ids_b = torch.empty_like(ids_a)
         ws2 = q.make_workspace(dims, T, G.dev())
-        q.moe_decode_route(dims, dl, x, ws2)
-        q.moe_decode_gate_up(dims, dl, x, ws2, ids=ids_b)
-        q.moe_decode_down_combine(dims, dl, T, out_b, ws2)
+        out_b = _stage_calls(dims, dl, x, ws2, ids=ids_b)
         torch.cuda.synchronize()
         assert torch.equal(out_a, out_b) and torch.equal(ids_a, ids_b)
         assert q.moe_get_device_status(ws2) == q.STRATA_OK
+        if T <= q.moe_layer_decode_max_tokens():
+            out_c = torch.empty_like(out_a)
+            q.moe_layer_forward(dims, dl, x, out_c, ws2)
+            torch.cuda.synchronize()
+            assert torch.equal(out_a, out_c)
+
+
+@pytest.mark.parametrize("T", [3, 7, 16, 31, 32])
+def test_decode_kernels_ragged_T(lib, T):
+    """The decode kernels above the whole-layer switch (the stage calls run
+    them up to moe_decode_max_tokens()): ids on clear tokens, and the output
+    with the oracle's routing forced, against the oracle."""
+    dims = gen.QWEN
+    planes, dl = layer(dims, 11)
+    xb = qwen_x(T, 500 + T)
+    ref = oracle.moe_forward(dims, planes, xb)
+    ws = q.make_workspace(dims, T, G.dev())
+    ids = torch.empty((T, dims.top_k), dtype=torch.int32, device=G.dev())
+    _stage_calls(dims, dl, G.u16(xb), ws, ids=ids)
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+    got = ids.cpu().numpy()
+    for t in G.clear_tokens(ref["gap"]):
+        assert np.array_equal(got[t], ref["ids"][t]), t
+    out = _stage_calls(dims, dl, G.u16(xb), ws, forced=(ref["ids"], ref["w"]))
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+    G.assert_close(G.bf16_to_np(out), ref["out"], f"decode kernels T={T}")
 
 
 def _oracle_stack_forced(dims, planes, r0):
