@@ -422,7 +422,7 @@ def run_strata(args, rank, world, local, ctl):
     dom_us, dom_bytes = per_stage[dom]
     hbm_peak, _, peak_src = measured_peaks()
     achieved = dom_bytes / (dom_us / 1e6) / 1e9
-    launches_per_layer = 9 if tc_path else 3
+    launches_per_layer = (7 if T <= 32 else 9) if tc_path else 3
 
     # end to end through the public API with host buffers
     e2e = None
@@ -696,8 +696,8 @@ def run_stack_line(args, rank, world, local, ctl):
     gbs = step_bytes / (ms / 1e3) / 1e9
     hbm, _, src = measured_peaks()
     # per step: the residual reset (a copy kernel) and each layer's kernels
-    # (rmsnorm + 3 decode kernels, or rmsnorm + 9 tcgen05-path kernels)
-    launches = 1 + nl * (4 if T <= q.moe_layer_decode_max_tokens() else 10)
+    # (rmsnorm + 3 decode kernels, or rmsnorm + 7 / 9 tcgen05-path kernels)
+    launches = 1 + nl * (4 if T <= q.moe_layer_decode_max_tokens() else (8 if T <= 32 else 10))
     return {
         "metric": METRIC,
         "value": T * world / (ms / 1e3),

@@ -309,7 +309,8 @@ STRATA_API strata_status moe_layer_forward_static(const strata_moe_dims* dims,
  * the kernel alone.  Order: decode kernels (T <= moe_layer_decode_max_tokens(),
  * three of them): route, gate/up, down+combine; tcgen05 kernels (nine):
  * router GEMM, top-K, count, scan, scatter, gather, gate/up GEMM, down GEMM,
- * combine. */
+ * combine -- seven at T <= 32, where count, scan and scatter are one
+ * bucketing kernel. */
 STRATA_API strata_status moe_layer_profile(const strata_moe_dims* dims,
                                            const strata_moe_layer* layer, const void* x_dev,
                                            int32_t T, void* out_dev, void* ws_dev,

@@ -129,8 +129,8 @@ cudaError_t launch_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x,
 
 // ---------------------------------------------------------------- prefill
 struct PfSelectLaunch {
-    const float* part; int nsplit;    // router GEMM K slices [nsplit][T][E + 1]
-    const float* bias; float* logits_user;
+    const float* part; int nsplit;    // router GEMM K slices [nsplit][T][E + 1], bias in slice 0
+    float* logits_user;
     const int32_t* forced_ids; const float* forced_w;
     int32_t* ids; float* w; float* sig;
     int32_t* ids_user; float* w_user; float* sig_user;

@@ -44,10 +44,71 @@
 namespace strata {
 
 // ------------------------------------------------------------- selection
+// Token t's logits e = lane + 32 i (i < NR; e = E is the gate) into the
+// warp's keys Lk and *gate: every K slice requested at once (one round trip),
+// the slices added in slice order (slice 0 holds the bias).  NR = 0: E too large for
+// registers, four logits a round.
+template <int NR>
+__device__ __forceinline__ void pf_logits(const PfSelectLaunch& a, int t, int lane, uint32_t* Lk,
+                                          float* gate) {
+    const int E = a.E, S = a.nsplit;
+    const size_t ld = size_t(E) + 1, sstride = size_t(a.T) * ld;
+    const float* p = a.part + size_t(t) * ld;
+    if constexpr (NR > 0) {
+        float u[kRouterSplitMax][NR];
+#pragma unroll
+        for (int sl = 0; sl < kRouterSplitMax; ++sl)
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                const int e = lane + 32 * i;
+                u[sl][i] = (sl < S && e <= E) ? __ldcg(p + sl * sstride + e) : 0.0f;
+            }
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            const int e = lane + 32 * i;
+            float v = 0.0f;
+#pragma unroll
+            for (int sl = 0; sl < kRouterSplitMax; ++sl) v += u[sl][i];
+            if (e < E) {
+                Lk[e] = logit_key(v);
+                if (a.logits_user) a.logits_user[size_t(t) * E + e] = v;
+            } else if (e == E) {
+                *gate = v;
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int e0 = lane; e0 <= E; e0 += 4 * 32) {
+            float u[kRouterSplitMax][4];
+#pragma unroll
+            for (int sl = 0; sl < kRouterSplitMax; ++sl)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    u[sl][j] = (sl < S && e0 + 32 * j <= E)
+                                   ? __ldcg(p + sl * sstride + e0 + 32 * j)
+                                   : 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = e0 + 32 * j;
+                float v = 0.0f;
+#pragma unroll
+                for (int sl = 0; sl < kRouterSplitMax; ++sl) v += u[sl][j];
+                if (e < E) {
+                    Lk[e] = logit_key(v);
+                    if (a.logits_user) a.logits_user[size_t(t) * E + e] = v;
+                } else if (e == E) {
+                    *gate = v;
+                }
+            }
+        }
+    }
+}
+
 // One warp a token: the logits are the router GEMM's K slices added in slice
-// order plus the bias; then top-K (ties to the lower id), ids ascending,
+// order (the bias is in slice 0); then top-K (ties to the lower id), ids ascending,
 // renormalised softmax weights and the sigmoid of the shared-gate logit, by
 // the decode path's selection; or the forced ids/weights.
+template <int NR>
 __global__ void __launch_bounds__(256) k_pf_select(PfSelectLaunch a) {
     extern __shared__ float s_dyn[];
     pdl_launch();
@@ -55,42 +116,13 @@ __global__ void __launch_bounds__(256) k_pf_select(PfSelectLaunch a) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int t = blockIdx.x * (blockDim.x >> 5) + wid;
     if (t >= a.T) return;
-    const int E = a.E, K = a.K, S = a.nsplit;
-    const size_t ld = size_t(E) + 1, sstride = size_t(a.T) * ld;
-    const float* p = a.part + size_t(t) * ld;
+    const int E = a.E, K = a.K;
     float* L = s_dyn + size_t(wid) * (E + 16);
     uint32_t* Lk = reinterpret_cast<uint32_t*>(L);
     __shared__ int s_ids[8][kMaxTopK];
     __shared__ float s_w[8][kMaxTopK];
     __shared__ float s_gate[8];
-    // logits e = lane, lane + 32, ... and the gate (e = E): four of them,
-    // times the slices, loads in flight at once
-#pragma unroll 1
-    for (int e0 = lane; e0 <= E; e0 += 4 * 32) {
-        float u[kRouterSplitMax][4];
-#pragma unroll
-        for (int sl = 0; sl < kRouterSplitMax; ++sl)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                u[sl][j] = (sl < S && e0 + 32 * j <= E) ? __ldcg(p + sl * sstride + e0 + 32 * j)
-                                                        : 0.0f;
-        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int sl = 0; sl < kRouterSplitMax; ++sl)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] += u[sl][j];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + 32 * j;
-            if (e < E) {
-                const float l = a.bias != nullptr ? v[j] + __ldg(a.bias + e) : v[j];
-                Lk[e] = logit_key(l);
-                if (a.logits_user) a.logits_user[size_t(t) * E + e] = l;
-            } else if (e == E) {
-                s_gate[wid] = v[j];
-            }
-        }
-    }
+    pf_logits<NR>(a, t, lane, Lk, &s_gate[wid]);
     __syncwarp();
     if (a.forced_ids) {
         for (int k = lane; k < K; k += 32) {
@@ -276,6 +308,75 @@ __global__ void __launch_bounds__(1024) k_pf_blocks(const int32_t* offsets, int 
     }
 }
 
+// The three bucketing kernels in one CTA when every pair fits one counting
+// block (T <= kPfTokBlock): histogram, offsets and block list, then each
+// pair's slot (the expert's offset + its rank among the expert's earlier
+// pairs) -- the same slots as k_pf_count / k_pf_scan / k_pf_scatter.
+__global__ void __launch_bounds__(1024) k_pf_bucket_small(PfScanLaunch a, const int32_t* ids,
+                                                          int K, int32_t* perm, int32_t* inv,
+                                                          uint32_t* err) {
+    __shared__ int s_ids[kPfTokBlock * kMaxTopK];
+    __shared__ int hist[kMaxExperts];
+    __shared__ int s_warp[33];
+    pdl_launch();
+    pdl_wait();
+    const int E = a.E, TK = a.T * K, tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
+    for (int i = tid; i < TK; i += blockDim.x) s_ids[i] = __ldcg(ids + i);
+    __syncthreads();
+    for (int i = tid; i < TK; i += blockDim.x) {
+        const int e = s_ids[i];
+        if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    const int e = tid;                    // E <= 1024: one expert a thread
+    const int total = e < E ? hist[e] : 0;
+    const int nmb = (total + kBM - 1) / kBM;
+    int sum_slots = 0, sum_mb = 0;
+    const int off = block_exclusive_scan(total, s_warp, &sum_slots);
+    const int mbo = block_exclusive_scan(nmb, s_warp, &sum_mb);
+    if (e < E) {
+        a.counts[e] = total;
+        a.offsets[e] = off;
+        hist[e] = off;                    // from here: the expert's first slot
+        for (int j = 0; j < nmb; ++j) {
+            MBlock mb;
+            mb.group = e;
+            mb.row = off + j * kBM;
+            mb.nrows = min(kBM, total - j * kBM);
+            mb.pad = 0;
+            a.mblocks[mbo + j] = mb;
+        }
+    }
+    if (tid == 0) {
+        a.offsets[E] = sum_slots;
+        const int nsh = a.with_shared ? (a.T + kBM - 1) / kBM : 0;
+        for (int j = 0; j < nsh; ++j) {
+            MBlock mb;
+            mb.group = E;
+            mb.row = j * kBM;
+            mb.nrows = min(kBM, a.T - j * kBM);
+            mb.pad = 0;
+            a.mblocks[sum_mb + j] = mb;
+        }
+        a.n_mblocks[0] = sum_mb + nsh;
+    }
+    __syncthreads();
+    for (int i = tid; i < TK; i += blockDim.x) {
+        const int ei = s_ids[i];
+        if (ei < 0 || ei >= E) {
+            latch(err, STRATA_EBADROUTE);
+            inv[i] = -1;
+            continue;
+        }
+        int rank = 0;
+        for (int j = 0; j < i; ++j) rank += (s_ids[j] == ei) ? 1 : 0;
+        const int slot = hist[ei] + rank;
+        perm[slot] = i;
+        inv[i] = slot;
+    }
+}
+
 // Slots of the block's pairs: base of (block, expert) + rank among the
 // block's earlier pairs of the same expert (pairs in ascending t*K + k, so
 // an expert's slots ascend in t).
@@ -445,6 +546,7 @@ constexpr uint32_t kRtStageBytes = kRtABytes + kRtBN * 128u;
 
 struct RouterLaunch {
     float* part;               // [S][T][E + 1]
+    const float* bias;         // [E] or NULL: added into slice 0
     uint32_t* err;
     int T, E, S, kbt, n_ttiles;
 };
@@ -525,6 +627,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         const int r = mt * kBM + q * 32 + lane;
         const size_t ld = size_t(a.E) + 1;
         float* out = a.part + size_t(sl) * size_t(a.T) * ld + r;
+        // slice 0 carries the bias (read while the products run)
+        const float b = (sl == 0 && a.bias != nullptr && r < a.E) ? __ldg(a.bias + r) : 0.0f;
         if (!mbar_wait(&acc_full, 0)) latch_timeout(a.err, 52, 0, 0, item);
         tc_fence_after();
         const int t0 = nt * kRtBN;
@@ -536,7 +640,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int t = t0 + 32 * c + j;
-                    if (t < a.T) out[size_t(t) * ld] = __uint_as_float(v[j]);
+                    if (t < a.T) out[size_t(t) * ld] = __uint_as_float(v[j]) + b;
                 }
             }
         }
@@ -623,7 +727,7 @@ cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s) {
     int S = device_info().sms / (n_mt * n_tt);
     S = S < 1 ? 1 : (S > kRouterSplitMax ? kRouterSplitMax : S);
     S = S > kbt ? kbt : S;
-    RouterLaunch g{r.part, r.err, r.T, r.E, S, kbt, n_tt};
+    RouterLaunch g{r.part, r.bias, r.err, r.T, r.E, S, kbt, n_tt};
     const size_t dyn = size_t(kRtStages) * kRtStageBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(k_pf_router, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(dyn));
@@ -633,7 +737,6 @@ cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s) {
     PfSelectLaunch sl{};
     sl.part = r.part;
     sl.nsplit = S;
-    sl.bias = r.bias;
     sl.logits_user = r.logits_user;
     sl.forced_ids = r.forced_ids;
     sl.forced_w = r.forced_w;
@@ -648,13 +751,15 @@ cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s) {
     sl.E = r.E;
     sl.K = r.K;
     const size_t sdyn = size_t(8) * (r.E + 16) * sizeof(float);
-    return launch_pdl(k_pf_select, (r.T + 7) / 8, 256, sdyn, s, sl);
+    const int grid = (r.T + 7) / 8, nr = (r.E + 1 + 31) / 32;
+    if (nr <= 2) return launch_pdl(k_pf_select<2>, grid, 256, sdyn, s, sl);
+    if (nr <= 5) return launch_pdl(k_pf_select<5>, grid, 256, sdyn, s, sl);
+    if (nr <= 9) return launch_pdl(k_pf_select<9>, grid, 256, sdyn, s, sl);
+    return launch_pdl(k_pf_select<0>, grid, 256, sdyn, s, sl);
 }
 
 cudaError_t launch_prefill_bucket(const PfBucket& b, cudaStream_t s) {
     const int nblk = (b.T + kPfTokBlock - 1) / kPfTokBlock;
-    cudaError_t e = launch_pdl(k_pf_count, nblk, 256, 0, s, b.ids, b.T, b.K, b.E, b.cnt_blk);
-    if (e != cudaSuccess) return e;
     PfScanLaunch sc{};
     sc.cnt_blk = b.cnt_blk;
     sc.base_blk = b.base_blk;
@@ -666,6 +771,10 @@ cudaError_t launch_prefill_bucket(const PfBucket& b, cudaStream_t s) {
     sc.E = b.E;
     sc.T = b.T;
     sc.with_shared = b.with_shared;
+    if (nblk == 1)          // every pair in one counting block: one kernel
+        return launch_pdl(k_pf_bucket_small, 1, 1024, 0, s, sc, b.ids, b.K, b.perm, b.inv, b.err);
+    cudaError_t e = launch_pdl(k_pf_count, nblk, 256, 0, s, b.ids, b.T, b.K, b.E, b.cnt_blk);
+    if (e != cudaSuccess) return e;
     e = launch_pdl(k_pf_scan, 1, 1024, 0, s, sc);
     if (e != cudaSuccess) return e;
     return launch_pdl(k_pf_scatter, nblk, 256, 0, s, b.ids, b.T, b.K, b.E,

@@ -306,6 +306,9 @@ def moe_layer_forward_static(dims, layer: DeviceLayer, x, out, ids=None, weights
 PROFILE_DECODE = ("k_route", "k_gate_up", "k_down")
 PROFILE_PREFILL = ("router_gemm", "select", "count", "scan", "scatter", "gather",
                    "gemm_gate_up", "gemm_down", "combine")
+# the tcgen05 path at T <= 32: the bucketing is one kernel
+PROFILE_PREFILL_SMALL = ("router_gemm", "select", "bucket", "gather", "gemm_gate_up",
+                         "gemm_down", "combine")
 
 
 def moe_layer_profile(dims, layer: DeviceLayer, x, out, ws, stream=None):
@@ -316,8 +319,10 @@ def moe_layer_profile(dims, layer: DeviceLayer, x, out, ws, stream=None):
     _check("moe_layer_profile", load().moe_layer_profile(
         ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(x), x.shape[0], _ptr(out), _ptr(ws),
         ws.numel(), _stream(stream), us, 64, ctypes.byref(n)))
-    # which kernels ran: the decode path launches three, the tensor-core path nine
-    names = PROFILE_DECODE if n.value == len(PROFILE_DECODE) else PROFILE_PREFILL
+    # which kernels ran: the decode path launches three, the tensor-core path
+    # seven (T <= 32) or nine
+    names = {len(PROFILE_DECODE): PROFILE_DECODE,
+             len(PROFILE_PREFILL_SMALL): PROFILE_PREFILL_SMALL}.get(n.value, PROFILE_PREFILL)
     return {names[i] if i < len(names) else f"k{i}": float(us[i]) for i in range(n.value)}
 
 

@@ -428,3 +428,11 @@ def test_layer_profile_kernels(lib):
     prof = q.moe_layer_profile(dims, dl, G.u16(xb), out, ws)
     assert list(prof) == list(q.PROFILE_DECODE)
     assert all(v > 0 for v in prof.values())
+    # above the whole-layer switch: the tcgen05 kernels, bucketing fused at T <= 32
+    for T, names in ((16, q.PROFILE_PREFILL_SMALL), (64, q.PROFILE_PREFILL)):
+        xt = qwen_x(T, 4)
+        wst = q.make_workspace(dims, T, G.dev())
+        ot = torch.empty((T, dims.hidden), dtype=torch.int16, device=G.dev())
+        prof = q.moe_layer_profile(dims, dl, G.u16(xt), ot, wst)
+        assert list(prof) == list(names)
+        assert all(v > 0 for v in prof.values())
