@@ -611,7 +611,7 @@ def run_prefill_line(args, rank, world, local, ctl):
                    "l2": "inputs larger than L2: 455.8 MB of weights read per step",
                    "arithmetic": "int4 weights dequantised to fp16 x fp16 activations on "
                                  "tcgen05, fp32 accumulate"},
-        "roofline": {"kernel": "k_pf_gemm<gate/up>", "bound": "tensor",
+        "roofline": {"kernel": "k_pf_gemm_sab<gate/up>", "bound": "tensor",
                      "achieved": pf["gate_up_gemm"]["tflops"], "peak": peak,
                      "unit": "TFLOP/s", "frac": pf["gate_up_gemm"]["frac"],
                      "peak_source": f"{src} bf16 (fp16 runs at the same rate), burst",
