@@ -840,6 +840,24 @@ def main():
                 print(json.dumps(result), flush=True)
             return
         dims, planes, xs, nl = extra
+        if rank == 0 and world == 1 and not args.no_prefill:
+            # the prefill configuration beside the decode line: T=2048 through
+            # one layer, tensor-core rate of the gate/up GEMM
+            import torch
+            pf = run_prefill(torch.device(f"cuda:{local}"), reps=20, warmup=3)
+            result["prefill"] = {
+                "workload": pf["workload"], "tokens": pf["tokens"],
+                "tok_per_s": pf["tok_per_s"], "us_per_layer": pf["us_per_layer"],
+                "roofline": {"kernel": "k_pf_gemm_sab<gate/up>", "bound": "tensor",
+                             "achieved": pf["gate_up_gemm"]["tflops"],
+                             "peak": pf["peak_tflops"], "unit": "TFLOP/s",
+                             "frac": pf["gate_up_gemm"]["frac"],
+                             "peak_source": pf["peak_source"],
+                             "traffic": kernel_traffic("k_pf_gemm_gate_up"),
+                             "us_per_launch": pf["gate_up_gemm"]["us"]},
+                "tc_frac_whole_layer": pf["tc_frac_of_peak"],
+                "kernels_us": pf["kernels_us"],
+            }
         if rank == 0:
             if world == 1 and args.cpu_budget > 0:
                 result["cpu_baseline"] = cpu_baseline_block(dims, planes, xs, nl,
