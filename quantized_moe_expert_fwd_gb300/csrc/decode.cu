@@ -342,22 +342,11 @@ __global__ void __launch_bounds__(kGuThreads, 1) k_gate_up(GuLaunch a) {
         // routing: the same in every CTA; CTA 0 publishes it
         route_cta(a.logits, T, E, K, a.forced_ids, a.forced_w, s_ids, s_w, s_sig,
                   reinterpret_cast<float*>(g_ring), a.err, tid, int(blockDim.x), BlockSync{});
-        BucketOut g{nullptr, nullptr, nullptr, nullptr, nullptr};
-        if (blockIdx.x == 0) g = BucketOut{a.counts, a.offsets, a.perm, a.inv, a.plan_out};
-        bucket_cta(s_ids, T, K, E, s_cnt, s_off, s_wsum, P, s_inv, g, tid, int(blockDim.x),
+        // the plan only; CTA 0 publishes the routing and the bucketing after
+        // its share of the experts, off the path to the first weight copy
+        const BucketOut none{nullptr, nullptr, nullptr, nullptr, nullptr};
+        bucket_cta(s_ids, T, K, E, s_cnt, s_off, s_wsum, P, s_inv, none, tid, int(blockDim.x),
                    BlockSync{});
-        if (blockIdx.x == 0) {
-            for (int p = tid; p < T * K; p += blockDim.x) {
-                a.ids[p] = s_ids[p];
-                a.w[p] = s_w[p];
-                if (a.ids_user) a.ids_user[p] = s_ids[p];
-                if (a.w_user) a.w_user[p] = s_w[p];
-            }
-            for (int t = tid; t < T; t += blockDim.x) {
-                a.sig[t] = s_sig[t];
-                if (a.sig_user) a.sig_user[t] = s_sig[t];
-            }
-        }
         __syncthreads();
     }
 
@@ -476,6 +465,21 @@ __global__ void __launch_bounds__(kGuThreads, 1) k_gate_up(GuLaunch a) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
         rp += nb;
+    }
+    if (a.mode == kGuRoute && blockIdx.x == 0) {
+        const int ct = tid - 32, cn = kGuConsumers * 32;
+        publish_bucket(T * K, E, P, s_inv,
+                       BucketOut{a.counts, a.offsets, a.perm, a.inv, a.plan_out}, ct, cn);
+        for (int p = ct; p < T * K; p += cn) {
+            a.ids[p] = s_ids[p];
+            a.w[p] = s_w[p];
+            if (a.ids_user) a.ids_user[p] = s_ids[p];
+            if (a.w_user) a.w_user[p] = s_w[p];
+        }
+        for (int t = ct; t < T; t += cn) {
+            a.sig[t] = s_sig[t];
+            if (a.sig_user) a.sig_user[t] = s_sig[t];
+        }
     }
 }
 

@@ -64,14 +64,52 @@ struct BucketOut {
     int32_t* plan;
 };
 
+// The global copies of a bucketing from the plan P and s_inv (any number of
+// pairs; no barrier inside): counts[e], offsets[0..E], perm, inv and the
+// plan, as bucket_cta writes them.
+__device__ inline void publish_bucket(int TK, int E, const SPlan& P, const int* s_inv,
+                                      const BucketOut& g, int tid, int nthr) {
+    #pragma unroll 1
+    for (int e = tid; e < E; e += nthr) {
+        int off = 0, cnt = 0;
+        #pragma unroll 1
+        for (int u = 0; u < P.n; ++u) {
+            off += P.e[u] < e ? P.cnt[u] : 0;
+            cnt += P.e[u] == e ? P.cnt[u] : 0;
+        }
+        if (g.counts) g.counts[e] = cnt;
+        if (g.offsets) g.offsets[e] = off;
+    }
+    if (tid == 0 && g.offsets) {
+        int tot = 0;
+        for (int u = 0; u < P.n; ++u) tot += P.cnt[u];
+        g.offsets[E] = tot;
+    }
+    #pragma unroll 1
+    for (int p = tid; p < TK; p += nthr) {
+        const int sl = s_inv[p];
+        if (g.inv) g.inv[p] = sl;
+        if (g.perm && sl >= 0) g.perm[sl] = p;
+    }
+    if (g.plan) {
+        if (tid == 0) g.plan[0] = P.n;
+        #pragma unroll 1
+        for (int i = tid; i < P.n; i += nthr) {
+            g.plan[kPlanHeader + i] = P.e[i];
+            g.plan[kPlanHeader + E + i] = P.off[i];
+            g.plan[kPlanHeader + 2 * E + i] = P.cnt[i];
+        }
+        #pragma unroll 1
+        for (int sl = tid; sl < TK; sl += nthr) g.plan[kPlanHeader + 3 * E + sl] = P.tok[sl];
+    }
+}
+
 // bucket_cta for at most 32 pairs: warp 0 holds pair p in lane p and ranks
 // it by (expert, p) with shuffles -- the same slots as the counting sort --
-// while the per-expert arrays wait for one barrier.  s_cnt zeroed, s_inv -1
-// on entry.
+// then one barrier; the global copies (when asked for) follow from P.
 template <typename Sync>
-__device__ void bucket_warp(const int* s_ids, int TK, int K, int E, int* s_cnt, int* s_off,
-                            SPlan& P, int* s_inv, const BucketOut& g, int tid, int nthr,
-                            Sync sync) {
+__device__ void bucket_warp(const int* s_ids, int TK, int K, int E, SPlan& P, int* s_inv,
+                            const BucketOut& g, int tid, int nthr, Sync sync) {
     const int lane = tid & 31;
     if (tid < 32) {
         const int p = lane;
@@ -95,49 +133,21 @@ __device__ void bucket_warp(const int* s_ids, int TK, int K, int E, int* s_cnt, 
             uidx += (((fm >> j) & 1u) != 0u && kj < key) ? 1 : 0;
         }
         const int nvalid = __popc(__ballot_sync(0xffffffffu, ok));
-        if (ok) {
-            s_inv[p] = rank;
-            P.tok[rank] = p / K;
-            if (g.perm) g.perm[rank] = p;
-        }
+        if (p < TK) s_inv[p] = ok ? rank : -1;
+        if (ok) P.tok[rank] = p / K;
         if (first) {
             P.e[uidx] = key;
             P.off[uidx] = rank;
             P.cnt[uidx] = cnt;
-            s_cnt[key] = cnt;
         }
         if (nvalid + lane < TK) P.tok[nvalid + lane] = -1;
-        if (lane == 0) {
-            P.n = __popc(fm);
-            s_off[E] = nvalid;
-        }
+        if (lane == 0) P.n = __popc(fm);
     }
     sync();
-    #pragma unroll 1
-    for (int e = tid; e < E; e += nthr) {
-        int off = 0;
-        #pragma unroll 1
-        for (int u = 0; u < P.n; ++u) off += P.e[u] < e ? P.cnt[u] : 0;
-        s_off[e] = off;
-        if (g.counts) g.counts[e] = s_cnt[e];
-        if (g.offsets) g.offsets[e] = off;
+    if (g.counts || g.offsets || g.perm || g.inv || g.plan) {
+        publish_bucket(TK, E, P, s_inv, g, tid, nthr);
+        sync();
     }
-    if (tid == 0 && g.offsets) g.offsets[E] = s_off[E];
-    if (g.inv)
-        #pragma unroll 1
-        for (int p = tid; p < TK; p += nthr) g.inv[p] = s_inv[p];
-    if (g.plan) {
-        if (tid == 0) g.plan[0] = P.n;
-        #pragma unroll 1
-        for (int i = tid; i < P.n; i += nthr) {
-            g.plan[kPlanHeader + i] = P.e[i];
-            g.plan[kPlanHeader + E + i] = P.off[i];
-            g.plan[kPlanHeader + 2 * E + i] = P.cnt[i];
-        }
-        #pragma unroll 1
-        for (int s = tid; s < TK; s += nthr) g.plan[kPlanHeader + 3 * E + s] = P.tok[s];
-    }
-    sync();
 }
 
 // Stable counting sort of the T*K (token, k) pairs by expert, by one CTA.
@@ -151,15 +161,15 @@ __device__ void bucket_cta(const int* s_ids, int T, int K, int E, int* s_cnt, in
                            int nthr, Sync sync) {
     const int lane = tid & 31, wid = tid >> 5, wpb = nthr >> 5;
     const int TK = T * K;
+    if (TK <= 32) {
+        bucket_warp(s_ids, TK, K, E, P, s_inv, g, tid, nthr, sync);
+        return;
+    }
     #pragma unroll 1
     for (int e = tid; e < E; e += nthr) s_cnt[e] = 0;
     #pragma unroll 1
     for (int p = tid; p < TK; p += nthr) s_inv[p] = -1;
     sync();
-    if (TK <= 32) {
-        bucket_warp(s_ids, TK, K, E, s_cnt, s_off, P, s_inv, g, tid, nthr, sync);
-        return;
-    }
     #pragma unroll 1
     for (int p = tid; p < TK; p += nthr) {
         const int e = s_ids[p];
