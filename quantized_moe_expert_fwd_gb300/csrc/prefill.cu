@@ -199,11 +199,49 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
     return ex;
 }
 
+// The 128-row blocks of every group, largest first, so that the expert
+// GEMMs' persistent CTAs, which take the block list's tiles in rounds, end
+// their last rounds together: every full block (routed experts ascending,
+// then the shared expert), then the partial blocks by descending row count
+// (blocks of equal size in any order -- each block's products are its own,
+// so the order moves work between CTAs, never a result).  Every thread of
+// the CTA calls it; thread e < E brings expert e's slots [off, off + total),
+// the others total = 0.  s_bin: kBM + 1 ints.
+__device__ void emit_mblocks(int off, int total, int E, int T, bool with_shared, MBlock* out,
+                             int32_t* n_out, int* s_warp, int* s_bin) {
+    const int tid = threadIdx.x;
+    for (int i = tid; i <= kBM; i += blockDim.x) s_bin[i] = 0;
+    __syncthreads();
+    const int nfull = total / kBM, rem = total % kBM;
+    const int nsh = with_shared ? T : 0, shfull = nsh / kBM, shrem = nsh % kBM;
+    // bin kBM - r holds the partial blocks of r rows: ascending bins are
+    // descending sizes
+    const int rank = rem > 0 ? atomicAdd(&s_bin[kBM - rem], 1) : 0;
+    const int shrank = (tid == 0 && shrem > 0) ? atomicAdd(&s_bin[kBM - shrem], 1) : 0;
+    int sum_full = 0;
+    const int fo = block_exclusive_scan(nfull, s_warp, &sum_full);
+    const int bc = (tid >= 1 && tid < kBM) ? s_bin[tid] : 0;
+    int npart = 0;
+    const int bstart = block_exclusive_scan(bc, s_warp, &npart);
+    if (tid >= 1 && tid < kBM) s_bin[tid] = bstart;
+    __syncthreads();
+    const int part0 = sum_full + shfull;
+    for (int j = 0; j < nfull; ++j) out[fo + j] = MBlock{tid, off + j * kBM, kBM, 0};
+    if (rem > 0) out[part0 + s_bin[kBM - rem] + rank] = MBlock{tid, off + nfull * kBM, rem, 0};
+    if (tid == 0) {
+        for (int j = 0; j < shfull; ++j) out[sum_full + j] = MBlock{E, j * kBM, kBM, 0};
+        if (shrem > 0)
+            out[part0 + s_bin[kBM - shrem] + shrank] = MBlock{E, shfull * kBM, shrem, 0};
+        n_out[0] = part0 + npart;
+    }
+}
+
 // One CTA of 1024 threads: per-expert totals, offsets, the per-block bases
-// of the scatter, and the 128-row blocks of every group (routed experts in
-// ascending id, then the shared expert over all T tokens).
+// of the scatter, and the 128-row blocks of every group (the routed
+// experts' and the shared expert's over all T tokens), largest first.
 __global__ void __launch_bounds__(1024) k_pf_scan(PfScanLaunch a) {
     __shared__ int s_warp[33];
+    __shared__ int s_bin[kBM + 1];
     pdl_launch();
     pdl_wait();
     const int E = a.E, nb = a.nblk;
@@ -220,10 +258,8 @@ __global__ void __launch_bounds__(1024) k_pf_scan(PfScanLaunch a) {
             for (int j = 0; j < CH; ++j) total += c[j];
         }
     }
-    const int nmb = (total + kBM - 1) / kBM;
-    int sum_slots = 0, sum_mb = 0;
+    int sum_slots = 0;
     const int off = block_exclusive_scan(total, s_warp, &sum_slots);
-    const int mbo = block_exclusive_scan(nmb, s_warp, &sum_mb);
     if (e < E) {
         a.counts[e] = total;
         a.offsets[e] = off;
@@ -240,37 +276,21 @@ __global__ void __launch_bounds__(1024) k_pf_scan(PfScanLaunch a) {
                     run += c[j];
                 }
         }
-        for (int j = 0; j < nmb; ++j) {
-            MBlock mb;
-            mb.group = e;
-            mb.row = off + j * kBM;
-            mb.nrows = min(kBM, total - j * kBM);
-            mb.pad = 0;
-            a.mblocks[mbo + j] = mb;
-        }
     }
-    if (threadIdx.x == 0) {
-        a.offsets[E] = sum_slots;
-        const int nsh = a.with_shared ? (a.T + kBM - 1) / kBM : 0;
-        for (int j = 0; j < nsh; ++j) {
-            MBlock mb;
-            mb.group = E;
-            mb.row = j * kBM;
-            mb.nrows = min(kBM, a.T - j * kBM);
-            mb.pad = 0;
-            a.mblocks[sum_mb + j] = mb;
-        }
-        a.n_mblocks[0] = sum_mb + nsh;
-    }
+    if (threadIdx.x == 0) a.offsets[E] = sum_slots;
+    emit_mblocks(off, e < E ? total : 0, E, a.T, a.with_shared != 0, a.mblocks, a.n_mblocks, s_warp,
+                 s_bin);
 }
 
 // The 128-row blocks of the routed slots from caller-supplied offsets (one
 // thread an expert; an expert whose range leaves [0, T*K] is skipped and
-// latches STRATA_EBADROUTE) and, with_shared, of the shared expert's tokens.
+// latches STRATA_EBADROUTE) and, with_shared, of the shared expert's tokens;
+// largest first.
 __global__ void __launch_bounds__(1024) k_pf_blocks(const int32_t* offsets, int T, int K, int E,
                                                     int with_shared, MBlock* mblocks,
                                                     int32_t* n_mblocks, uint32_t* err) {
     __shared__ int s_warp[33];
+    __shared__ int s_bin[kBM + 1];
     pdl_launch();
     pdl_wait();
     const int e = threadIdx.x;
@@ -283,29 +303,7 @@ __global__ void __launch_bounds__(1024) k_pf_blocks(const int32_t* offsets, int 
             total = 0;
         }
     }
-    const int nmb = (total + kBM - 1) / kBM;
-    int sum_mb = 0;
-    const int mbo = block_exclusive_scan(nmb, s_warp, &sum_mb);
-    for (int j = 0; j < nmb; ++j) {
-        MBlock mb;
-        mb.group = e;
-        mb.row = off + j * kBM;
-        mb.nrows = min(kBM, total - j * kBM);
-        mb.pad = 0;
-        mblocks[mbo + j] = mb;
-    }
-    if (threadIdx.x == 0) {
-        const int nsh = with_shared ? (T + kBM - 1) / kBM : 0;
-        for (int j = 0; j < nsh; ++j) {
-            MBlock mb;
-            mb.group = E;
-            mb.row = j * kBM;
-            mb.nrows = min(kBM, T - j * kBM);
-            mb.pad = 0;
-            mblocks[sum_mb + j] = mb;
-        }
-        n_mblocks[0] = sum_mb + nsh;
-    }
+    emit_mblocks(off, total, E, T, with_shared != 0, mblocks, n_mblocks, s_warp, s_bin);
 }
 
 // The three bucketing kernels in one CTA when every pair fits one counting
@@ -318,6 +316,7 @@ __global__ void __launch_bounds__(1024) k_pf_bucket_small(PfScanLaunch a, const 
     __shared__ int s_ids[kPfTokBlock * kMaxTopK];
     __shared__ int hist[kMaxExperts];
     __shared__ int s_warp[33];
+    __shared__ int s_bin[kBM + 1];
     pdl_launch();
     pdl_wait();
     const int E = a.E, TK = a.T * K, tid = threadIdx.x;
@@ -331,36 +330,15 @@ __global__ void __launch_bounds__(1024) k_pf_bucket_small(PfScanLaunch a, const 
     __syncthreads();
     const int e = tid;                    // E <= 1024: one expert a thread
     const int total = e < E ? hist[e] : 0;
-    const int nmb = (total + kBM - 1) / kBM;
-    int sum_slots = 0, sum_mb = 0;
+    int sum_slots = 0;
     const int off = block_exclusive_scan(total, s_warp, &sum_slots);
-    const int mbo = block_exclusive_scan(nmb, s_warp, &sum_mb);
     if (e < E) {
         a.counts[e] = total;
         a.offsets[e] = off;
         hist[e] = off;                    // from here: the expert's first slot
-        for (int j = 0; j < nmb; ++j) {
-            MBlock mb;
-            mb.group = e;
-            mb.row = off + j * kBM;
-            mb.nrows = min(kBM, total - j * kBM);
-            mb.pad = 0;
-            a.mblocks[mbo + j] = mb;
-        }
     }
-    if (tid == 0) {
-        a.offsets[E] = sum_slots;
-        const int nsh = a.with_shared ? (a.T + kBM - 1) / kBM : 0;
-        for (int j = 0; j < nsh; ++j) {
-            MBlock mb;
-            mb.group = E;
-            mb.row = j * kBM;
-            mb.nrows = min(kBM, a.T - j * kBM);
-            mb.pad = 0;
-            a.mblocks[sum_mb + j] = mb;
-        }
-        a.n_mblocks[0] = sum_mb + nsh;
-    }
+    if (tid == 0) a.offsets[E] = sum_slots;
+    emit_mblocks(off, total, E, a.T, a.with_shared != 0, a.mblocks, a.n_mblocks, s_warp, s_bin);
     __syncthreads();
     for (int i = tid; i < TK; i += blockDim.x) {
         const int ei = s_ids[i];

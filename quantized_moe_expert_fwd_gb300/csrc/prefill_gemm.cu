@@ -214,6 +214,14 @@ __global__ void __launch_bounds__(kSabThreads, 1)
     const int n_tiles = s_ntiles;
     const uint32_t tmem = tmem_base;
 
+    // The CTAs take the tiles in rounds of gridDim.x, alternate rounds in
+    // reverse CTA order: with the block list largest first, the CTAs that
+    // drew the larger tiles of one round draw the smaller ones of the next.
+    // A CTA's tile grows with its round, so the first past n_tiles ends it.
+    auto tile_at = [&](int r) {
+        const int G = int(gridDim.x), b = int(blockIdx.x);
+        return r * G + ((r & 1) ? G - 1 - b : b);
+    };
     // tile -> (token block, 128-row weight tile); false when the weight tile
     // does not exist for the block's group
     // Every role reads the next tile's block entry one tile ahead, so its L2
@@ -244,10 +252,10 @@ __global__ void __launch_bounds__(kSabThreads, 1)
             uint32_t kst = 0, ti = 0;               // pipeline stages and tiles so far
             uint32_t ws = 0, wph = 0;               // weight ring slot and phase
             uint32_t wcount = 0;                     // weight stages so far
-            MBlock mb_next = fetch(blockIdx.x);
-            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            MBlock mb_next = fetch(tile_at(0));
+            for (int r = 0, tile = tile_at(0); tile < n_tiles; tile = tile_at(++r)) {
                 const MBlock mb = mb_next;
-                mb_next = fetch(tile + int(gridDim.x));
+                mb_next = fetch(tile_at(r + 1));
                 int g, row, nrows, mt, W, K;
                 if (!tile_info(tile, mb, g, row, nrows, mt, W, K)) continue;
                 const bool sh = g == a.E;
@@ -308,10 +316,10 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         if (lane == 0) {
             const int mw = wid - 1;          // with two accumulators: K steps j % 2 == mw
             uint32_t kst = 0, ti = 0;
-            MBlock mb_next = fetch(blockIdx.x);
-            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            MBlock mb_next = fetch(tile_at(0));
+            for (int r = 0, tile = tile_at(0); tile < n_tiles; tile = tile_at(++r)) {
                 const MBlock mb = mb_next;
-                mb_next = fetch(tile + int(gridDim.x));
+                mb_next = fetch(tile_at(r + 1));
                 int g, row, nrows, mt, W, K;
                 if (!tile_info(tile, mb, g, row, nrows, mt, W, K)) continue;
                 const uint32_t dbuf = ti & 1u, dround = ti >> 1;
@@ -366,10 +374,10 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         const uint32_t set = uint32_t(wid - kSabDeq0) >> 2;   // this set's stages: kst % 2 == set
         uint32_t kst = 0, ti = 0;
         uint32_t ws = 0, wph = 0;
-        MBlock mb_next = fetch(blockIdx.x);
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        MBlock mb_next = fetch(tile_at(0));
+        for (int r = 0, tile = tile_at(0); tile < n_tiles; tile = tile_at(++r)) {
             const MBlock mb = mb_next;
-            mb_next = fetch(tile + int(gridDim.x));
+            mb_next = fetch(tile_at(r + 1));
             int g, row, nrows, mt, W, K;
             if (!tile_info(tile, mb, g, row, nrows, mt, W, K)) continue;
             const uint32_t buf = ti & 1u, sround = ti >> 1;
@@ -421,10 +429,10 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         const int q = wid & 3;
         const int m = q * 32 + lane;           // weight row of the tile
         uint32_t ti = 0;
-        MBlock mb_next = fetch(blockIdx.x);
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        MBlock mb_next = fetch(tile_at(0));
+        for (int r = 0, tile = tile_at(0); tile < n_tiles; tile = tile_at(++r)) {
             const MBlock mb = mb_next;
-            mb_next = fetch(tile + int(gridDim.x));
+            mb_next = fetch(tile_at(r + 1));
             int g, row, nrows, mt, W, K;
             if (!tile_info(tile, mb, g, row, nrows, mt, W, K)) continue;
             const bool sh = g == a.E;
