@@ -239,47 +239,68 @@ __device__ void emit_mblocks(int off, int total, int E, int T, bool with_shared,
 // One CTA of 1024 threads: per-expert totals, offsets, the per-block bases
 // of the scatter, and the 128-row blocks of every group (the routed
 // experts' and the shared expert's over all T tokens), largest first.
+// P threads an expert (P * E <= 1024) each take a contiguous range of the
+// counting blocks, so the counts come in one round of loads per pass instead
+// of nblk / P; thread e + E p holds part p of expert e (neighbouring threads
+// read neighbouring experts' counts).
 __global__ void __launch_bounds__(1024) k_pf_scan(PfScanLaunch a) {
     __shared__ int s_warp[33];
     __shared__ int s_bin[kBM + 1];
+    __shared__ int s_part[1024];
     pdl_launch();
     pdl_wait();
-    const int E = a.E, nb = a.nblk;
-    const int e = threadIdx.x;            // E <= 1024: one expert a thread
+    const int E = a.E, nb = a.nblk, tid = threadIdx.x;
+    const int P = max(1, min(int(blockDim.x) / E, nb));
+    const int e = tid % E, part = tid / E;
+    const bool act = part < P;
+    const int b_lo = act ? int((long long)part * nb / P) : 0;
+    const int b_hi = act ? int((long long)(part + 1) * nb / P) : 0;
     constexpr int CH = 16;                // counts loaded CH blocks at a time
-    int total = 0;
-    if (e < E) {
-        for (int b0 = 0; b0 < nb; b0 += CH) {
-            int c[CH];
+    int sum = 0;
+    for (int b0 = b_lo; b0 < b_hi; b0 += CH) {
+        int c[CH];
 #pragma unroll
-            for (int j = 0; j < CH; ++j)
-                c[j] = (b0 + j < nb) ? __ldcg(a.cnt_blk + size_t(b0 + j) * E + e) : 0;
+        for (int j = 0; j < CH; ++j)
+            c[j] = (b0 + j < b_hi) ? __ldcg(a.cnt_blk + size_t(b0 + j) * E + e) : 0;
 #pragma unroll
-            for (int j = 0; j < CH; ++j) total += c[j];
-        }
+        for (int j = 0; j < CH; ++j) sum += c[j];
     }
+    s_part[tid] = sum;
+    __syncthreads();
+    int pre = 0, total = 0;               // the parts before this one; all parts
+    if (act)
+        for (int p = 0; p < P; ++p) {
+            const int v = s_part[p * E + e];
+            pre += p < part ? v : 0;
+            total += v;
+        }
+    // thread e < E (part 0) brings expert e to the scans
+    const int tot_e = tid < E ? total : 0;
     int sum_slots = 0;
-    const int off = block_exclusive_scan(total, s_warp, &sum_slots);
-    if (e < E) {
-        a.counts[e] = total;
-        a.offsets[e] = off;
-        int run = off;
-        for (int b0 = 0; b0 < nb; b0 += CH) {
+    const int off = block_exclusive_scan(tot_e, s_warp, &sum_slots);
+    if (tid < E) {
+        a.counts[tid] = tot_e;
+        a.offsets[tid] = off;
+        s_part[tid] = off;                // every part reads it below
+    }
+    if (tid == 0) a.offsets[E] = sum_slots;
+    __syncthreads();
+    if (act) {
+        int run = s_part[e] + pre;
+        for (int b0 = b_lo; b0 < b_hi; b0 += CH) {
             int c[CH];
 #pragma unroll
             for (int j = 0; j < CH; ++j)
-                c[j] = (b0 + j < nb) ? __ldcg(a.cnt_blk + size_t(b0 + j) * E + e) : 0;
+                c[j] = (b0 + j < b_hi) ? __ldcg(a.cnt_blk + size_t(b0 + j) * E + e) : 0;
 #pragma unroll
             for (int j = 0; j < CH; ++j)
-                if (b0 + j < nb) {
+                if (b0 + j < b_hi) {
                     a.base_blk[size_t(b0 + j) * E + e] = run;
                     run += c[j];
                 }
         }
     }
-    if (threadIdx.x == 0) a.offsets[E] = sum_slots;
-    emit_mblocks(off, e < E ? total : 0, E, a.T, a.with_shared != 0, a.mblocks, a.n_mblocks, s_warp,
-                 s_bin);
+    emit_mblocks(off, tot_e, E, a.T, a.with_shared != 0, a.mblocks, a.n_mblocks, s_warp, s_bin);
 }
 
 // The 128-row blocks of the routed slots from caller-supplied offsets (one
@@ -385,14 +406,19 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int T, i
 
 // xg[row] = fp16(x[token(row)]) in the operand order; rows < T*K are the
 // routed slots (token perm[row] / K), the next T rows the tokens in order.
+// A thread takes four 8-element groups of one row, a quarter row apart (so
+// neighbouring threads stay on neighbouring groups): one slot lookup, then
+// four independent 16-byte loads in flight (H % 32 == 0).
+constexpr int kGatherPer = 4;
+
 __global__ void k_pf_gather(const uint16_t* x, const int32_t* perm, int T, int K, int H,
                             __half* xg, int nrows) {
     pdl_launch();
     pdl_wait();
-    const int groups = H >> 3;
+    const int gq = H / (8 * kGatherPer);               // groups in a quarter row
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (long long)nrows * groups) return;
-    const int row = int(i / groups), g = int(i % groups);
+    if (i >= (long long)nrows * gq) return;
+    const int row = int(i / gq), g0 = int(i % gq);
     int t;
     if (row < T * K) {
         const int p = __ldcg(perm + row);
@@ -400,27 +426,34 @@ __global__ void k_pf_gather(const uint16_t* x, const int32_t* perm, int T, int K
     } else {
         t = row - T * K;
     }
-    uint4 out = make_uint4(0u, 0u, 0u, 0u);
-    if (t >= 0) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + size_t(t) * H + 8 * g));
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-        float f[8];
+    uint4 v[kGatherPer];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f[2 * j] = bf16_lo(wv[j]);
-            f[2 * j + 1] = bf16_hi(wv[j]);
+    for (int q = 0; q < kGatherPer; ++q)
+        v[q] = t >= 0 ? __ldg(reinterpret_cast<const uint4*>(x + size_t(t) * H) + g0 + q * gq)
+                      : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int q = 0; q < kGatherPer; ++q) {
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+        if (t >= 0) {
+            const uint32_t wv[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[2 * j] = bf16_lo(wv[j]);
+                f[2 * j + 1] = bf16_hi(wv[j]);
+            }
+            // positions [0,4,1,5,2,6,3,7]
+            const __half2 h0 = __floats2half2_rn(f[0], f[4]);
+            const __half2 h1 = __floats2half2_rn(f[1], f[5]);
+            const __half2 h2 = __floats2half2_rn(f[2], f[6]);
+            const __half2 h3 = __floats2half2_rn(f[3], f[7]);
+            out = make_uint4(*reinterpret_cast<const uint32_t*>(&h0),
+                             *reinterpret_cast<const uint32_t*>(&h1),
+                             *reinterpret_cast<const uint32_t*>(&h2),
+                             *reinterpret_cast<const uint32_t*>(&h3));
         }
-        // positions [0,4,1,5,2,6,3,7]
-        const __half2 h0 = __floats2half2_rn(f[0], f[4]);
-        const __half2 h1 = __floats2half2_rn(f[1], f[5]);
-        const __half2 h2 = __floats2half2_rn(f[2], f[6]);
-        const __half2 h3 = __floats2half2_rn(f[3], f[7]);
-        out = make_uint4(*reinterpret_cast<const uint32_t*>(&h0),
-                         *reinterpret_cast<const uint32_t*>(&h1),
-                         *reinterpret_cast<const uint32_t*>(&h2),
-                         *reinterpret_cast<const uint32_t*>(&h3));
+        reinterpret_cast<uint4*>(xg + size_t(row) * H)[g0 + q * gq] = out;
     }
-    *reinterpret_cast<uint4*>(xg + size_t(row) * H + 8 * g) = out;
 }
 
 // fp32 -> fp16 in the operand order, 8 elements a thread.
@@ -768,7 +801,8 @@ cudaError_t launch_prefill_blocks(const int32_t* offsets, int T, int K, int E, i
 
 cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, int T, int K, int H,
                                   __half* xg, int rows, cudaStream_t s) {
-    const long long n = (long long)rows * (H / 8);
+    if (H % (8 * kGatherPer) != 0) return cudaErrorInvalidValue;
+    const long long n = (long long)rows * (H / (8 * kGatherPer));
     return launch_pdl(k_pf_gather, int((n + 255) / 256), 256, 0, s, x, perm, T, K, H, xg, rows);
 }
 
