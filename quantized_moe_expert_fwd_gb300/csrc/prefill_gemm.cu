@@ -11,11 +11,11 @@
 // instead of padding every expert to 128 rows.  The activations (B) come by
 // TMA into 128-byte-swizzled shared memory, one 3-D box a pipeline stage:
 // the block's rows rounded up to 32 (one tensor map per height) by the
-// stage's two 64-wide K blocks.
+// stage's four 64-wide K blocks.
 //
 // Warps: 0 TMA producer; 1 and 2 the MMAs (lane 0; warp 1 also allocates
-// the TMEM); 3..10 dequantisation, two sets of four taking alternate K
-// blocks (warp w owns TMEM lanes 32 (w % 4) .. +32: weight rows); 11..14
+// the TMEM); 3..10 dequantisation, two sets of four taking alternate
+// stages (warp w owns TMEM lanes 32 (w % 4) .. +32: weight rows); 11..14
 // epilogue (the same lane quarters): SwiGLU of gate/up row pairs (rows 2i,
 // 2i+1 sit in neighbouring lanes) or the down product's outputs.
 // One thread issues a tcgen05.mma about every 54 cycles however small N is,
@@ -23,10 +23,11 @@
 // a tile of at most 64 tokens therefore splits its K steps between the two
 // MMA warps, each into an accumulator of its own, which the epilogue adds.
 // Accumulators are double-buffered (2 x 128 columns) so a tile's epilogue
-// overlaps the next tile's MMAs; the dequantised A stages take 4 x 64
-// columns.  A pipeline stage is K = 128 (eight MMAs), so the per-stage
-// bookkeeping of the single-thread roles (waits, commits, TMA issue) is
-// spread over enough tensor work even for experts with few tokens.
+// overlaps the next tile's MMAs; the dequantised A stages take 2 x 128
+// columns.  A pipeline stage is K = 256 (sixteen MMAs): an MMA warp pays
+// about 220 cycles a stage for its fence and commit and 70-95 an MMA, so
+// fewer, longer stages leave more of its time to the MMAs (K = 128 stages:
+// gate/up 158 us, down 94 us at T = 2048; K = 256: 141 and 86).
 //
 // The pages found a fused dequantise + matrix-unit kernel losing to
 // dequantise-then-library-GEMM when the two did not overlap (Strata, "Strata
@@ -50,8 +51,8 @@ constexpr int kSabThreads = 480;
 constexpr int kSabMmaWarps = 2;          // MMA issuing warps (1, 2)
 constexpr int kSabDeq0 = 1 + kSabMmaWarps;   // first dequantisation warp
 constexpr int kSabDeqSets = 2;           // dequantisation warp sets: K blocks alternate
-constexpr int kSabKS = 128;              // K of one pipeline stage: 8 MMAs of K = 16
-constexpr int kSabStages = 4;            // activation stages = dequantised A stages
+constexpr int kSabKS = 256;              // K of one pipeline stage: 16 MMAs of K = 16
+constexpr int kSabStages = 2;            // activation stages = dequantised A stages
 constexpr int kSabACols = kSabKS / 2;    // TMEM columns of one A stage (two fp16 a column)
 constexpr int kSabDCols = 128;           // one accumulator buffer: up to 128 token columns
 constexpr int kSabACol0 = 2 * kSabDCols; // first A column
@@ -59,24 +60,26 @@ constexpr int kSabTmemCols = 512;
 constexpr int kSabBoxRows = 32;          // activation box heights: 32, 64, 96, 128 rows
 constexpr int kSabXMaps = kBM / kSabBoxRows;
 constexpr uint32_t kSabSubBytes = kBM * 128u;          // 128 rows x 64 fp16 (one MMA K block)
-constexpr uint32_t kSabStageBytes = 2 * kSabSubBytes;  // K = 128: two 64-wide sub-blocks
+constexpr uint32_t kSabStageBytes = (kSabKS / 64) * kSabSubBytes;  // 64-wide K sub-blocks
 
 // Activation maps of one operand, one per box height (rows 32 (i + 1)).
-// The box of map i lands as [2 K blocks][32 (i + 1) rows][64 fp16].
+// The box of map i lands as [4 K blocks][32 (i + 1) rows][64 fp16].
 struct SabXMaps {
     CUtensorMap m[kSabXMaps];
 };
-// Weight stages: 128 rows x 128 packed bytes = 256 inputs = 2 pipeline
-// stages, one TMA box with the 128-byte swizzle, so every row is read from
+// Weight stages: 128 rows x 128 packed bytes = 256 inputs = one pipeline
+// stage, one TMA box with the 128-byte swizzle, so every row is read from
 // memory as a whole 128-byte line and a lane's 16-byte reads of its row are
 // spread over the banks.
-constexpr uint32_t kSabWBytes = kBM * 128u;
+constexpr uint32_t kSabWRowBytes = 128;  // packed bytes of a row in a weight stage
+constexpr uint32_t kSabWBytes = kBM * kSabWRowBytes;
 constexpr int kSabWStages = 3;
 static_assert(kSabStages * kSabACols + kSabACol0 <= kSabTmemCols, "TMEM columns");
+static_assert(kSabKS / 2 == int(kSabWRowBytes), "one weight stage a pipeline stage");
 
 // A tile's scales land as [K / 256][128 rows][8 fp16]: the 8 scales of a
-// row for 256 inputs (two pipeline stages) side by side, so a stage's read
-// of 8 bytes per row by 32 consecutive rows spans only a few wavefronts
+// row for 256 inputs (one pipeline stage) side by side, so a stage's read
+// of 16 bytes per row by 32 consecutive rows spans only a few wavefronts
 // (row-major [128][K / 32] put all 32 rows of a warp in one bank).
 __host__ __device__ inline uint32_t sab_scale_bytes(int K_max) {
     return uint32_t(kBM) * uint32_t(K_max / 32) * 2u;
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         }
         for (int i = 0; i < kSabWStages; ++i) {
             mbar_init(&wfull[i], 1);
-            mbar_init(&wempty[i], 128 * kSabDeqSets);
+            mbar_init(&wempty[i], 128);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sc_full[i], 1);
@@ -270,12 +273,12 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                     latch_timeout(a.err, 31, buf, sround, tile);
                 mbar_expect_tx(&sc_full[buf], uint32_t(kBM) * uint32_t(K / 32) * 2u);
                 tma_load_3d(sc_base + buf * scb, mws, 0, wrow, 0, &sc_full[buf]);
-                const uint32_t xbytes = uint32_t(nbox) * (kSabBoxRows * 128u) * 2u;
+                const uint32_t xbytes = uint32_t(nbox) * (kSabBoxRows * 128u) * uint32_t(kSabKS / 64);
                 const int nks = K / kSabKS;
                 for (int ks = 0; ks < nks; ++ks, ++kst) {
-                    if ((ks & 1) == 0) {
-                        // one weight stage: the next two pipeline stages
-                        if (kst >= 2u * kSabWStages && !sab_wait(&wempty[ws], wph ^ 1u, a.err))
+                    {
+                        // one weight stage: this pipeline stage
+                        if (kst >= uint32_t(kSabWStages) && !sab_wait(&wempty[ws], wph ^ 1u, a.err))
                             latch_timeout(a.err, 30, ws, kst, tile);
                         mbar_expect_tx(&wfull[ws], kSabWBytes);
                         tma_load_2d(w_base + ws * kSabWBytes, mw, ks * (kSabKS / 2), wrow,
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                         latch_timeout(a.err, 32, s, round, tile);
                     uint8_t* st = base + s * kSabStageBytes;
                     mbar_expect_tx(&full[s], xbytes);
-                    tma_load_3d(st, mx, 0, xrow, 2 * ks, &full[s]);
+                    tma_load_3d(st, mx, 0, xrow, (kSabKS / 64) * ks, &full[s]);
                 }
                 ++ti;
             }
@@ -387,30 +390,28 @@ __global__ void __launch_bounds__(kSabThreads, 1)
             const int nks = K / kSabKS;
             for (int ks = 0; ks < nks; ++ks, ++kst) {
                 const uint32_t cws = ws, cwph = wph;
-                if (ks & 1) {
-                    if (++ws == uint32_t(kSabWStages)) {
-                        ws = 0;
-                        wph ^= 1u;
-                    }
+                if (++ws == uint32_t(kSabWStages)) {
+                    ws = 0;
+                    wph ^= 1u;
                 }
                 if ((kst & 1u) != set) continue;
                 const uint32_t s = kst & (kSabStages - 1), round = kst / kSabStages;
                 if (!sab_wait(&wfull[cws], cwph, a.err)) latch_timeout(a.err, 37, cws, kst, tile);
                 const uint32_t wrow_s = smem_u32(w_base + cws * kSabWBytes) + uint32_t(m * 128);
-                // the stage's 4 scales: group ks / 2, half ks % 2
-                const uint2 sc4 =
-                    lds_u2(scrow + uint32_t(ks >> 1) * (kBM * 16u) + uint32_t(ks & 1) * 8u);
+                // the stage's 8 scales (two a 64-wide sub-block)
+                const uint4 sc8 = lds128(scrow + uint32_t(ks) * (kBM * 16u));
+                const uint32_t scw[4] = {sc8.x, sc8.y, sc8.z, sc8.w};
                 if (round > 0 && !sab_wait(&empty[s], (round - 1) & 1, a.err))
                     latch_timeout(a.err, 38, s, round, tile);
                 tc_fence_after();
 #pragma unroll
-                for (int sb = 0; sb < 2; ++sb) {
+                for (int sb = 0; sb < kSabKS / 64; ++sb) {
                     // 32 bytes of row m: 16-byte chunks c, c + 1 of the swizzled row
-                    const int c = (ks & 1) * 4 + sb * 2;
+                    const int c = sb * 2;
                     const uint4 w0 = lds128(wrow_s + uint32_t(((c ^ (m & 7)) & 7) * 16));
                     const uint4 w1 = lds128(wrow_s + uint32_t((((c + 1) ^ (m & 7)) & 7) * 16));
                     uint32_t r[32];
-                    dequant_row_regs(w0, w1, sb ? sc4.y : sc4.x, r);
+                    dequant_row_regs(w0, w1, scw[sb], r);
                     tmem_st32(tmem + (uint32_t(q * 32) << 16) + uint32_t(kSabACol0) +
                                   s * kSabACols + uint32_t(32 * sb),
                               r);
@@ -418,7 +419,6 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&full[s]);
-                // each set has one of the weight stage's two pipeline stages
                 mbar_arrive(&wempty[cws]);
             }
             mbar_arrive(&sc_empty[buf]);
@@ -571,7 +571,8 @@ bool sab_xmaps(SabXMaps* m, const void* base, uint64_t K, uint64_t rows) {
     const cuuint64_t gstride[2] = {K * 2, uint64_t(kBK) * 2};
     const cuuint32_t estr[3] = {1, 1, 1};
     for (int i = 0; i < kSabXMaps; ++i) {
-        const cuuint32_t box[3] = {cuuint32_t(kBK), cuuint32_t(kSabBoxRows * (i + 1)), 2};
+        const cuuint32_t box[3] = {cuuint32_t(kBK), cuuint32_t(kSabBoxRows * (i + 1)),
+                                   cuuint32_t(kSabKS / kBK)};
         if (fn(&m->m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), gdim,
                gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -618,12 +619,12 @@ cudaError_t launch_prefill_gate_up(const PfExperts& p, cudaStream_t s) {
     if (!sab_xmaps(&mx, p.xg, H, p.xg_rows)) return cudaErrorInvalidValue;
     if (p.routed &&
         (!sab_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.gu_q, H / 2, uint64_t(E) * 2 * I,
-                  kSabKS, kBM, true) ||
+                  kSabWRowBytes, kBM, true) ||
          !sab_scale_map(&ms, p.gu_s, H, uint64_t(E) * 2 * I)))
         return cudaErrorInvalidValue;
     if (p.shared &&
         (!sab_map(&mq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_gu_q, H / 2, 2 * Is,
-                  kSabKS, kBM, true) ||
+                  kSabWRowBytes, kBM, true) ||
          !sab_scale_map(&ms2, p.sh_gu_s, H, 2 * Is)))
         return cudaErrorInvalidValue;
     if (!p.routed) {
@@ -662,13 +663,13 @@ cudaError_t launch_prefill_down(const PfExperts& p, cudaStream_t s) {
     if (p.routed &&
         (!sab_xmaps(&mx, p.h, I, uint64_t(T) * K) ||
          !sab_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.dn_q, I / 2, uint64_t(E) * H,
-                  kSabKS, kBM, true) ||
+                  kSabWRowBytes, kBM, true) ||
          !sab_scale_map(&ms, p.dn_s, I, uint64_t(E) * H)))
         return cudaErrorInvalidValue;
     if (p.shared &&
         (!sab_xmaps(&mx2, p.hs, Is, T) ||
          !sab_map(&mq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sh_dn_q, Is / 2, H,
-                  kSabKS, kBM, true) ||
+                  kSabWRowBytes, kBM, true) ||
          !sab_scale_map(&ms2, p.sh_dn_s, Is, H)))
         return cudaErrorInvalidValue;
     if (!p.routed) {
