@@ -204,12 +204,29 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
 // their last rounds together: every full block (routed experts ascending,
 // then the shared expert), then the partial blocks by descending row count
 // (blocks of equal size in any order -- each block's products are its own,
-// so the order moves work between CTAs, never a result).  Every thread of
-// the CTA calls it; thread e < E brings expert e's slots [off, off + total),
-// the others total = 0.  s_bin: kBM + 1 ints.
-__device__ void emit_mblocks(int off, int total, int E, int T, bool with_shared, MBlock* out,
-                             int32_t* n_out, int* s_warp, int* s_bin) {
+// so the order moves work between CTAs, never a result).  largest_first =
+// false keeps expert order (groups of a few tokens, where every block is
+// small and the sort's scans cost more than they balance).  Every thread of
+// the CTA calls it with the same largest_first; thread e < E brings expert
+// e's slots [off, off + total), the others total = 0.  s_bin: kBM + 1 ints.
+__device__ void emit_mblocks(int off, int total, int E, int T, bool with_shared,
+                             bool largest_first, MBlock* out, int32_t* n_out, int* s_warp,
+                             int* s_bin) {
     const int tid = threadIdx.x;
+    if (!largest_first) {
+        const int nmb = (total + kBM - 1) / kBM, nsh = with_shared ? T : 0;
+        int sum_mb = 0;
+        const int mbo = block_exclusive_scan(nmb, s_warp, &sum_mb);
+        for (int j = 0; j < nmb; ++j)
+            out[mbo + j] = MBlock{tid, off + j * kBM, min(kBM, total - j * kBM), 0};
+        if (tid == 0) {
+            const int nshb = (nsh + kBM - 1) / kBM;
+            for (int j = 0; j < nshb; ++j)
+                out[sum_mb + j] = MBlock{E, j * kBM, min(kBM, nsh - j * kBM), 0};
+            n_out[0] = sum_mb + nshb;
+        }
+        return;
+    }
     for (int i = tid; i <= kBM; i += blockDim.x) s_bin[i] = 0;
     __syncthreads();
     const int nfull = total / kBM, rem = total % kBM;
@@ -300,7 +317,8 @@ __global__ void __launch_bounds__(1024) k_pf_scan(PfScanLaunch a) {
                 }
         }
     }
-    emit_mblocks(off, tot_e, E, a.T, a.with_shared != 0, a.mblocks, a.n_mblocks, s_warp, s_bin);
+    emit_mblocks(off, tot_e, E, a.T, a.with_shared != 0, true, a.mblocks, a.n_mblocks, s_warp,
+                 s_bin);
 }
 
 // The 128-row blocks of the routed slots from caller-supplied offsets (one
@@ -324,7 +342,7 @@ __global__ void __launch_bounds__(1024) k_pf_blocks(const int32_t* offsets, int 
             total = 0;
         }
     }
-    emit_mblocks(off, total, E, T, with_shared != 0, mblocks, n_mblocks, s_warp, s_bin);
+    emit_mblocks(off, total, E, T, with_shared != 0, true, mblocks, n_mblocks, s_warp, s_bin);
 }
 
 // The three bucketing kernels in one CTA when every pair fits one counting
@@ -359,7 +377,8 @@ __global__ void __launch_bounds__(1024) k_pf_bucket_small(PfScanLaunch a, const 
         hist[e] = off;                    // from here: the expert's first slot
     }
     if (tid == 0) a.offsets[E] = sum_slots;
-    emit_mblocks(off, total, E, a.T, a.with_shared != 0, a.mblocks, a.n_mblocks, s_warp, s_bin);
+    emit_mblocks(off, total, E, a.T, a.with_shared != 0, false, a.mblocks, a.n_mblocks, s_warp,
+                 s_bin);
     __syncthreads();
     for (int i = tid; i < TK; i += blockDim.x) {
         const int ei = s_ids[i];
@@ -518,6 +537,70 @@ __global__ void k_pf_combine(const void* y, const __half* y_sh, const int32_t* i
             h8_to_f32(v, f);
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] += wk * f[j];
+    }
+    const float s = __ldcg(sig + t);
+    float f[8];
+    h8_to_f32(__ldcg(reinterpret_cast<const uint4*>(y_sh + size_t(t) * H + 8 * g)), f);
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float a0 = acc[2 * j] + s * f[2 * j];
+        const float a1 = acc[2 * j + 1] + s * f[2 * j + 1];
+        o[j] = uint32_t(f32_to_bf16(a0)) | (uint32_t(f32_to_bf16(a1)) << 16);
+    }
+    *reinterpret_cast<uint4*>(out + size_t(t) * H + 8 * g) = make_uint4(o[0], o[1], o[2], o[3]);
+    if (resid) {
+        float* rr = resid + size_t(t) * H + 8 * g;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            rr[2 * j] += bf16_lo(o[j]);
+            rr[2 * j + 1] += bf16_hi(o[j]);
+        }
+    }
+}
+
+// The same sums for few tokens, where the grid is too small to hide
+// latency: every pick's slot index and weight, then every pick's row, are
+// loaded before any sum (two round trips instead of 2 K).  At many tokens
+// the registers this takes cost more occupancy than the loads save.
+template <bool Y_BF16, int MAXK>
+__global__ void __launch_bounds__(256)
+    k_pf_combine_few(const void* y, const __half* y_sh, const int32_t* inv,
+                             const float* w, const float* sig, int T, int K, int H,
+                             uint16_t* out, float* resid) {
+    pdl_launch();
+    pdl_wait();
+    const int groups = H >> 3;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)T * groups) return;
+    const int t = int(i / groups), g = int(i % groups);
+    // every slot index and weight, then every slot's row, before any sum:
+    // the loads of the K picks are in flight together
+    int sl[MAXK];
+    float wk[MAXK];
+#pragma unroll
+    for (int k = 0; k < MAXK; ++k) {
+        sl[k] = k < K ? __ldcg(inv + size_t(t) * K + k) : -1;
+        wk[k] = k < K ? __ldcg(w + size_t(t) * K + k) : 0.0f;
+    }
+    uint4 v[MAXK];
+#pragma unroll
+    for (int k = 0; k < MAXK; ++k) {
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (sl[k] >= 0 && sl[k] < T * K)
+            v[k] = __ldcg(reinterpret_cast<const uint4*>(y) + (size_t(sl[k]) * H + 8 * g) / 8);
+    }
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int k = 0; k < MAXK; ++k) {
+        if (sl[k] < 0 || sl[k] >= T * K) continue;          // also k >= K
+        float f[8];
+        if (Y_BF16)
+            b8_to_f32(v[k], f);
+        else
+            h8_to_f32(v[k], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] += wk[k] * f[j];
     }
     const float s = __ldcg(sig + t);
     float f[8];
@@ -819,11 +902,23 @@ cudaError_t launch_prefill_experts(const PfExperts& p, cudaStream_t s) {
     return launch_prefill_down(p, s);
 }
 
+// Below this token count the combine loads every pick before summing.
+constexpr int kCombineFewTokens = 256;
+
 cudaError_t launch_prefill_combine(const __half* y_f16, const uint16_t* y_bf16, const __half* ysh,
                                    const int32_t* inv, const float* w, const float* sig, int T,
                                    int K, int H, uint16_t* out, float* resid, cudaStream_t s) {
     const long long n = (long long)T * (H / 8);
     const int grid = int((n + 255) / 256);
+    if (T <= kCombineFewTokens && K <= 8) {
+        const void* y = y_bf16 != nullptr ? static_cast<const void*>(y_bf16)
+                                          : static_cast<const void*>(y_f16);
+        if (y_bf16 != nullptr)
+            return launch_pdl(k_pf_combine_few<true, 8>, grid, 256, 0, s, y, ysh, inv, w, sig, T,
+                              K, H, out, resid);
+        return launch_pdl(k_pf_combine_few<false, 8>, grid, 256, 0, s, y, ysh, inv, w, sig, T, K,
+                          H, out, resid);
+    }
     if (y_bf16 != nullptr)
         return launch_pdl(k_pf_combine<true>, grid, 256, 0, s, static_cast<const void*>(y_bf16),
                           ysh, inv, w, sig, T, K, H, out, resid);
