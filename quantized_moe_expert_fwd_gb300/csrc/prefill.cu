@@ -633,10 +633,16 @@ __global__ void __launch_bounds__(256)
 // its partial products; the selection adds the slices in slice order, so the
 // result does not depend on scheduling.
 constexpr int kRtThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kRtBN = 256;               // tokens per tile
+// Tokens per tile: 256, or 64 for calls of at most 64 tokens (a smaller box
+// to fill and MMAs of N = 64 instead of N = 256 over mostly zero rows).
+constexpr int kRtBNMax = 256;
+constexpr int kRtBNSmall = 64;
 constexpr int kRtStages = 4;
 constexpr uint32_t kRtABytes = kBM * 128u;
-constexpr uint32_t kRtStageBytes = kRtABytes + kRtBN * 128u;
+template <int BN>
+__host__ __device__ constexpr uint32_t rt_stage_bytes() {
+    return kRtABytes + uint32_t(BN) * 128u;
+}
 
 struct RouterLaunch {
     float* part;               // [S][T][E + 1]
@@ -645,6 +651,7 @@ struct RouterLaunch {
     int T, E, S, kbt, n_ttiles;
 };
 
+template <int BN>
 __global__ void __launch_bounds__(kRtThreads, 1)
     k_pf_router(const __grid_constant__ CUtensorMap map_r, const __grid_constant__ CUtensorMap map_x,
                 RouterLaunch a) {
@@ -671,7 +678,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         tma_prefetch_map(&map_x);
     }
     if (wid == 1) {
-        tmem_alloc(&tmem_base, kRtBN);
+        tmem_alloc(&tmem_base, BN);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -686,10 +693,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                 const int s = kb % kRtStages, round = kb / kRtStages;
                 if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1))
                     latch_timeout(a.err, 50, s, round, item);
-                uint8_t* st = base + size_t(s) * kRtStageBytes;
-                mbar_expect_tx(&full[s], kRtStageBytes);
+                uint8_t* st = base + size_t(s) * rt_stage_bytes<BN>();
+                mbar_expect_tx(&full[s], rt_stage_bytes<BN>());
                 tma_load_2d(st, &map_r, (kb0 + kb) * kBK, mt * kBM, &full[s]);
-                tma_load_2d(st + kRtABytes, &map_x, (kb0 + kb) * kBK, nt * kRtBN, &full[s]);
+                tma_load_2d(st + kRtABytes, &map_x, (kb0 + kb) * kBK, nt * BN, &full[s]);
             }
             // every copy has landed before the CTA exits
             for (int i = 0; i < kRtStages && i < nkb; ++i) {
@@ -699,12 +706,12 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         }
     } else if (wid == 1) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16(kBM, kRtBN, 1);
+            const uint32_t idesc = idesc_f16(kBM, BN, 1);
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % kRtStages, round = kb / kRtStages;
                 if (!mbar_wait(&full[s], round & 1)) latch_timeout(a.err, 51, s, round, item);
                 tc_fence_after();
-                const uint32_t st = smem_u32(base + size_t(s) * kRtStageBytes);
+                const uint32_t st = smem_u32(base + size_t(s) * rt_stage_bytes<BN>());
                 const uint64_t ad = sdesc_k_sw128(st), bd = sdesc_k_sw128(st + kRtABytes);
 #pragma unroll
                 for (int j = 0; j < kBK / 16; ++j)      // + 32 bytes a K step
@@ -725,8 +732,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         const float b = (sl == 0 && a.bias != nullptr && r < a.E) ? __ldg(a.bias + r) : 0.0f;
         if (!mbar_wait(&acc_full, 0)) latch_timeout(a.err, 52, 0, 0, item);
         tc_fence_after();
-        const int t0 = nt * kRtBN;
-        for (int c = 0; c < kRtBN / 32 && t0 + 32 * c < a.T; ++c) {    // warp-uniform
+        const int t0 = nt * BN;
+        for (int c = 0; c < BN / 32 && t0 + 32 * c < a.T; ++c) {    // warp-uniform
             uint32_t v[32];
             tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(32 * c), v);
             tmem_ld_wait();
@@ -742,7 +749,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (wid == 1) tmem_dealloc(tmem, kRtBN);
+    if (wid == 1) tmem_dealloc(tmem, BN);
 }
 
 // ------------------------------------------------------------------ host
@@ -811,22 +818,30 @@ bool prefill_supported(const strata_moe_dims& d) {
 }
 
 cudaError_t launch_prefill_route(const PfRoute& r, cudaStream_t s) {
-    // logit slices: router rows in 128-row boxes, tokens in 256-row boxes
+    // logit slices: router rows in 128-row boxes, tokens in 256- or 64-row boxes
     CUtensorMap mr, mx;
     if (!make_map(&mr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, r.router, r.H, r.E + 1, kBK, kBM, true) ||
-        !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, r.x, r.H, r.T, kBK, kRtBN, true))
+        !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, r.x, r.H, r.T, kBK,
+                  r.T <= kRtBNSmall ? kRtBNSmall : kRtBNMax, true))
         return cudaErrorInvalidValue;
-    const int n_mt = (r.E + 1 + kBM - 1) / kBM, n_tt = (r.T + kRtBN - 1) / kRtBN, kbt = r.H / kBK;
+    const bool small = r.T <= kRtBNSmall;
+    const int BN = small ? kRtBNSmall : kRtBNMax;
+    const int n_mt = (r.E + 1 + kBM - 1) / kBM, n_tt = (r.T + BN - 1) / BN, kbt = r.H / kBK;
     // enough K slices to give every SM one tile
     int S = device_info().sms / (n_mt * n_tt);
     S = S < 1 ? 1 : (S > kRouterSplitMax ? kRouterSplitMax : S);
     S = S > kbt ? kbt : S;
     RouterLaunch g{r.part, r.bias, r.err, r.T, r.E, S, kbt, n_tt};
-    const size_t dyn = size_t(kRtStages) * kRtStageBytes + 1024;
-    cudaError_t e = cudaFuncSetAttribute(k_pf_router, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(dyn));
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(k_pf_router, n_mt * n_tt * S, kRtThreads, dyn, s, mr, mx, g);
+    const size_t dyn =
+        size_t(kRtStages) * (small ? rt_stage_bytes<kRtBNSmall>() : rt_stage_bytes<kRtBNMax>()) +
+        1024;
+    auto go = [&](auto kern) {
+        cudaError_t ee =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn));
+        return ee != cudaSuccess ? ee
+                                 : launch_pdl(kern, n_mt * n_tt * S, kRtThreads, dyn, s, mr, mx, g);
+    };
+    cudaError_t e = small ? go(k_pf_router<kRtBNSmall>) : go(k_pf_router<kRtBNMax>);
     if (e != cudaSuccess) return e;
     PfSelectLaunch sl{};
     sl.part = r.part;
