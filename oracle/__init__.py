@@ -155,6 +155,46 @@ def select(logits, K: int):
     return ids, w, gap
 
 
+def tail_skip(ids, w, n: int):
+    """Tail-skip of one call's routing (PolyStrata, "Models and backends",
+    section "What was tuned": an expert that every token of a call ranks at
+    place n + 1 or later of its picks is left out, and the picks that stay
+    keep the weights the router gave them; prompt batches are not touched).
+
+    ids, w: [T][K] routing of the call.  A pick's place is 1 + the number of
+    its token's picks with a larger weight, or an equal weight and a lower
+    id (the selection's own order: larger logit first, ties to the lower
+    id).  Returns (w2, skipped): w with the left-out picks' weights set to
+    0, and a [T][K] bool mask of those picks.  n <= 0 or n >= K leaves every
+    pick (n = 0 is "off").  Plain loops: calls have at most a few hundred
+    picks."""
+    ids = np.asarray(ids, dtype=np.int64)
+    w = np.asarray(w, dtype=np.float32)
+    T, K = ids.shape
+    skipped = np.zeros((T, K), dtype=bool)
+    if n <= 0 or n >= K:
+        return w.copy(), skipped
+    place = np.zeros((T, K), dtype=np.int64)
+    for t in range(T):
+        for k in range(K):
+            before = 0
+            for j in range(K):
+                if w[t, j] > w[t, k] or (w[t, j] == w[t, k] and ids[t, j] < ids[t, k]):
+                    before += 1
+            place[t, k] = before + 1
+    kept = set()
+    for t in range(T):
+        for k in range(K):
+            if place[t, k] <= n:
+                kept.add(int(ids[t, k]))
+    for t in range(T):
+        for k in range(K):
+            skipped[t, k] = int(ids[t, k]) not in kept
+    w2 = w.copy()
+    w2[skipped] = 0.0
+    return w2, skipped
+
+
 def sigmoid(s: float) -> float:
     return float(lib().orc_sigmoid(ctypes.c_float(s)))
 
