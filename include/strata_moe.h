@@ -216,6 +216,30 @@ STRATA_API strata_status moe_layer_forward_routed(const strata_moe_dims* dims,
                                        const float* weights_dev, void* out_dev, void* ws_dev,
                                        size_t ws_bytes, void* stream);
 
+/* As moe_layer_forward, with tail-skip (PolyStrata, "Models and backends",
+ * section "What was tuned"): in a decode window (T <= moe_decode_max_tokens())
+ * an expert that every token of the call ranks at place tail_skip + 1 or
+ * later of its top_k picks is not computed; the picks that stay keep the
+ * router's weights (no renormalisation).  A pick's place counts its token's
+ * picks with a larger weight, or an equal weight and a lower id.  The
+ * window runs on the decode kernels whatever T is.  A prompt batch
+ * (T > moe_decode_max_tokens()) is not touched and runs as
+ * moe_layer_forward.  tail_skip = 0 or >= top_k leaves every pick.
+ *   forced_ids_dev / forced_weights_dev: both NULL to route, or both given
+ *     to force the routing (the places are then those of the given weights).
+ *   ids_dev / weights_dev / shared_gate_dev (out, optional): the routing;
+ *     the weights of left-out picks are written as 0, their ids as chosen.
+ * Changes the layer's result by design: not a drop-in for the exact call.
+ * STRATA_EINVAL for tail_skip < 0 or one of the forced pointers alone. */
+STRATA_API strata_status moe_layer_forward_tail_skip(const strata_moe_dims* dims,
+                                          const strata_moe_layer* layer, const void* x_dev,
+                                          int32_t T, int32_t tail_skip,
+                                          const int32_t* forced_ids_dev,
+                                          const float* forced_weights_dev, int32_t* ids_dev,
+                                          float* weights_dev, float* shared_gate_dev,
+                                          void* out_dev, void* ws_dev, size_t ws_bytes,
+                                          void* stream);
+
 /* One residual MoE block of a layer stack:
  *   x = bf16(rmsnorm(resid, eps));  out = layer(x);  resid += float(out)
  * resid_dev fp32 [T][H] (in/out).  ids_dev / weights_dev: NULL to route, or

@@ -175,7 +175,7 @@ strata_status stage_route(const strata_moe_dims* d, const strata_moe_layer* L, c
 strata_status stage_gate_up(const strata_moe_dims* d, const strata_moe_layer* L, const void* x,
                             int T, const int32_t* forced_ids, const float* forced_w,
                             int32_t* ids_user, float* w_user, float* sig_user, void* ws,
-                            cudaStream_t s) {
+                            cudaStream_t s, int tail_skip = 0) {
     const WsLayout W = ws_layout(*d, T);
     GuLaunch g{};
     g.q = L->gu_q_dev;
@@ -203,6 +203,7 @@ strata_status stage_gate_up(const strata_moe_dims* d, const strata_moe_layer* L,
     g.E = d->n_experts;
     g.K = d->top_k;
     g.mode = kGuRoute;
+    g.tail_skip = tail_skip;
     return cuda_status(launch_gate_up_decode(g, s));
 }
 
@@ -234,14 +235,16 @@ strata_status stage_down(const strata_moe_dims* d, const strata_moe_layer* L, in
 }
 
 // One layer on the decode kernels.  forced_ids/forced_w: NULL to route.
-// resid: NULL, or the residual that gets += the bf16 output.
+// resid: NULL, or the residual that gets += the bf16 output.  tail_skip: 0,
+// or the place past which an expert every token ranks there is left out.
 strata_status decode_layer(const strata_moe_dims* d, const strata_moe_layer* L, const void* x,
                            int T, const int32_t* forced_ids, const float* forced_w,
                            int32_t* ids_user, float* w_user, float* sig_user, void* out,
-                           float* resid, void* ws, cudaStream_t s) {
+                           float* resid, void* ws, cudaStream_t s, int tail_skip = 0) {
     strata_status st = stage_route(d, L, x, T, forced_ids != nullptr, ws, s);
     if (st != STRATA_OK) return st;
-    st = stage_gate_up(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, ws, s);
+    st = stage_gate_up(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, ws, s,
+                       tail_skip);
     if (st != STRATA_OK) return st;
     return stage_down(d, L, T, out, resid, ws, s);
 }
@@ -706,6 +709,34 @@ strata_status moe_layer_forward_routed(const strata_moe_dims* dims,
         return STRATA_EINVAL;
     return any_layer(dims, layer, x_dev, T, ids_dev, weights_dev, nullptr, nullptr, nullptr,
                      out_dev, nullptr, ws_dev, static_cast<cudaStream_t>(stream));
+}
+
+strata_status moe_layer_forward_tail_skip(const strata_moe_dims* dims,
+                                          const strata_moe_layer* layer, const void* x_dev,
+                                          int32_t T, int32_t tail_skip,
+                                          const int32_t* forced_ids_dev,
+                                          const float* forced_weights_dev, int32_t* ids_dev,
+                                          float* weights_dev, float* shared_gate_dev,
+                                          void* out_dev, void* ws_dev, size_t ws_bytes,
+                                          void* stream) {
+    if (!dims_ok(dims) || T < 0 || tail_skip < 0 ||
+        !layer_ok(layer, kRouter | kRouted | kShared) ||
+        ((forced_ids_dev == nullptr) != (forced_weights_dev == nullptr)))
+        return STRATA_EINVAL;
+    if (T == 0) return STRATA_OK;
+    if (!al16(x_dev) || !opt4(forced_ids_dev) || !opt4(forced_weights_dev) || !opt4(ids_dev) ||
+        !opt4(weights_dev) || !opt4(shared_gate_dev) || !al16(out_dev) ||
+        !ws_ok(dims, T, ws_dev, ws_bytes))
+        return STRATA_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // a decode window: the decode kernels with the skip; a prompt batch is
+    // not touched
+    if (T <= kDecodeMaxTokens)
+        return decode_layer(dims, layer, x_dev, T, forced_ids_dev, forced_weights_dev, ids_dev,
+                            weights_dev, shared_gate_dev, out_dev, nullptr, ws_dev, s,
+                            tail_skip < dims->top_k ? tail_skip : 0);
+    return any_layer(dims, layer, x_dev, T, forced_ids_dev, forced_weights_dev, ids_dev,
+                     weights_dev, shared_gate_dev, out_dev, nullptr, ws_dev, s);
 }
 
 strata_status moe_block_forward(const strata_moe_dims* dims, const strata_moe_layer* layer,

@@ -342,10 +342,22 @@ __global__ void __launch_bounds__(kGuThreads, 1) k_gate_up(GuLaunch a) {
         // routing: the same in every CTA; CTA 0 publishes it
         route_cta(a.logits, T, E, K, a.forced_ids, a.forced_w, s_ids, s_w, s_sig,
                   reinterpret_cast<float*>(g_ring), a.err, tid, int(blockDim.x), BlockSync{});
+        // tail-skip: the bucketing sees the left-out picks as unrouted; the
+        // selection's scratch at the start of the ring is free until the
+        // first weight copy, which needs the plan
+        const int* bids = s_ids;
+        if (a.tail_skip > 0 && a.tail_skip < K) {
+            int* rank = reinterpret_cast<int*>(g_ring);
+            int* bid = rank + kDecodeMaxTokens * kMaxTopK;
+            int* keep = bid + kDecodeMaxTokens * kMaxTopK;
+            tail_skip_cta(s_ids, s_w, T, K, E, a.tail_skip, rank, bid, keep, tid,
+                          int(blockDim.x));
+            bids = bid;
+        }
         // the plan only; CTA 0 publishes the routing and the bucketing after
         // its share of the experts, off the path to the first weight copy
         const BucketOut none{nullptr, nullptr, nullptr, nullptr, nullptr};
-        bucket_cta(s_ids, T, K, E, s_cnt, s_off, s_wsum, P, s_inv, none, tid, int(blockDim.x),
+        bucket_cta(bids, T, K, E, s_cnt, s_off, s_wsum, P, s_inv, none, tid, int(blockDim.x),
                    BlockSync{});
         __syncthreads();
     }
@@ -744,6 +756,9 @@ cudaError_t launch_gate_up_decode(GuLaunch a, cudaStream_t s) {
     size_t dyn = size_t(a.stages) * stage + (a.x_smem ? size_t(a.T) * a.H * 2 : 0);
     const size_t sel = size_t(kGuConsumers + 1) * (a.E + 16) * sizeof(float);
     if (dyn < sel) dyn = sel;
+    // tail-skip scratch (ranks, bucketing ids, expert flags) at the ring's start
+    const size_t skip = size_t(2 * kDecodeMaxTokens * kMaxTopK + a.E) * sizeof(int);
+    if (a.tail_skip > 0 && dyn < skip) dyn = skip;
     cudaError_t err;
     if (mc <= 1) {
         if ((err = allow_smem(k_gate_up<1>, dyn)) != cudaSuccess) return err;

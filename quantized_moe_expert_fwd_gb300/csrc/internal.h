@@ -100,6 +100,8 @@ struct GuLaunch {
     uint32_t* err;
     int T, H, I, E, K;
     int mode;
+    int tail_skip;                    // kGuRoute: 0 off, else leave out experts every token
+                                      // ranks past this place (1 <= tail_skip < K)
     int stages, x_smem;               // set by the launcher
 };
 cudaError_t launch_gate_up_decode(GuLaunch a, cudaStream_t s);

@@ -257,6 +257,46 @@ __device__ void bucket_cta(const int* s_ids, int T, int K, int E, int* s_cnt, in
     }
 }
 
+// Tail-skip of one call's routing (PolyStrata, "Models and backends",
+// section "What was tuned"): an expert that every token of the call ranks
+// at place n + 1 or later of its K picks is left out; the picks that stay
+// keep their weights.  A pick's place counts its token's picks with a
+// larger weight, or an equal weight and a lower id (the selection's order).
+// Writes bid[p] = s_ids[p], or -1 for a left-out pick (no slot in the
+// bucketing), and sets a left-out pick's weight to 0.  rank: T*K ints,
+// keep: E ints of scratch.  Every thread of the CTA calls it.
+__device__ inline void tail_skip_cta(const int* s_ids, float* s_w, int T, int K, int E, int n,
+                                     int* rank, int* bid, int* keep, int tid, int nthr) {
+    const int TK = T * K;
+    #pragma unroll 1
+    for (int e = tid; e < E; e += nthr) keep[e] = 0;
+    #pragma unroll 1
+    for (int p = tid; p < TK; p += nthr) {
+        const int t0 = (p / K) * K, id = s_ids[p];
+        const float w = s_w[p];
+        int r = 0;
+        #pragma unroll 1
+        for (int j = t0; j < t0 + K; ++j) r += (s_w[j] > w || (s_w[j] == w && s_ids[j] < id)) ? 1 : 0;
+        rank[p] = r;
+    }
+    __syncthreads();
+    #pragma unroll 1
+    for (int p = tid; p < TK; p += nthr) {
+        const int id = s_ids[p];
+        if (rank[p] < n && id >= 0 && id < E) keep[id] = 1;
+    }
+    __syncthreads();
+    #pragma unroll 1
+    for (int p = tid; p < TK; p += nthr) {
+        const int id = s_ids[p];
+        const bool valid = id >= 0 && id < E;
+        const bool left_out = valid && keep[id] == 0;
+        bid[p] = valid && !left_out ? id : -1;
+        if (left_out) s_w[p] = 0.0f;
+    }
+    __syncthreads();
+}
+
 // ------------------------------------------------------------- selection
 // Order-preserving 32-bit key of a logit: a larger float has a larger key.
 // NaN (and a taken entry) gets key 0, which never wins.

@@ -76,6 +76,7 @@ def load() -> ctypes.CDLL:
             "moe_combine": (I32, [D, L, P, I32, P, P, P, P, P, P, SZ, P]),
             "moe_layer_forward": (I32, [D, L, P, I32, P, P, P, P, P, SZ, P]),
             "moe_layer_forward_routed": (I32, [D, L, P, I32, P, P, P, P, SZ, P]),
+            "moe_layer_forward_tail_skip": (I32, [D, L, P, I32, I32, P, P, P, P, P, P, P, SZ, P]),
             "moe_block_forward": (I32, [D, L, P, I32, ctypes.c_float, P, P, P, P, P, SZ, P]),
             "moe_stack_forward": (I32, [D, L, I32, P, I32, ctypes.c_float, P, P, P, P, SZ, P]),
             "moe_decode_route": (I32, [D, L, P, I32, I32, P, SZ, P]),
@@ -99,6 +100,7 @@ EXPORTED = ("moe_workspace_bytes", "moe_decode_max_tokens", "moe_layer_decode_ma
             "moe_rmsnorm", "moe_route",
             "moe_permute", "moe_expert_gate_up", "moe_expert_down", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_routed",
+            "moe_layer_forward_tail_skip",
             "moe_block_forward", "moe_stack_forward", "moe_decode_route", "moe_decode_gate_up",
             "moe_decode_down_combine", "moe_layer_forward_static", "moe_layer_profile",
             "moe_get_device_status",
@@ -247,6 +249,16 @@ def moe_layer_forward_routed(dims, layer: DeviceLayer, x, ids, weights, out, ws,
     _check("moe_layer_forward_routed", load().moe_layer_forward_routed(
         ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(x), x.shape[0], _ptr(ids),
         _ptr(weights), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_layer_forward_tail_skip(dims, layer: DeviceLayer, x, out, ws, tail_skip: int,
+                                forced_ids=None, forced_weights=None, ids=None, weights=None,
+                                shared_gate=None, stream=None):
+    d = dims_struct(dims)
+    _check("moe_layer_forward_tail_skip", load().moe_layer_forward_tail_skip(
+        ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(x), x.shape[0], int(tail_skip),
+        _ptr(forced_ids), _ptr(forced_weights), _ptr(ids), _ptr(weights), _ptr(shared_gate),
+        _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_block_forward(dims, layer: DeviceLayer, resid, ws, eps: float = 1e-6, ids=None,

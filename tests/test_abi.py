@@ -78,6 +78,14 @@ def test_invalid_arguments_return_einval_without_launching(lib):
     assert st == q.STRATA_OK
     st = lib.moe_rmsnorm(null, 3, 2050, ctypes.c_float(1e-6), null, null)
     assert st == q.STRATA_EINVAL
+    # tail-skip: a negative place, and forced ids without forced weights
+    st = lib.moe_layer_forward_tail_skip(ctypes.byref(d), ctypes.byref(L), null, 1, -1, null,
+                                         null, null, null, null, null, null, 0, null)
+    assert st == q.STRATA_EINVAL
+    st = lib.moe_layer_forward_tail_skip(ctypes.byref(d), ctypes.byref(L), null, 1, 5,
+                                         ctypes.c_void_p(256), null, null, null, null, null, null,
+                                         0, null)
+    assert st == q.STRATA_EINVAL
     # misaligned workspace pointer
     st = lib.moe_get_device_status(ctypes.c_void_p(8), null)
     assert st == q.STRATA_EINVAL
