@@ -1,0 +1,83 @@
+"""Pins of the MXFP8 emulation used for the 8-bit-activation tolerance study
+(oracle/w4a8.py): the e4m3 rounding against the format's own value table
+and tie rule, the block scales, and the harness against the exact oracle
+(with quantization off it must reproduce the oracle's layer)."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import w4a8
+from workloads import gen
+
+
+def test_value_table_from_the_bit_fields():
+    v = w4a8.e4m3_values()
+    assert len(v) == 253                      # 2 x 126 nonzero finite values and zero
+    assert v.max() == 448.0 and -v.min() == 448.0
+    assert v[v > 0].min() == 2.0 ** -9        # smallest subnormal
+    assert np.array_equal(w4a8.e4m3_round(v), v)
+
+
+def test_round_to_nearest_table_value():
+    table = w4a8.e4m3_values()
+    rng = np.random.default_rng(0)
+    x = rng.normal(0, 1, 20000) * np.exp2(rng.integers(-12, 9, 20000))
+    x = x[np.abs(x) <= 448.0]
+    got = w4a8.e4m3_round(x)
+    idx = np.abs(x[:, None] - table[None, :]).argmin(axis=1)
+    assert np.array_equal(got, table[idx])
+
+
+@pytest.mark.parametrize("x,want", [
+    (1.0 + 1 / 16, 1.0),          # halfway 1 and 1.125: even mantissa (000)
+    (1.0 + 3 / 16, 1.25),         # halfway 1.125 and 1.25: even mantissa (010)
+    (464.0, 448.0),               # halfway 448 (110) and 480 (111, not a value)
+    (1000.0, 448.0),              # saturates
+    (2.0 ** -10, 0.0),            # halfway 0 and the smallest subnormal
+    (3 * 2.0 ** -10, 2.0 ** -8),  # halfway 2^-9 (001) and 2^-8 (010)
+    (-(1.0 + 3 / 16), -1.25),
+])
+def test_ties_to_even_and_saturation(x, want):
+    assert w4a8.e4m3_round(x) == want
+
+
+def test_block_scales_are_powers_of_two_and_fit():
+    rng = np.random.default_rng(1)
+    x = rng.normal(0, 1, (5, 128))
+    el, sc = w4a8.mx_quantize(x)
+    assert sc.shape == (5, 4)
+    assert np.all(np.exp2(np.round(np.log2(sc))) == sc)
+    blocks = np.abs(el).reshape(5, 4, 32).max(axis=-1)
+    assert np.all((blocks >= 256.0) & (blocks <= 448.0))   # the spec's scale: top binade
+    err = np.abs(el * np.repeat(sc, 32, axis=1) - x)
+    # within half a spacing of the element's binade, or the saturation loss
+    assert np.all(err <= np.maximum(np.abs(x) * 2.0 ** -4, 64 * np.repeat(sc, 32, axis=1)))
+
+
+def test_power_of_two_scales_make_weights_exact():
+    rng = np.random.default_rng(2)
+    q = rng.integers(-8, 8, (4, 64)).astype(np.float64)
+    s = np.exp2(rng.integers(-10, -3, (4, 2))).astype(np.float16)
+    got = w4a8.weight_mx(q, s.view(np.uint16))
+    assert np.array_equal(got, q * np.repeat(s.astype(np.float64), 32, axis=1))
+
+
+def test_unpack_matches_the_oracle_dequantisation():
+    planes = gen.draw_layer(gen.TOY, 5)
+    q = planes["gu_q"][3]
+    s = planes["gu_s"][3]
+    want = oracle.dequant_matrix(q, s, q.shape[0], 2 * q.shape[1])
+    got = w4a8.unpack_q(q) * np.repeat(s.view(np.float16).astype(np.float64), 32, axis=1)
+    assert np.array_equal(got.astype(np.float32), want)
+
+
+def test_harness_without_quantization_is_the_oracle():
+    dims = gen.TOY
+    planes = gen.draw_layer(dims, 6)
+    xb = gen.draw_tokens(dims, 6, 6, "bf16")
+    ref = oracle.moe_forward(dims, planes, xb)
+    ex = w4a8.layer_forward(dims, planes, xb, ref["ids"], ref["w"], ref["sig"], quantize=False)
+    assert np.linalg.norm(ex - ref["out"]) / np.linalg.norm(ref["out"]) < 1e-5
+    qz = w4a8.layer_forward(dims, planes, xb, ref["ids"], ref["w"], ref["sig"], quantize=True)
+    rel = np.linalg.norm(qz - ref["out"]) / np.linalg.norm(ref["out"])
+    assert 0.01 < rel < 0.2                   # the scheme's own error: percent, not bits
