@@ -15,11 +15,16 @@ inputs, bf16 activations):
             and a Zipf(1.1) router bias.
   stack     one token (--tokens 1 or 4) through a 40-layer residual MoE stack
             (one moe_stack_forward call, 18.2 GB resident) as one CUDA graph.
+  prefill   T=2048 prompt tokens through one layer with Zipf-skewed routing
+            (the tensor-core grouped GEMMs).
 
 Printed: one JSON line (rank 0).  value = tokens per second through one MoE
 layer (decode1/decode16: layer-tokens / s; stack: tokens / s through all 40
-layers).  The roofline object is for the dominant decode kernel, timed alone
-with CUDA events on its own stream; cpu_baseline is the C oracle on the host.
+layers; prefill: prompt tokens / s).  The roofline object is for the
+dominant kernel, timed alone with CUDA events on its own stream (HBM-bound
+for the decode kernels, tensor-bound for the prefill GEMM); the default
+decode1 line also carries a "prefill" block with the T=2048 layer and its
+gate/up GEMM's tensor roofline.  cpu_baseline is the C oracle on the host.
 --impl reference times that oracle itself on the same workload and metric.
 """
 from __future__ import annotations
