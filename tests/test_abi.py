@@ -40,6 +40,26 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(_header_functions()) == set(q.strata_moe.EXPORTED)
 
 
+def _header_arity():
+    """Parameter count of every declared prototype (void-parameter lists: 0)."""
+    with open(os.path.join(ROOT, "include", "strata_moe.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"STRATA_API\s+[\w\s\*]+?\b((?:moe|strata)_\w+)\s*\(([^)]*)\)", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    """The binding's ctypes argument lists have the header's arity, so a
+    changed prototype cannot be called with a stale argument list."""
+    arity = _header_arity()
+    assert set(arity) == set(_header_functions())
+    for name, n in arity.items():
+        assert len(getattr(lib, name).argtypes) == n, name
+
+
 def test_workspace_bytes(lib):
     assert q.moe_workspace_bytes(gen.QWEN, 1) > 0
     assert q.moe_workspace_bytes(gen.QWEN, 32) > q.moe_workspace_bytes(gen.QWEN, 1)
