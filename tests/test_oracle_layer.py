@@ -1,6 +1,7 @@
 """Pins of the oracle's expert FFN, combine and whole layer."""
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from tests import brute
@@ -176,3 +177,93 @@ def test_stack_residual_chain_two_layers():
         out = oracle.moe_forward(dims, L, x)["out"]
         rr = rr + oracle.bf16_array_to_f32(oracle.round_bf16(out))
     assert np.array_equal(r, rr)
+
+
+def _bf16_bits_f64(a):
+    """float64 -> bf16 bits, round to nearest even (torch's conversion)."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _round_like(v, got_bits, tol):
+    """Rounds the float64 values v to bf16 and checks the oracle's bits
+    got_bits against them: a correct rounding of a value computed within
+    `tol` (absolute, per element: the fp32 error bound) of v is a bf16 value
+    within half a bf16 ulp of v plus tol.  Where the oracle's bits differ
+    from v's own rounding but obey that bound, they are kept.  Returns the
+    bits to continue with and the number of elements that broke the bound."""
+    v = np.asarray(v, dtype=np.float64)
+    want = _bf16_bits_f64(v)
+    got = np.asarray(got_bits, dtype=np.uint16).reshape(v.shape)
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(v), 1e-300))) - 8.0)
+    ok = (got == want) | (np.abs(brute.bf16_bits_to_f64(got) - v) <= half_ulp + tol)
+    return np.where(ok, got, want), int((~ok).sum())
+
+
+def _stack64(dims, layers, r0, recs, forced=None):
+    """The residual stack in float64 with no oracle arithmetic: r +=
+    bf16(layer(x)), x = bf16(r / sqrt(mean(r^2) + 1e-6)), each layer by the
+    float64 brute force.  At each bf16 rounding the oracle's bits (recs) must
+    be the float64 chain's, except within fp32 error of a rounding midpoint,
+    where the oracle's choice of neighbour is followed.  Returns the final r
+    and the number of roundings that broke that rule."""
+    r = np.asarray(r0, dtype=np.float64).copy()
+    bad = 0
+    for li, L in enumerate(layers):
+        xn = r / np.sqrt((r * r).mean(axis=1, keepdims=True) + 1e-6)
+        xb, n = _round_like(xn, recs[li]["x"], 4e-7 * np.abs(xn) + 1e-30)
+        bad += n
+        if forced is None:
+            res = brute.layer(dims, L, xb)
+        else:
+            res = brute.layer(dims, L, xb, ids=forced[li][0], w=forced[li][1])
+        out = res["out"]
+        rms = np.sqrt((out * out).mean(axis=1, keepdims=True))
+        ob, n = _round_like(out, recs[li]["out_bf16"], 1e-5 * np.abs(out) + 1e-6 * rms)
+        bad += n
+        r = r + brute.bf16_bits_to_f64(ob)
+    return r, bad
+
+
+def test_stack_against_float64_composition():
+    """stack_forward against the chain written out in float64 from the
+    brute-force layer (no oracle function on the reference side): every
+    rounded input and output of every layer is the float64 chain's (up to
+    the choice of neighbour within fp32 error of a bf16 midpoint) and the
+    final residual agrees to fp32 accumulation error."""
+    dims = gen.TOY
+    layers = [gen.draw_layer(dims, s) for s in (3, 4, 5)]
+    r0 = gen.draw_tokens(dims, 3, 9, "resid")
+    r, recs = oracle.stack_forward(dims, layers, r0)
+    r64, bad = _stack64(dims, layers, r0, recs)
+    assert bad == 0
+    rel = np.linalg.norm(r - r64) / np.linalg.norm(r64)
+    assert rel < 1e-6, rel
+    # a misplaced rounding is far larger: leaving out the bf16 rounding of
+    # each layer's output moves r by ~1e-4 relative
+    r_noround = np.asarray(r0, dtype=np.float64).copy()
+    for L in layers:
+        xn = r_noround / np.sqrt((r_noround ** 2).mean(axis=1, keepdims=True) + 1e-6)
+        r_noround = r_noround + brute.layer(dims, L, _bf16_bits_f64(xn))["out"]
+    assert np.linalg.norm(r - r_noround) / np.linalg.norm(r64) > 20 * rel
+
+
+def test_stack_one_hot_routing_two_layers():
+    """Forced one-hot routing (weight 1 on one expert, 0 on the others) in a
+    2-layer stack: each layer is the shared expert plus one dense SwiGLU FFN;
+    stack_forward must follow the float64 chain."""
+    dims = gen.TOY
+    layers = [gen.draw_layer(dims, s) for s in (6, 7)]
+    T, K = 2, dims.top_k
+    r0 = gen.draw_tokens(dims, T, 11, "resid")
+    forced = []
+    for li in range(2):
+        ids = np.array([[3 + li, 10, 20, 30], [0, 5 + li, 17, 31]], dtype=np.int32)[:, :K]
+        w = np.zeros((T, K), dtype=np.float32)
+        w[0, 0] = 1.0
+        w[1, 1] = 1.0
+        forced.append((ids, w))
+    r, recs = oracle.stack_forward(dims, layers, r0, forced=forced)
+    r64, bad = _stack64(dims, layers, r0, recs, forced=forced)
+    assert bad == 0
+    assert np.linalg.norm(r - r64) / np.linalg.norm(r64) < 1e-6
