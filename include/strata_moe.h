@@ -111,12 +111,10 @@ STRATA_API int32_t moe_decode_max_tokens(void);
 
 /* The T at and below which the whole-layer calls (moe_layer_forward,
  * moe_layer_forward_routed, moe_block_forward, moe_stack_forward) take the
- * decode kernels; above it they take the tcgen05 kernels, unless the shape
- * does not allow those (hidden % 256 != 0 or an intermediate size below 256),
- * when the decode kernels serve up to moe_decode_max_tokens().  Measured on
- * GB300 at the 2048-hidden, 256-expert, top-8 shape: the decode kernels' layer
- * time grows by ~16 us a token from ~32 us at T = 1, the tcgen05 kernels' by
- * ~2 us a token from ~45 us, about equal at T = 2. */
+ * three decode kernels when the persistent kernel does not take the call
+ * (see moe_layer_path); above it they take the tcgen05 kernels, unless the
+ * shape does not allow those (hidden % 256 != 0 or an intermediate size
+ * below 256), when the decode kernels serve up to moe_decode_max_tokens(). */
 STRATA_API int32_t moe_layer_decode_max_tokens(void);
 
 /* Input RMSNorm, unit weight:  x[t][h] = bf16( r[t][h] / sqrt(mean_h r^2 + eps) ).
@@ -197,10 +195,13 @@ STRATA_API strata_status moe_combine(const strata_moe_dims* dims, const strata_m
                           const float* shared_gate_dev, void* out_dev, void* ws_dev,
                           size_t ws_bytes, void* stream);
 
-/* The whole layer: route, permute, experts, shared expert, combine.  For
- * T <= moe_layer_decode_max_tokens() it runs three decode kernels (router +
- * shared gate/up in one; selection, bucketing and routed gate/up in one;
- * every down product + combine in one); above, the tcgen05 prefill kernels.
+/* The whole layer: route, permute, experts, shared expert, combine.  Which
+ * kernels run is moe_layer_path(dims, T): at decode sizes ONE persistent
+ * kernel (one CTA per SM; the router product, top-K and bucketing, the
+ * routed gate/up, the down products and the combine separated by grid-wide
+ * barriers on flags in the workspace; PolyStrata, "Models and backends",
+ * section "What was tuned": decode was launch-bound at ~35 launches a
+ * layer), else three decode kernels or the tcgen05 prefill kernels.
  * ids_dev / weights_dev / shared_gate_dev receive the routing when non-NULL.
  * out_dev bf16 [T][H]. */
 STRATA_API strata_status moe_layer_forward(const strata_moe_dims* dims, const strata_moe_layer* layer,
@@ -242,6 +243,7 @@ STRATA_API strata_status moe_layer_forward_tail_skip(const strata_moe_dims* dims
 
 /* One residual MoE block of a layer stack:
  *   x = bf16(rmsnorm(resid, eps));  out = layer(x);  resid += float(out)
+ * On the persistent kernel (moe_layer_path) the norm runs inside it. 
  * resid_dev fp32 [T][H] (in/out).  ids_dev / weights_dev: NULL to route, or
  * both non-NULL to force the routing.  x_out_dev / out_dev: optional bf16
  * [T][H] copies of the block's input and output (NULL: workspace only). */
@@ -256,9 +258,13 @@ STRATA_API strata_status moe_block_forward(const strata_moe_dims* dims, const st
  * read during the call only.  resid_dev fp32 [T][H] (in/out); ids_dev /
  * weights_dev: NULL to route every layer, or both int32 / fp32
  * [n_layers][T][K] to force the routing; out_dev: NULL or bf16 [T][H], the
- * last layer's output.  One moe_block_forward per layer, all enqueued by
- * this call ("qwen36: CUDA VRAM expert tier", section "Placement": a token's
- * routed experts are 40 layers of top-8). */
+ * last layer's output ("qwen36: CUDA VRAM expert tier", section
+ * "Placement": a token's routed experts are 40 layers of top-8).  Where
+ * moe_layer_path(dims, T) is STRATA_PATH_PERSISTENT the whole stack runs as
+ * one persistent kernel per 40 layers: each layer's RMSNorm, routing,
+ * experts and residual add inside it, and each CTA's share of the next
+ * layer's router and shared-expert rows requested while the current layer
+ * streams its experts.  Otherwise one moe_block_forward per layer. */
 STRATA_API strata_status moe_stack_forward(const strata_moe_dims* dims,
                                            const strata_moe_layer* layers, int32_t n_layers,
                                            float* resid_dev, int32_t T, float eps,
@@ -341,10 +347,42 @@ STRATA_API strata_status moe_layer_profile(const strata_moe_dims* dims,
                                            size_t ws_bytes, void* stream, float* us,
                                            int32_t max_n, int32_t* n_out);
 
+/* Which kernels a whole-layer call (moe_layer_forward, _routed,
+ * moe_block_forward, moe_stack_forward) runs for T tokens of this shape on
+ * the current device: STRATA_PATH_PERSISTENT (one persistent kernel a call;
+ * a stack, one per 40 layers), STRATA_PATH_DECODE (three decode kernels a
+ * layer, plus the RMSNorm kernel in a block), STRATA_PATH_TC (the tcgen05
+ * prefill kernels), or 0 for an unsupported shape or T < 1.  forced != 0
+ * asks for a call with forced routing.  Host only; no GPU work. */
+#define STRATA_PATH_PERSISTENT 1
+#define STRATA_PATH_DECODE 2
+#define STRATA_PATH_TC 3
+STRATA_API int32_t moe_layer_path(const strata_moe_dims* dims, int32_t T, int32_t forced);
+
+/* The bucketing of the last whole-layer call (moe_layer_forward or _routed,
+ * any path) made on this workspace with this T: copies counts int32 [E],
+ * offsets int32 [E+1], perm int32 [T*K] and inv_perm int32 [T*K] (layout as
+ * moe_permute) out of the workspace, on `stream`.  For tests and debugging:
+ * it shows the bucketing the layer's own kernels built, which the stage call
+ * moe_permute does not run.  STRATA_EINVAL for a bad argument. */
+STRATA_API strata_status moe_layer_bucketing(const strata_moe_dims* dims, int32_t T,
+                                             const void* ws_dev, size_t ws_bytes,
+                                             int32_t* counts_dev, int32_t* offsets_dev,
+                                             int32_t* perm_dev, int32_t* inv_perm_dev,
+                                             void* stream);
+
 /* Synchronises `stream`, returns the status latched in the workspace's error
  * word (STRATA_OK when none) and clears the word.  For tests and debugging;
  * it is the one call that synchronises. */
 STRATA_API strata_status moe_get_device_status(void* ws_dev, void* stream);
+
+/* Testing hook: the number of polls after which a grid-wide barrier of the
+ * persistent kernel gives up, latches STRATA_ETIMEOUT in the workspace's
+ * error word and lets the kernel run on to its end (with wrong values, but
+ * without hanging).  0 restores the default (~2^21 polls, a second or two).
+ * Applies to launches made after the call, from any host thread.  Copies
+ * into shared memory are always waited for in full. */
+STRATA_API void strata_set_grid_wait_limit(uint32_t polls);
 
 /* Static, human-readable name of a status. */
 STRATA_API const char* strata_status_str(strata_status s);

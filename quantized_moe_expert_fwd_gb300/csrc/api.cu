@@ -22,6 +22,7 @@ WsLayout ws_layout(const strata_moe_dims& d, int T) {
         return at;
     };
     L.ctl = take(sizeof(Ctl));
+    L.flags = take(size_t(kMaxGrid) * 4);     // at a fixed offset: every T shares it
     L.logits = take(t * (E + 1) * 4);
     L.ids = take(t * K * 4);
     L.w = take(t * K * 4);
@@ -38,6 +39,12 @@ WsLayout ws_layout(const strata_moe_dims& d, int T) {
         L.hs = take(t * Is * 4);
     }
     L.decode_end = o;
+    if (T <= kPersistMaxTokens) {
+        L.ll_logits = take(t * (E + 1) * 8);
+        L.ll_hs = take(t * Is * 8);
+        L.ll_h = take(t * K * I * 8);
+        L.ll_resid = take(t * H * 8);
+    }
     if (T > kLayerDecodeMaxTokens) {
         const size_t nblk = (t + 31) / 32;
         const size_t max_mb = (t * K) / kBM + E + t / kBM + 2;
@@ -395,13 +402,96 @@ strata_status pf_down(const strata_moe_dims* d, const strata_moe_layer* L, int T
     return STRATA_OK;
 }
 
-// The layer at any T: decode kernels up to kLayerDecodeMaxTokens (or up to
+// n_layers residual layers (resid != NULL) or one layer on x_in, as
+// persistent-kernel launches of up to kPxMaxLayers layers each;
+// STRATA_EUNSUPPORTED (nothing launched) when that kernel does not take the
+// shape or T.
+strata_status persist_layers(const strata_moe_dims* d, const strata_moe_layer* layers,
+                             int n_layers, const void* x_in, float* resid, float eps, int T,
+                             const int32_t* forced_ids, const float* forced_w, int32_t* ids_user,
+                             float* w_user, float* sig_user, void* out, void* x_out, void* ws,
+                             cudaStream_t s) {
+    PxGeo g;
+    if ((x_in == nullptr) == (resid == nullptr) || (x_in != nullptr && n_layers != 1) ||
+        !px_geometry(*d, T, forced_ids != nullptr, resid != nullptr, device_info().sms, &g))
+        return STRATA_EUNSUPPORTED;
+    const WsLayout W = ws_layout(*d, T);
+    PxArgs a{};
+    a.T = T;
+    a.H = d->hidden;
+    a.E = d->n_experts;
+    a.K = d->top_k;
+    a.I = d->inter;
+    a.Is = d->shared_inter;
+    a.eps = eps;
+    a.x_in = static_cast<const uint16_t*>(x_in);
+    a.resid = resid;
+    a.ll_logits = at<uint64_t>(ws, W.ll_logits);
+    a.ll_hs = at<uint64_t>(ws, W.ll_hs);
+    a.ll_h = at<uint64_t>(ws, W.ll_h);
+    a.ll_resid = at<uint64_t>(ws, W.ll_resid);
+    a.ids = at<int32_t>(ws, W.ids);
+    a.w = at<float>(ws, W.w);
+    a.sig = at<float>(ws, W.sig);
+    a.counts = at<int32_t>(ws, W.counts);
+    a.offsets = at<int32_t>(ws, W.offsets);
+    a.perm = at<int32_t>(ws, W.perm);
+    a.inv = at<int32_t>(ws, W.inv);
+    a.flags = at<uint32_t>(ws, W.flags);
+    a.err = &at<Ctl>(ws, W.ctl)->err;
+    a.grid_wait_limit = grid_wait_limit();
+    a.R = g.R;
+    a.gu_stages = g.gu_stages;
+    a.dn_stages = g.dn_stages;
+    a.off_x = g.off_x;
+    a.off_r = g.off_r;
+    a.off_sd = g.off_sd;
+    a.off_d = g.off_d;
+    a.off_y = g.off_y;
+    a.off_g = g.off_g;
+    a.sd_q = g.sd_q;
+    a.sd_bytes = g.sd_bytes;
+    a.d_q = g.d_q;
+    a.d_stage = g.d_stage;
+    a.g_q = g.g_q;
+    a.g_stage = g.g_stage;
+    const size_t TK = size_t(T) * d->top_k;
+    for (int c0 = 0; c0 < n_layers; c0 += kPxMaxLayers) {
+        const int n = n_layers - c0 < kPxMaxLayers ? n_layers - c0 : kPxMaxLayers;
+        const bool last = c0 + n == n_layers;
+        a.n_layers = n;
+        for (int l = 0; l < n; ++l) {
+            const strata_moe_layer& L = layers[c0 + l];
+            a.L[l] = PxLayer{static_cast<const uint16_t*>(L.router_dev), L.router_bias_dev,
+                             L.gu_q_dev, L.gu_s_dev, L.dn_q_dev, L.dn_s_dev,
+                             L.sh_gu_q_dev, L.sh_gu_s_dev, L.sh_dn_q_dev, L.sh_dn_s_dev};
+        }
+        a.forced_ids = forced_ids ? forced_ids + size_t(c0) * TK : nullptr;
+        a.forced_w = forced_w ? forced_w + size_t(c0) * TK : nullptr;
+        a.out = last ? static_cast<uint16_t*>(out) : nullptr;
+        a.x_out = last ? static_cast<uint16_t*>(x_out) : nullptr;
+        a.ids_user = last ? ids_user : nullptr;
+        a.w_user = last ? w_user : nullptr;
+        a.sig_user = last ? sig_user : nullptr;
+        STRATA_TRY(launch_persistent(a, g, s));
+    }
+    return STRATA_OK;
+}
+
+// The layer at any T: the persistent decode kernel where it takes the shape
+// and T, else the three decode kernels up to kLayerDecodeMaxTokens (or up to
 // kDecodeMaxTokens when the shape does not allow the tensor-core kernels),
 // the tensor-core (prefill) kernels above.
 strata_status any_layer(const strata_moe_dims* d, const strata_moe_layer* L, const void* x, int T,
                         const int32_t* forced_ids, const float* forced_w, int32_t* ids_user,
                         float* w_user, float* sig_user, void* out, float* resid, void* ws,
                         cudaStream_t s) {
+    if (resid == nullptr) {
+        const strata_status st = persist_layers(d, L, 1, x, nullptr, 0.0f, T, forced_ids,
+                                                forced_w, ids_user, w_user, sig_user, out,
+                                                nullptr, ws, s);
+        if (st != STRATA_EUNSUPPORTED) return st;
+    }
     if (T <= kLayerDecodeMaxTokens || (T <= kDecodeMaxTokens && !prefill_supported(*d)))
         return decode_layer(d, L, x, T, forced_ids, forced_w, ids_user, w_user, sig_user, out,
                             resid, ws, s);
@@ -415,10 +505,15 @@ extern "C" {
 
 size_t moe_workspace_bytes(const strata_moe_dims* dims, int32_t max_tokens) {
     if (!dims_ok(dims) || max_tokens < 1) return 0;
-    // a call with T <= max_tokens takes the decode or the prefill layout
+    // a call with T <= max_tokens takes the persistent, the decode or the
+    // prefill layout; each grows with T
+    const int pmax = max_tokens < kPersistMaxTokens ? max_tokens : kPersistMaxTokens;
     const int dmax = max_tokens < kDecodeMaxTokens ? max_tokens : kDecodeMaxTokens;
+    size_t n = ws_layout(*dims, pmax).total;
     const size_t a = ws_layout(*dims, dmax).total, b = ws_layout(*dims, max_tokens).total;
-    return a > b ? a : b;
+    if (a > n) n = a;
+    if (b > n) n = b;
+    return n;
 }
 
 int32_t moe_decode_max_tokens(void) { return kDecodeMaxTokens; }
@@ -754,6 +849,10 @@ strata_status moe_block_forward(const strata_moe_dims* dims, const strata_moe_la
         return STRATA_EINVAL;
     const WsLayout W = ws_layout(*dims, T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const strata_status st = persist_layers(dims, layer, 1, nullptr, resid_dev, eps, T, ids_dev,
+                                            weights_dev, nullptr, nullptr, nullptr, out_dev,
+                                            x_out_dev, ws_dev, s);
+    if (st != STRATA_EUNSUPPORTED) return st;
     void* x = x_out_dev ? x_out_dev : at<void>(ws_dev, W.x);
     void* out = out_dev ? out_dev : at<void>(ws_dev, W.out);
     STRATA_TRY(launch_rmsnorm(resid_dev, T, dims->hidden, eps, static_cast<uint16_t*>(x), s));
@@ -775,6 +874,11 @@ strata_status moe_stack_forward(const strata_moe_dims* dims, const strata_moe_la
         !opt4(weights_dev) || !ws_ok(dims, T, ws_dev, ws_bytes))
         return STRATA_EINVAL;
     const size_t TK = size_t(T) * dims->top_k;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const strata_status pst = persist_layers(dims, layers, n_layers, nullptr, resid_dev, eps, T,
+                                             ids_dev, weights_dev, nullptr, nullptr, nullptr,
+                                             out_dev, nullptr, ws_dev, s);
+    if (pst != STRATA_EUNSUPPORTED) return pst;
     for (int l = 0; l < n_layers; ++l) {
         const strata_status st = moe_block_forward(
             dims, layers + l, resid_dev, T, eps, ids_dev ? ids_dev + l * TK : nullptr,
@@ -872,6 +976,39 @@ strata_status moe_get_device_status(void* ws_dev, void* stream) {
     if (cudaStreamSynchronize(s) != cudaSuccess) return STRATA_ECUDA;
     return static_cast<strata_status>(word);
 }
+
+int32_t moe_layer_path(const strata_moe_dims* dims, int32_t T, int32_t forced) {
+    if (!dims_ok(dims) || T < 1) return 0;
+    PxGeo g;
+    if (px_geometry(*dims, T, forced != 0, false, device_info().sms, &g))
+        return STRATA_PATH_PERSISTENT;
+    if (T <= kLayerDecodeMaxTokens || (T <= kDecodeMaxTokens && !prefill_supported(*dims)))
+        return STRATA_PATH_DECODE;
+    return prefill_supported(*dims) ? STRATA_PATH_TC : 0;
+}
+
+strata_status moe_layer_bucketing(const strata_moe_dims* dims, int32_t T, const void* ws_dev,
+                                  size_t ws_bytes, int32_t* counts_dev, int32_t* offsets_dev,
+                                  int32_t* perm_dev, int32_t* inv_dev, void* stream) {
+    if (!dims_ok(dims) || T < 1 || !ws_ok(dims, T, ws_dev, ws_bytes) || !al4(counts_dev) ||
+        !al4(offsets_dev) || !al4(perm_dev) || !al4(inv_dev))
+        return STRATA_EINVAL;
+    const WsLayout W = ws_layout(*dims, T);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* w = const_cast<void*>(ws_dev);
+    const size_t E = size_t(dims->n_experts), TK = size_t(T) * dims->top_k;
+    STRATA_TRY(cudaMemcpyAsync(counts_dev, at<int32_t>(w, W.counts), E * 4,
+                               cudaMemcpyDeviceToDevice, s));
+    STRATA_TRY(cudaMemcpyAsync(offsets_dev, at<int32_t>(w, W.offsets), (E + 1) * 4,
+                               cudaMemcpyDeviceToDevice, s));
+    STRATA_TRY(cudaMemcpyAsync(perm_dev, at<int32_t>(w, W.perm), TK * 4,
+                               cudaMemcpyDeviceToDevice, s));
+    STRATA_TRY(cudaMemcpyAsync(inv_dev, at<int32_t>(w, W.inv), TK * 4,
+                               cudaMemcpyDeviceToDevice, s));
+    return STRATA_OK;
+}
+
+void strata_set_grid_wait_limit(uint32_t polls) { set_grid_wait_limit(polls); }
 
 const char* strata_last_cuda_error(void) {
     return t_last_cuda == cudaSuccess ? "no error" : cudaGetErrorName(t_last_cuda);

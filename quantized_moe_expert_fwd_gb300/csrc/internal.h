@@ -46,11 +46,13 @@ struct MBlock {
 // Byte offsets of the workspace regions for a call with T tokens.  Every
 // region starts on a 256-byte boundary; the control block is at 0.  The
 // decode regions (plan, h, hs as fp32) exist for T <= kDecodeMaxTokens and
-// end at decode_end; the prefill ones (per-block counts, row blocks, fp16
-// operands, bf16 outputs) follow for T > kLayerDecodeMaxTokens.
+// end at decode_end; the persistent kernel's tagged exchanges follow for
+// T <= kPersistMaxTokens, the prefill ones (per-block counts, row blocks,
+// fp16 operands, bf16 outputs) for T > kLayerDecodeMaxTokens.
 struct WsLayout {
-    size_t ctl, logits, ids, w, sig, counts, offsets, perm, inv, plan, h, hs, x, out;
+    size_t ctl, flags, logits, ids, w, sig, counts, offsets, perm, inv, plan, h, hs, x, out;
     size_t cnt_blk, base_blk, mblocks, n_mblocks, lgp, xg, h16, hs16, y, ysh;
+    size_t ll_logits, ll_hs, ll_h, ll_resid;   // persistent kernel (T <= kPersistMaxTokens)
     size_t decode_end, total;
 };
 
@@ -128,6 +130,72 @@ cudaError_t launch_permute_small(const int32_t* ids, int T, int K, int E, int32_
                                  int32_t* offsets, int32_t* perm, int32_t* inv, uint32_t* err,
                                  cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x, cudaStream_t s);
+
+// ------------------------------------------------ persistent decode layers
+// A whole decode-size layer (or a stack of residual layers) as one launch of
+// one CTA per SM (persist.cu).
+constexpr int kPersistMaxTokens = 16;     // tokens a call it takes
+constexpr int kMaxGrid = 1024;            // grid barrier flags in the workspace
+constexpr int kPxMaxLayers = 40;          // layers one launch carries
+// 1 producer + 15 consumer warps (128 registers a thread): the int4 dot
+// products keep the ALU pipes busy only with several warps on each of the
+// SM's four sub-partitions
+constexpr int kPxConsumers = 15;
+constexpr int kPxRowPairs = 2;            // gate/up row pairs per ring stage (one warp's)
+constexpr int kPxGuMaxStages = 30;
+constexpr int kPxDnMaxStages = 32;
+constexpr size_t kPxSmemBudget = 200 * 1024;   // dynamic shared memory at most
+constexpr size_t kPxSmemMin = 120 * 1024;      // at least: one CTA per SM
+
+struct PxLayer {
+    const uint16_t* router; const float* bias;
+    const uint8_t* gu_q; const uint16_t* gu_s;
+    const uint8_t* dn_q; const uint16_t* dn_s;
+    const uint8_t* sh_gu_q; const uint16_t* sh_gu_s;
+    const uint8_t* sh_dn_q; const uint16_t* sh_dn_s;
+};
+
+// Launch geometry: down rows a CTA owns, ring depths, dynamic shared memory
+// offsets (bytes, 128-aligned) and stage sizes.
+struct PxGeo {
+    int MC, R, gu_stages, dn_stages;
+    uint32_t off_x, off_r, off_sd, off_d, off_y, off_g;
+    uint32_t sd_q, sd_bytes, d_q, d_stage, g_q, g_stage, dyn;
+};
+
+struct PxArgs {
+    int T, H, E, K, I, Is, n_layers;
+    float eps;
+    const uint16_t* x_in;            // resid == NULL (one layer): bf16 [T][H]
+    float* resid;                    // fp32 [T][H]: each layer normalises it, adds its output
+    uint16_t* out;                   // the last layer's bf16 output [T][H], or NULL
+    uint16_t* x_out;                 // the last layer's normalised input [T][H], or NULL
+    const int32_t* forced_ids;       // [n_layers][T][K] or NULL
+    const float* forced_w;
+    int32_t* ids_user; float* w_user; float* sig_user;   // the last layer's routing, or NULL
+    // workspace: the cross-CTA exchanges as tagged 64-bit words (value low,
+    // tag high): logits [T][E+1], shared SwiGLU [T][Is], routed SwiGLU
+    // [T*K][I] in slot order, the stack's residual [T][H]
+    uint64_t* ll_logits; uint64_t* ll_hs; uint64_t* ll_h; uint64_t* ll_resid;
+    int32_t* ids; float* w; float* sig;
+    int32_t* counts; int32_t* offsets; int32_t* perm; int32_t* inv;
+    uint32_t* flags; uint32_t* err;
+    uint32_t grid_wait_limit;        // polls before a grid barrier gives up
+    int R, gu_stages, dn_stages;
+    uint32_t off_x, off_r, off_sd, off_d, off_y, off_g;
+    uint32_t sd_q, sd_bytes, d_q, d_stage, g_q, g_stage;
+    PxLayer L[kPxMaxLayers];
+};
+
+// Whether the persistent kernel takes this shape at T tokens on a grid of G
+// CTAs (resid: the calls that normalise a residual in the kernel), and its
+// geometry.
+bool px_geometry(const strata_moe_dims& d, int T, bool forced, bool resid, int G, PxGeo* g);
+cudaError_t launch_persistent(const PxArgs& a, const PxGeo& g, cudaStream_t s);
+// polls before a grid barrier of the persistent kernel gives up (testing
+// hook, strata_set_grid_wait_limit; 0: the default)
+uint32_t grid_wait_limit();
+void set_grid_wait_limit(uint32_t polls);
 
 // ---------------------------------------------------------------- prefill
 struct PfSelectLaunch {

@@ -84,7 +84,10 @@ def load() -> ctypes.CDLL:
             "moe_decode_down_combine": (I32, [D, L, I32, P, P, P, SZ, P]),
             "moe_layer_forward_static": (I32, [D, L, P, I32, P, P, P, P, P]),
             "moe_layer_profile": (I32, [D, L, P, I32, P, P, SZ, P, P, I32, P]),
+            "moe_layer_path": (I32, [D, I32, I32]),
+            "moe_layer_bucketing": (I32, [D, I32, P, SZ, P, P, P, P, P]),
             "moe_get_device_status": (I32, [P, P]),
+            "strata_set_grid_wait_limit": (None, [ctypes.c_uint32]),
             "strata_status_str": (ctypes.c_char_p, [I32]),
             "strata_last_cuda_error": (ctypes.c_char_p, []),
         }
@@ -103,7 +106,8 @@ EXPORTED = ("moe_workspace_bytes", "moe_decode_max_tokens", "moe_layer_decode_ma
             "moe_layer_forward_tail_skip",
             "moe_block_forward", "moe_stack_forward", "moe_decode_route", "moe_decode_gate_up",
             "moe_decode_down_combine", "moe_layer_forward_static", "moe_layer_profile",
-            "moe_get_device_status",
+            "moe_layer_path", "moe_layer_bucketing", "moe_get_device_status",
+            "strata_set_grid_wait_limit",
             "strata_status_str", "strata_last_cuda_error")
 
 
@@ -315,6 +319,7 @@ def moe_layer_forward_static(dims, layer: DeviceLayer, x, out, ids=None, weights
         _ptr(weights), _ptr(shared_gate), _ptr(out), _stream(stream)))
 
 
+PROFILE_PERSISTENT = ("k_persist",)
 PROFILE_DECODE = ("k_route", "k_gate_up", "k_down")
 PROFILE_PREFILL = ("router_gemm", "select", "count", "scan", "scatter", "gather",
                    "gemm_gate_up", "gemm_down", "combine")
@@ -331,11 +336,34 @@ def moe_layer_profile(dims, layer: DeviceLayer, x, out, ws, stream=None):
     _check("moe_layer_profile", load().moe_layer_profile(
         ctypes.byref(d), ctypes.byref(layer.ptrs), _ptr(x), x.shape[0], _ptr(out), _ptr(ws),
         ws.numel(), _stream(stream), us, 64, ctypes.byref(n)))
-    # which kernels ran: the decode path launches three, the tensor-core path
-    # seven (T <= 32) or nine
-    names = {len(PROFILE_DECODE): PROFILE_DECODE,
+    # which kernels ran: the persistent path launches one, the decode path
+    # three, the tensor-core path seven (T <= 32) or nine
+    names = {len(PROFILE_PERSISTENT): PROFILE_PERSISTENT, len(PROFILE_DECODE): PROFILE_DECODE,
              len(PROFILE_PREFILL_SMALL): PROFILE_PREFILL_SMALL}.get(n.value, PROFILE_PREFILL)
     return {names[i] if i < len(names) else f"k{i}": float(us[i]) for i in range(n.value)}
+
+
+PATH_PERSISTENT, PATH_DECODE, PATH_TC = 1, 2, 3
+
+
+def moe_layer_path(dims, T: int, forced: bool = False) -> int:
+    """Which kernels a whole-layer call of T tokens runs (PATH_*; 0: none)."""
+    d = dims_struct(dims)
+    return int(load().moe_layer_path(ctypes.byref(d), int(T), 1 if forced else 0))
+
+
+def moe_layer_bucketing(dims, T: int, ws, counts, offsets, perm, inv, stream=None):
+    """The bucketing the last whole-layer call on `ws` made (int32 tensors)."""
+    d = dims_struct(dims)
+    _check("moe_layer_bucketing", load().moe_layer_bucketing(
+        ctypes.byref(d), int(T), _ptr(ws), ws.numel(), _ptr(counts), _ptr(offsets), _ptr(perm),
+        _ptr(inv), _stream(stream)))
+
+
+def strata_set_grid_wait_limit(polls: int) -> None:
+    """Testing hook: polls before a persistent-kernel grid barrier gives up
+    (0: the default)."""
+    load().strata_set_grid_wait_limit(int(polls))
 
 
 def moe_get_device_status(ws, stream=None) -> int:

@@ -1,13 +1,15 @@
 """Helpers of the GPU parity tests: device upload, the tolerance, the
 near-tie rule.
 
-Tolerance of floating outputs (bf16 from the GPU against the fp32 oracle):
-relative L2 <= 5e-3 of the raw difference, and for every element
-|got - ref| - half a bf16 ulp of max(|got|, |ref|) <= 2e-2 * rms(ref): the
-max-abs bar bounds the error beyond the output format's own rounding.  Read
-literally it cannot be met by any bf16 output whose largest elements exceed
-about 5 rms: rounding the exact (float64) result of a Qwen-shaped layer at
-T=100 to bf16 alone gives max |diff| = 2.01e-2 * rms.
+Tolerance of floating outputs against the fp32 oracle: relative L2 <= 5e-3
+of the raw difference, and a max-abs bar of 2e-2 * rms(ref).  For fp32
+outputs (the routed SwiGLU vectors h) the max-abs bar is literal.  For bf16
+outputs it bounds the error beyond the output format's own rounding: for
+every element |got - ref| - half a bf16 ulp of max(|got|, |ref|) <= 2e-2 *
+rms(ref).  Read literally it cannot be met by any bf16 output whose largest
+elements exceed about 5 rms: rounding the exact (float64) result of a
+Qwen-shaped layer at T=100 to bf16 alone gives max |diff| = 2.01e-2 * rms.
+Both figures of every comparison are printed at the end of the session.
 Near ties: a token whose oracle K-th and (K+1)-th logits differ by less than
 1e-4 may be routed differently by an fp32 sum taken in another order; its ids
 are not compared, and its floats are checked on a run with the oracle's
@@ -67,12 +69,26 @@ def excess_stats(got, want):
     return float(max(ex.max(), 0.0) / max(rms, 1e-30))
 
 
-def assert_close(got, want, what=""):
+# every comparison made, for the session summary: (what, dtype, rel_l2,
+# literal max_abs/rms, beyond-rounding max_abs/rms)
+RECORDS = []
+
+
+def assert_close(got, want, what="", dtype="bf16"):
+    """The benchmark spec bar.  rel-L2 <= 5e-3 on the raw difference, always.
+    max-abs: for a bf16 output (dtype "bf16") the error beyond the output's
+    own rounding (half a bf16 ulp) must stay <= 2e-2 rms(ref); for an fp32
+    output (dtype "f32": no output rounding to set aside) the literal
+    max |got - ref| <= 2e-2 rms(ref).  Both max-abs figures are recorded and
+    printed at the end of the session."""
+    assert dtype in ("bf16", "f32")
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     rel, mx = err_stats(got, want)
     ex = excess_stats(got, want)
-    assert rel <= REL_L2 and ex <= MAX_ABS_RMS, \
-        f"{what}: rel_l2 {rel:.3e}, max_abs/rms {mx:.3e}, beyond bf16 rounding {ex:.3e}"
+    RECORDS.append((what, dtype, rel, mx, ex))
+    bar = mx if dtype == "f32" else ex
+    assert rel <= REL_L2 and bar <= MAX_ABS_RMS, \
+        f"{what} ({dtype}): rel_l2 {rel:.3e}, max_abs/rms {mx:.3e}, beyond bf16 rounding {ex:.3e}"
     return rel, mx
 
 

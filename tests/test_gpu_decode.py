@@ -196,7 +196,7 @@ def test_separate_calls(lib):
     h = torch.empty((T * K, I), dtype=torch.float32, device=G.dev())
     q.moe_expert_gate_up(dims, dl, x, offsets, perm, h, ws)
     href = ref["h"].reshape(T * K, I)[op]
-    G.assert_close(h.cpu().numpy(), href, "gate/up h")
+    G.assert_close(h.cpu().numpy(), href, "gate/up h", dtype="f32")
     y = torch.empty((T * K, dims.hidden), dtype=torch.int16, device=G.dev())
     q.moe_expert_ffn(dims, dl, x, offsets, perm, y, ws)
     yref = ref["y"].reshape(T * K, dims.hidden)[op]
@@ -321,8 +321,8 @@ def _stage_calls(dims, dl, x, ws, forced=None, ids=None):
 def test_stage_calls_equal_static_layer(lib):
     """moe_decode_route -> moe_decode_gate_up -> moe_decode_down_combine is
     the decode-kernel layer (moe_layer_forward_static), bit for bit, and
-    publishes the same routing; at T = 1 moe_layer_forward is that layer
-    too."""
+    publishes the same routing; where moe_layer_forward takes the persistent
+    kernel (or the decode kernels), it is that layer too."""
     dims = gen.QWEN
     planes, dl = layer(dims, 8)
     for T in (1, 9):
@@ -337,7 +337,7 @@ def test_stage_calls_equal_static_layer(lib):
         torch.cuda.synchronize()
         assert torch.equal(out_a, out_b) and torch.equal(ids_a, ids_b)
         assert q.moe_get_device_status(ws2) == q.STRATA_OK
-        if T <= q.moe_layer_decode_max_tokens():
+        if q.moe_layer_path(dims, T) in (q.PATH_PERSISTENT, q.PATH_DECODE):
             out_c = torch.empty_like(out_a)
             q.moe_layer_forward(dims, dl, x, out_c, ws2)
             torch.cuda.synchronize()
@@ -420,19 +420,20 @@ def test_stack_call_own_routing(lib):
 
 
 def test_layer_profile_kernels(lib):
+    """moe_layer_profile names the kernels of the path moe_layer_path reports:
+    one persistent kernel at decode sizes, the tcgen05 kernels above (the
+    bucketing fused into one kernel at T <= 32)."""
     dims = gen.QWEN
     _, dl = layer(dims, 0)
-    xb = qwen_x(1, 3)
-    ws = q.make_workspace(dims, 1, G.dev())
-    out = torch.empty((1, dims.hidden), dtype=torch.int16, device=G.dev())
-    prof = q.moe_layer_profile(dims, dl, G.u16(xb), out, ws)
-    assert list(prof) == list(q.PROFILE_DECODE)
-    assert all(v > 0 for v in prof.values())
-    # above the whole-layer switch: the tcgen05 kernels, bucketing fused at T <= 32
-    for T, names in ((16, q.PROFILE_PREFILL_SMALL), (64, q.PROFILE_PREFILL)):
+    want = {q.PATH_PERSISTENT: lambda T: q.PROFILE_PERSISTENT,
+            q.PATH_DECODE: lambda T: q.PROFILE_DECODE,
+            q.PATH_TC: lambda T: q.PROFILE_PREFILL_SMALL if T <= 32 else q.PROFILE_PREFILL}
+    assert q.moe_layer_path(dims, 1) == q.PATH_PERSISTENT
+    assert q.moe_layer_path(dims, 64) == q.PATH_TC
+    for T in (1, 16, 24, 64):
         xt = qwen_x(T, 4)
         wst = q.make_workspace(dims, T, G.dev())
         ot = torch.empty((T, dims.hidden), dtype=torch.int16, device=G.dev())
         prof = q.moe_layer_profile(dims, dl, G.u16(xt), ot, wst)
-        assert list(prof) == list(names)
+        assert list(prof) == list(want[q.moe_layer_path(dims, T)](T)), T
         assert all(v > 0 for v in prof.values())

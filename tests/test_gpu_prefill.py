@@ -175,7 +175,7 @@ def test_prefill_separate_calls(T):
     assert np.array_equal(perm.cpu().numpy(), op) and np.array_equal(inv.cpu().numpy(), oi)
     h = torch.empty((T * K, I), dtype=torch.float32, device=G.dev())
     q.moe_expert_gate_up(dims, dl, x, offsets, perm, h, ws)
-    G.assert_close(h.cpu().numpy(), ref["h"].reshape(T * K, I)[op], "gate/up h")
+    G.assert_close(h.cpu().numpy(), ref["h"].reshape(T * K, I)[op], "gate/up h", dtype="f32")
     y = torch.empty((T * K, H), dtype=torch.int16, device=G.dev())
     q.moe_expert_ffn(dims, dl, x, offsets, perm, y, ws)
     G.assert_close(G.bf16_to_np(y), ref["y"].reshape(T * K, H)[op], "expert y")
@@ -209,4 +209,5 @@ def test_prefill_stage_calls_reject_bad_offsets():
     ids = np.zeros((T, K), dtype=np.int32)
     ref = oracle.moe_forward(dims, planes, xb, ids=ids, w=np.full((T, K), 1.0 / K, np.float32),
                              want_h=True)
-    G.assert_close(h.cpu().numpy(), ref["h"].reshape(T * K, I), "valid expert beside bad offsets")
+    G.assert_close(h.cpu().numpy(), ref["h"].reshape(T * K, I), "valid expert beside bad offsets",
+                   dtype="f32")
