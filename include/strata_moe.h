@@ -32,8 +32,11 @@
  *     STRATA_OK and launches nothing.  A failed launch returns STRATA_ECUDA.
  *   - Kernels never trap.  A forced expert id outside [0, E) is skipped and
  *     latches STRATA_EBADROUTE in the workspace's error word; a bounded wait
- *     that runs out latches STRATA_ETIMEOUT.  moe_get_device_status reads and
- *     clears the word.
+ *     that runs out latches STRATA_ETIMEOUT; on the tensor-core path
+ *     (STRATA_PATH_TC), an activation, h or expert output whose fp16 operand
+ *     copy is not finite (|value| beyond 65504, or a non-finite input)
+ *     latches STRATA_ERANGE and the call's outputs are not to be used.
+ *     moe_get_device_status reads and clears the word.
  *   - Results are deterministic: ids, permutations and every floating sum are
  *     computed in a fixed order, with no floating-point atomics.
  *
@@ -79,7 +82,8 @@ typedef enum {
     STRATA_ECUDA = 2,         /* a CUDA launch or query failed             */
     STRATA_EUNSUPPORTED = 3,  /* valid request this build does not handle  */
     STRATA_ETIMEOUT = 4,      /* a bounded device wait ran out (latched)   */
-    STRATA_EBADROUTE = 5      /* a forced expert id was out of range (latched) */
+    STRATA_EBADROUTE = 5,     /* a forced expert id was out of range (latched) */
+    STRATA_ERANGE = 6         /* a tensor-core fp16 operand overflowed (latched) */
 } strata_status;
 
 typedef struct {
@@ -315,9 +319,11 @@ STRATA_API strata_status moe_decode_down_combine(const strata_moe_dims* dims,
  *     moe_decode_max_tokens() and the decode kernels' part of the workspace
  *     <= 2 MiB (every decode T of the 2048-hidden, 256-expert, top-8 shape
  *     fits); a larger request returns STRATA_EINVAL with nothing launched.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.  No call allocates or frees anything.
+ *   - Every call looks up the array's device address in the current
+ *     device's context (cudaGetSymbolAddress; nothing cached, so a context
+ *     made again after cudaDeviceReset gets its own copy).  The first call on
+ *     a device loads the library's kernels there: make it before any stream
+ *     capture.  No call allocates or frees anything.
  *   - Calls that may overlap on the GPU (several streams, or several host
  *     threads on one device) race on the shared array and give wrong results:
  *     serialise them, or use moe_layer_forward with one workspace each.
@@ -336,8 +342,8 @@ STRATA_API strata_status moe_layer_forward_static(const strata_moe_dims* dims,
  * every kernel launch, synchronises `stream`, and writes each kernel's
  * duration in microseconds to us[0..max_n) in launch order; *n_out gets the
  * number of kernels.  The events serialise the kernels, so each duration is
- * the kernel alone.  Order: decode kernels (T <= moe_layer_decode_max_tokens(),
- * three of them): route, gate/up, down+combine; tcgen05 kernels (nine):
+ * the kernel alone.  Order, by moe_layer_path: the persistent kernel (one);
+ * the decode kernels (three): route, gate/up, down+combine; tcgen05 kernels (nine):
  * router GEMM, top-K, count, scan, scatter, gather, gate/up GEMM, down GEMM,
  * combine -- seven at T <= 32, where count, scan and scatter are one
  * bucketing kernel. */

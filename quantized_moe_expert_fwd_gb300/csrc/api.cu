@@ -2,7 +2,6 @@
 // dispatch to the decode (GEMV) or prefill (tcgen05 GEMM) kernels.
 #include <atomic>
 #include <cstring>
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -39,7 +38,7 @@ WsLayout ws_layout(const strata_moe_dims& d, int T) {
         L.hs = take(t * Is * 4);
     }
     L.decode_end = o;
-    if (T <= kPersistMaxTokens) {
+    if (T <= kPersistTokensCap) {
         L.ll_logits = take(t * (E + 1) * 8);
         L.ll_hs = take(t * Is * 8);
         L.ll_h = take(t * K * I * 8);
@@ -379,7 +378,8 @@ strata_status pf_gate_up(const strata_moe_dims* d, const strata_moe_layer* L, co
     STRATA_TRY(launch_prefill_blocks(offsets, T, d->top_k, d->n_experts, 0,
                                      const_cast<MBlock*>(p.mblocks),
                                      const_cast<int32_t*>(p.n_mblocks), p.err, s));
-    STRATA_TRY(launch_prefill_gather(p.x, perm, T, d->top_k, d->hidden, p.xg, p.xg_rows, s));
+    STRATA_TRY(launch_prefill_gather(p.x, perm, T, d->top_k, d->hidden, p.xg, p.xg_rows, p.err,
+                                     s));
     STRATA_TRY(launch_prefill_gate_up(p, s));
     return STRATA_OK;
 }
@@ -507,7 +507,7 @@ size_t moe_workspace_bytes(const strata_moe_dims* dims, int32_t max_tokens) {
     if (!dims_ok(dims) || max_tokens < 1) return 0;
     // a call with T <= max_tokens takes the persistent, the decode or the
     // prefill layout; each grows with T
-    const int pmax = max_tokens < kPersistMaxTokens ? max_tokens : kPersistMaxTokens;
+    const int pmax = max_tokens < kPersistTokensCap ? max_tokens : kPersistTokensCap;
     const int dmax = max_tokens < kDecodeMaxTokens ? max_tokens : kDecodeMaxTokens;
     size_t n = ws_layout(*dims, pmax).total;
     const size_t a = ws_layout(*dims, dmax).total, b = ws_layout(*dims, max_tokens).total;
@@ -664,7 +664,8 @@ strata_status moe_expert_down(const strata_moe_dims* dims, const strata_moe_laye
         if (!prefill_supported(*dims)) return STRATA_EUNSUPPORTED;
         const WsLayout W = ws_layout(*dims, T);
         STRATA_TRY(launch_prefill_pack(h_dev, (long long)T * dims->top_k * dims->inter,
-                                       at<__half>(ws_dev, W.h16), s));
+                                       at<__half>(ws_dev, W.h16), &at<Ctl>(ws_dev, W.ctl)->err,
+                                       s));
         return pf_down(dims, layer, T, offsets_dev, true, y_dev, ws_dev, s);
     }
     const WsLayout W = ws_layout(*dims, T);
@@ -735,7 +736,7 @@ strata_status moe_combine(const strata_moe_dims* dims, const strata_moe_layer* l
         STRATA_TRY(launch_prefill_blocks(nullptr, T, dims->top_k, dims->n_experts, 1,
                                          const_cast<MBlock*>(p.mblocks),
                                          const_cast<int32_t*>(p.n_mblocks), p.err, s));
-        STRATA_TRY(launch_prefill_gather(p.x, nullptr, T, 0, dims->hidden, p.xg, T, s));
+        STRATA_TRY(launch_prefill_gather(p.x, nullptr, T, 0, dims->hidden, p.xg, T, p.err, s));
         STRATA_TRY(launch_prefill_gate_up(p, s));
         STRATA_TRY(launch_prefill_down(p, s));
         STRATA_TRY(launch_prefill_combine(nullptr, static_cast<const uint16_t*>(y_dev), p.ysh,
@@ -1022,6 +1023,7 @@ const char* strata_status_str(strata_status s) {
         case STRATA_EUNSUPPORTED: return "STRATA_EUNSUPPORTED: not handled by this build";
         case STRATA_ETIMEOUT: return "STRATA_ETIMEOUT: a bounded device wait ran out";
         case STRATA_EBADROUTE: return "STRATA_EBADROUTE: expert id out of range";
+        case STRATA_ERANGE: return "STRATA_ERANGE: a value left the fp16 operand range";
     }
     return "unknown strata_status";
 }
@@ -1041,20 +1043,14 @@ namespace {
 constexpr size_t kStaticWsBytes = size_t(2) << 20;
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
-// The array's device address, looked up once per device with that device
-// current (host code may not use the symbol itself as a device pointer).
+// The array's device address in the current device's context, looked up on
+// every call (host code may not use the symbol itself as a device pointer).
+// Nothing is cached, so a context torn down and made again (cudaDeviceReset)
+// gets the address of its own copy of the array.
 void* static_ws_address() {
-    static std::mutex mu;
-    static void* addr[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess) return nullptr;
+    return p;
 }
 
 }  // namespace

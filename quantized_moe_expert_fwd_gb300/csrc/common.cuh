@@ -19,6 +19,11 @@ __device__ __forceinline__ void latch(uint32_t* err, uint32_t code) {
     atomicCAS(err, 0u, code);
 }
 
+// Nonzero when either fp16 half of w has an all-ones exponent (inf or NaN).
+__device__ __forceinline__ uint32_t f16x2_not_finite(uint32_t w) {
+    return uint32_t((w & 0x7c00u) == 0x7c00u) | uint32_t((w & 0x7c000000u) == 0x7c000000u);
+}
+
 // A bounded wait ran out: latch STRATA_ETIMEOUT and record where (the first
 // one only).  `err` points at Ctl::err.
 __device__ __forceinline__ void latch_timeout(uint32_t* err, uint32_t site, uint32_t slot,

@@ -134,7 +134,13 @@ cudaError_t launch_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x,
 // ------------------------------------------------ persistent decode layers
 // A whole decode-size layer (or a stack of residual layers) as one launch of
 // one CTA per SM (persist.cu).
-constexpr int kPersistMaxTokens = 16;     // tokens a call it takes
+// Tokens a whole-layer call it takes.  Measured on GB300 at the 2048-hidden,
+// 256-expert, top-8 shape (ten layers rotating, CUDA graph): T = 1 27.4 us
+// against 32.2 on the three decode kernels; T = 2 47.0 against 45.5; T = 3..6
+// 59..129 against 48..62 on the tcgen05 kernels.  The kernel itself takes up
+// to kPersistTokensCap tokens (the shared memory decides above a few).
+constexpr int kPersistMaxTokens = 1;
+constexpr int kPersistTokensCap = 16;
 constexpr int kMaxGrid = 1024;            // grid barrier flags in the workspace
 constexpr int kPxMaxLayers = 40;          // layers one launch carries
 // 1 producer + 15 consumer warps (128 registers a thread): the int4 dot
@@ -268,9 +274,10 @@ cudaError_t launch_prefill_blocks(const int32_t* offsets, int T, int K, int E, i
                                   cudaStream_t s);
 // xg rows: the T*K routed slots (token perm[row] / K), then the T tokens
 cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, int T, int K, int H,
-                                  __half* xg, int rows, cudaStream_t s);
+                                  __half* xg, int rows, uint32_t* err, cudaStream_t s);
 // fp32 [n] -> fp16 in the operand order (n a multiple of 8)
-cudaError_t launch_prefill_pack(const float* src, long long n, __half* dst, cudaStream_t s);
+cudaError_t launch_prefill_pack(const float* src, long long n, __half* dst, uint32_t* err,
+                                cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const PfExperts& p, cudaStream_t s);
 cudaError_t launch_prefill_down(const PfExperts& p, cudaStream_t s);
 // gather + gate/up + down of the routed experts and the shared one

@@ -968,7 +968,9 @@ PxFn px_kernel(int MC) { return MC == 1 ? k_persist<1> : k_persist<2>; }
 bool px_geometry(const strata_moe_dims& d, int T, bool forced, bool resid, int G, PxGeo* g) {
     const int H = d.hidden, E = d.n_experts, K = d.top_k, I = d.inter, Is = d.shared_inter;
     *g = PxGeo{};
-    if (T < 1 || T > kPersistMaxTokens || H > 2048 || G < 1 || G > kMaxGrid) return false;
+    if (T < 1 || T > kPersistMaxTokens || T > kPersistTokensCap || H > 2048 || G < 1 ||
+        G > kMaxGrid)
+        return false;
     const int MC = H <= 1024 ? 1 : 2;
     const int q = 256 / (I < Is ? I : Is) > 1 ? 256 / (I < Is ? I : Is) : 1;
     int R = (H + G - 1) / G;

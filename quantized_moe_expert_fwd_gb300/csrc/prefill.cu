@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int T, i
 constexpr int kGatherPer = 4;
 
 __global__ void k_pf_gather(const uint16_t* x, const int32_t* perm, int T, int K, int H,
-                            __half* xg, int nrows) {
+                            __half* xg, int nrows, uint32_t* err) {
     pdl_launch();
     pdl_wait();
     const int gq = H / (8 * kGatherPer);               // groups in a quarter row
@@ -450,6 +450,7 @@ __global__ void k_pf_gather(const uint16_t* x, const int32_t* perm, int T, int K
     for (int q = 0; q < kGatherPer; ++q)
         v[q] = t >= 0 ? __ldg(reinterpret_cast<const uint4*>(x + size_t(t) * H) + g0 + q * gq)
                       : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t inf_nan = 0u;       // an fp16 result with an all-ones exponent
 #pragma unroll
     for (int q = 0; q < kGatherPer; ++q) {
         uint4 out = make_uint4(0u, 0u, 0u, 0u);
@@ -470,13 +471,16 @@ __global__ void k_pf_gather(const uint16_t* x, const int32_t* perm, int T, int K
                              *reinterpret_cast<const uint32_t*>(&h1),
                              *reinterpret_cast<const uint32_t*>(&h2),
                              *reinterpret_cast<const uint32_t*>(&h3));
+            inf_nan |= f16x2_not_finite(out.x) | f16x2_not_finite(out.y) |
+                       f16x2_not_finite(out.z) | f16x2_not_finite(out.w);
         }
         reinterpret_cast<uint4*>(xg + size_t(row) * H)[g0 + q * gq] = out;
     }
+    if (inf_nan != 0u) latch(err, STRATA_ERANGE);
 }
 
 // fp32 -> fp16 in the operand order, 8 elements a thread.
-__global__ void k_pf_pack(const float* src, long long n8, __half* dst) {
+__global__ void k_pf_pack(const float* src, long long n8, __half* dst, uint32_t* err) {
     pdl_launch();
     pdl_wait();
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -487,10 +491,14 @@ __global__ void k_pf_pack(const float* src, long long n8, __half* dst) {
     const __half2 h1 = __floats2half2_rn(a.y, b.y);
     const __half2 h2 = __floats2half2_rn(a.z, b.z);
     const __half2 h3 = __floats2half2_rn(a.w, b.w);
-    reinterpret_cast<uint4*>(dst)[i] = make_uint4(*reinterpret_cast<const uint32_t*>(&h0),
-                                                  *reinterpret_cast<const uint32_t*>(&h1),
-                                                  *reinterpret_cast<const uint32_t*>(&h2),
-                                                  *reinterpret_cast<const uint32_t*>(&h3));
+    const uint4 out = make_uint4(*reinterpret_cast<const uint32_t*>(&h0),
+                                 *reinterpret_cast<const uint32_t*>(&h1),
+                                 *reinterpret_cast<const uint32_t*>(&h2),
+                                 *reinterpret_cast<const uint32_t*>(&h3));
+    reinterpret_cast<uint4*>(dst)[i] = out;
+    if ((f16x2_not_finite(out.x) | f16x2_not_finite(out.y) | f16x2_not_finite(out.z) |
+         f16x2_not_finite(out.w)) != 0u)
+        latch(err, STRATA_ERANGE);
 }
 
 // out[t] = bf16( sum_k w[t][k] y[inv[t*K+k]] + sig[t] y_sh[t] ), 8 columns
@@ -898,19 +906,21 @@ cudaError_t launch_prefill_blocks(const int32_t* offsets, int T, int K, int E, i
 }
 
 cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, int T, int K, int H,
-                                  __half* xg, int rows, cudaStream_t s) {
+                                  __half* xg, int rows, uint32_t* err, cudaStream_t s) {
     if (H % (8 * kGatherPer) != 0) return cudaErrorInvalidValue;
     const long long n = (long long)rows * (H / (8 * kGatherPer));
-    return launch_pdl(k_pf_gather, int((n + 255) / 256), 256, 0, s, x, perm, T, K, H, xg, rows);
+    return launch_pdl(k_pf_gather, int((n + 255) / 256), 256, 0, s, x, perm, T, K, H, xg, rows,
+                      err);
 }
 
-cudaError_t launch_prefill_pack(const float* src, long long n, __half* dst, cudaStream_t s) {
+cudaError_t launch_prefill_pack(const float* src, long long n, __half* dst, uint32_t* err,
+                                cudaStream_t s) {
     const long long n8 = n / 8;
-    return launch_pdl(k_pf_pack, int((n8 + 255) / 256), 256, 0, s, src, n8, dst);
+    return launch_pdl(k_pf_pack, int((n8 + 255) / 256), 256, 0, s, src, n8, dst, err);
 }
 
 cudaError_t launch_prefill_experts(const PfExperts& p, cudaStream_t s) {
-    cudaError_t e = launch_prefill_gather(p.x, p.perm, p.T, p.K, p.H, p.xg, p.xg_rows, s);
+    cudaError_t e = launch_prefill_gather(p.x, p.perm, p.T, p.K, p.H, p.xg, p.xg_rows, p.err, s);
     if (e != cudaSuccess) return e;
     e = launch_prefill_gate_up(p, s);
     if (e != cudaSuccess) return e;

@@ -457,6 +457,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                     tmem_ld_wait();
                 }
                 const int nv = min(32, nrows - c0);
+                uint32_t inf_nan = 0u;    // an fp16 operand left the finite range
                 if (MODE == kGemmGateUp) {
                     // rows 2i (gate) and 2i + 1 (up) are lanes l and l + 1, each
                     // with every token.  One exchange per token pair gives the
@@ -478,7 +479,9 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                         const float gt = odd ? other : keep, up = odd ? keep : other;
                         if (j + odd < nv) {
                             const float h = __fdividef(gt, 1.0f + __expf(-gt)) * up;
-                            hb[size_t(j) * ld] = __float2half_rn(h);
+                            const __half hh = __float2half_rn(h);
+                            inf_nan |= f16x2_not_finite(__half_as_ushort(hh));
+                            hb[size_t(j) * ld] = hh;
                             if (hf != nullptr) hf[size_t(j) * ld] = h;
                         }
                     }
@@ -495,9 +498,14 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                         __half* yh = (sh ? a.out2_f16 : a.out_f16) + r0;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (j < nv) yh[j * ld] = __float2half_rn(__uint_as_float(v[j]));
+                            if (j < nv) {
+                                const __half yv = __float2half_rn(__uint_as_float(v[j]));
+                                inf_nan |= f16x2_not_finite(__half_as_ushort(yv));
+                                yh[j * ld] = yv;
+                            }
                     }
                 }
+                if (inf_nan != 0u) latch(a.err, STRATA_ERANGE);
             }
             tc_fence_before();
             mbar_arrive(&acc_empty[dbuf]);

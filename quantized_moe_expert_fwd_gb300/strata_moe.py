@@ -17,7 +17,7 @@ import torch
 from . import build as _build
 
 STRATA_OK, STRATA_EINVAL, STRATA_ECUDA, STRATA_EUNSUPPORTED, STRATA_ETIMEOUT, \
-    STRATA_EBADROUTE = range(6)
+    STRATA_EBADROUTE, STRATA_ERANGE = range(7)
 
 _lock = threading.Lock()
 _lib = None
@@ -161,6 +161,18 @@ class DeviceLayer:
             self.tensors[n] = t
         self.ptrs = LayerPtrs(*[(None if self.tensors[n] is None else self.tensors[n].data_ptr())
                                 for n in _LAYER_FIELDS])
+
+    def with_bias(self, bias, device="cuda") -> "DeviceLayer":
+        """The same resident planes with another router bias (fp32 [E] array,
+        or None): no plane is copied again."""
+        other = DeviceLayer.__new__(DeviceLayer)
+        other.tensors = dict(self.tensors)
+        other.tensors["router_bias"] = (None if bias is None else
+                                        torch.from_numpy(np.ascontiguousarray(bias, dtype=np.float32))
+                                        .to(device))
+        other.ptrs = LayerPtrs(*[(None if other.tensors[n] is None else other.tensors[n].data_ptr())
+                                 for n in _LAYER_FIELDS])
+        return other
 
     def nbytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in self.tensors.values() if t is not None)

@@ -94,3 +94,15 @@ def assert_close(got, want, what="", dtype="bf16"):
 
 def clear_tokens(gap):
     return [t for t in range(len(gap)) if not (gap[t] < NEAR_TIE)]
+
+
+def leading_clear_layers(recs, bar):
+    """Per token, how many layers of an oracle stack record it passes, from
+    the first, with its routing gap at or above `bar` (no near tie)."""
+    gaps = np.stack([np.asarray(rec["gap"]) for rec in recs])      # [L][T]
+    clear = gaps >= bar
+    n = np.zeros(gaps.shape[1], dtype=np.int64)
+    for t in range(gaps.shape[1]):
+        while n[t] < gaps.shape[0] and clear[n[t], t]:
+            n[t] += 1
+    return n

@@ -75,8 +75,10 @@ def test_workspace_bytes(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert q.strata_status_str(s).startswith("STRATA_")
+    assert q.strata_status_str(q.STRATA_ERANGE).startswith("STRATA_ERANGE")
+    assert q.strata_status_str(7).startswith("unknown")
 
 
 def test_invalid_arguments_return_einval_without_launching(lib):

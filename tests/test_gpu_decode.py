@@ -286,14 +286,19 @@ def test_block_forward_stack(lib):
     torch.cuda.synchronize()
     assert q.moe_get_device_status(ws) == q.STRATA_OK
     G.assert_close(resid.cpu().numpy(), rref, "4-block stack, forced routing")
-    # free-running: ids agree block by block while no near tie was met
+    # free-running: a token that meets no near tie in any block routes as the
+    # oracle does and ends within tolerance of it (tokens are independent);
+    # the seeds give at least one such token
+    n_tok = G.leading_clear_layers(recs, 1e-3)
+    rows = [t for t in range(T) if n_tok[t] == len(layers)]
+    assert rows, "every token meets a near tie: pick other seeds"
     resid = G.f32(r0)
     for li, (_, dl) in enumerate(layers):
         x_out = torch.empty((T, dims.hidden), dtype=torch.int16, device=G.dev())
         q.moe_block_forward(dims, dl, resid, ws, eps=1e-6, x_out=x_out)
     torch.cuda.synchronize()
-    if all(np.all(rec["gap"] >= 1e-3) for rec in recs):
-        G.assert_close(resid.cpu().numpy(), rref, "4-block stack, own routing")
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+    G.assert_close(resid.cpu().numpy()[rows], rref[rows], f"4-block stack, own routing, {rows}")
 
 
 def _static(lib, dims, dl, x, out, ids=None):

@@ -115,12 +115,31 @@ def test_stack_40_layers_stack_call(T):
     torch.cuda.synchronize()
     assert q.moe_get_device_status(ws) == q.STRATA_OK
     G.assert_close(resid.cpu().numpy() - r0, rref - r0, f"40-layer stack T={T}, stack call")
-    n_ok = 0
-    while n_ok < len(recs) and np.all(recs[n_ok]["gap"] >= 3e-3):
-        n_ok += 1
-    if n_ok:
-        resid = G.f32(r0)
-        q.moe_stack_forward(dims, layers[:n_ok], resid, ws, eps=1e-6)
-        torch.cuda.synchronize()
-        want = r0 + sum(oracle.bf16_array_to_f32(recs[i]["out_bf16"]) for i in range(n_ok))
-        G.assert_close(resid.cpu().numpy() - r0, want - r0, f"{n_ok} layers, own routing")
+    # own routing: a token whose top-K gap stays clear (>= 3e-3) over its
+    # leading layers routes there as the oracle does.  Over the longest such
+    # run of any token (at least one layer, by the seeds), the stack call with
+    # its own routing must then equal, on those tokens, the same call with the
+    # oracle's routing forced -- up to the weights' last bits (the forced
+    # weights are the oracle's); one expert chosen differently moves a row by
+    # a tenth of its norm or more.  Tokens are independent, so the others are
+    # free to differ.
+    # Tiny differences grow along the stack when each layer routes by itself
+    # (the softmax weights follow the drifted logits: measured 3.7e-3 relative
+    # after 15 layers of the tcgen05 path with the same ids), so the run is
+    # capped at 8 layers, where that drift is ~1e-4 and a changed expert
+    # still shows at the percent level.
+    n_tok = G.leading_clear_layers(recs, 3e-3)
+    n_ok = min(int(n_tok.max()), 8)
+    assert n_ok >= 1, "every token meets a near tie in the first layer: pick another seed"
+    rows = [t for t in range(T) if n_tok[t] >= n_ok]
+    own = G.f32(r0)
+    q.moe_stack_forward(dims, layers[:n_ok], own, ws, eps=1e-6)
+    forced = G.f32(r0)
+    q.moe_stack_forward(dims, layers[:n_ok], forced, ws, eps=1e-6, ids=G.i32(ids[:n_ok]),
+                        weights=G.f32(w[:n_ok]))
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+    d_own = own.cpu().numpy()[rows] - r0[rows]
+    d_forced = forced.cpu().numpy()[rows] - r0[rows]
+    rel = float(np.linalg.norm(d_own - d_forced) / np.linalg.norm(d_forced))
+    assert rel <= 1e-3, f"{n_ok} layers, tokens {rows}: own routing off forced by {rel:.2e}"

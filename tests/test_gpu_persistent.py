@@ -155,6 +155,8 @@ def test_stack_bit_identical_to_kernel_chain(lib, T):
     separate kernels: moe_rmsnorm, then the three decode stages with the
     residual add, layer after layer."""
     dims = gen.QWEN
+    if q.moe_layer_path(dims, T) != q.PATH_PERSISTENT:
+        pytest.skip(f"T={T}: the stack takes the other kernels")
     layers = [layer(dims, 50 + i)[1] for i in range(6)]
     r0 = G.f32(gen.draw_tokens(dims, T, 60 + T, "resid"))
     ra = r0.clone()
@@ -177,7 +179,7 @@ def test_stack_bit_identical_to_kernel_chain(lib, T):
 def test_block_forward_bit_identical(lib):
     dims = gen.QWEN
     _, dl = layer(dims, 55)
-    T = 3
+    T = 1
     r0 = G.f32(gen.draw_tokens(dims, T, 77, "resid"))
     ra, rb = r0.clone(), r0.clone()
     xa = zeros_i16(T, dims.hidden)
@@ -316,7 +318,8 @@ def test_wait_for_another_cta_runs_out(lib):
     right again."""
     dims = gen.QWEN
     _, dl = layer(dims, 32)
-    T = 4
+    T = 1
+    assert q.moe_layer_path(dims, T) == q.PATH_PERSISTENT
     x = G.u16(qwen_x(T, 1234))
     ws = q.make_workspace(dims, T, G.dev())
     good, _, _, _ = persistent_layer(dims, dl, x, ws)

@@ -211,3 +211,41 @@ def test_prefill_stage_calls_reject_bad_offsets():
                              want_h=True)
     G.assert_close(h.cpu().numpy(), ref["h"].reshape(T * K, I), "valid expert beside bad offsets",
                    dtype="f32")
+
+
+@pytest.mark.parametrize("scale,what", [(1e5, "x"), (300.0, "h")])
+def test_tc_path_latches_erange_on_fp16_overflow(scale, what):
+    """The tensor-core path holds activations, h and expert outputs as fp16
+    operands.  Scaled inputs whose fp16 copy (x * 1e5: |x| up to ~5e5) or
+    whose h (x * 300: the oracle's fp32 h far beyond 65504) leaves the finite
+    fp16 range latch STRATA_ERANGE; the unscaled input passes clean, and the
+    same scaled token through the persistent decode kernel (fp32 h) does too."""
+    dims = gen.QWEN
+    planes, dl = layer(dims, 7)
+    T = 40
+    x0 = oracle.rmsnorm(gen.draw_tokens(dims, T, 91, "resid"))
+    xf = oracle.bf16_array_to_f32(x0) * np.float32(scale)
+    xb = oracle.round_bf16(xf)
+    if what == "x":
+        assert np.abs(xf).max() > 65504.0
+    else:
+        assert np.abs(xf).max() < 60000.0
+        ref = oracle.moe_forward(dims, planes, xb[:4], want_h=True)
+        assert np.abs(ref["h"]).max() > 7e4
+    out = torch.empty((T, dims.hidden), dtype=torch.int16, device=G.dev())
+    ws = q.make_workspace(dims, T, G.dev())
+    assert q.moe_layer_path(dims, T) == q.PATH_TC
+    q.moe_layer_forward(dims, dl, G.u16(x0), out, ws)
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+    q.moe_layer_forward(dims, dl, G.u16(xb), out, ws)
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_ERANGE
+    # the word was cleared by the read: the next clean call reports OK
+    q.moe_layer_forward(dims, dl, G.u16(x0), out, ws)
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_OK
+    one = torch.empty((1, dims.hidden), dtype=torch.int16, device=G.dev())
+    q.moe_layer_forward(dims, dl, G.u16(xb[:1]), one, ws)
+    torch.cuda.synchronize()
+    assert q.moe_get_device_status(ws) == q.STRATA_OK

@@ -5,7 +5,9 @@ fixed workspace inside the library instead of one the caller passes.
 
 Checked through the C ABI against moe_layer_forward with a caller-allocated
 workspace, on two calls in a row (the second one reuses the array the first
-one left behind), within the tolerance of the other GPU tests.  This file is
+one left behind), within the tolerance of the other GPU tests; around the
+second call the device's free memory (cudaMemGetInfo) and torch's allocated
+bytes stay exactly as they were.  This file is
 collected last so that a run stopping at its first failure has run every
 other test already; it also passes alone in a fresh process.
 """
@@ -44,8 +46,16 @@ def test_static_workspace_matches_caller_workspace_twice():
         ws = q.make_workspace(dims, T, G.dev())
         q.moe_layer_forward(dims, dl, x, want, ws)
         got = torch.full((T, dims.hidden), -1, dtype=torch.int16, device=G.dev())
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        held0 = torch.cuda.memory_allocated()
         assert _call_static(lib, dims, dl, x, got) == q.STRATA_OK
         torch.cuda.synchronize()
+        if call > 0:
+            # the second call: the array and its kernels are in place, and
+            # neither the device's free memory nor torch's allocator moved
+            assert torch.cuda.mem_get_info()[0] == free0
+            assert torch.cuda.memory_allocated() == held0
         g, w = G.bf16_to_np(got), G.bf16_to_np(want)
         G.assert_close(g, w, f"static workspace, call {call + 1}")
         assert q.moe_get_device_status(ws) == q.STRATA_OK
