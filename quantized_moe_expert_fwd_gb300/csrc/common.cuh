@@ -10,7 +10,7 @@ constexpr int kWarp = 32;
 
 // Workspace control block (offset 0 of every workspace).
 struct Ctl {
-    uint32_t err;       // latched strata_status (first error wins)
+    uint32_t err;       // latched strata_status (first error wins; a timeout replaces it)
     uint32_t where[7];  // first timed-out wait: site, block, warp, slot, round, item, 1
     uint32_t pad[56];
 };
@@ -19,16 +19,39 @@ __device__ __forceinline__ void latch(uint32_t* err, uint32_t code) {
     atomicCAS(err, 0u, code);
 }
 
+// latch() from the lowest lane of `bad` (a ballot of the lanes that hit the
+// condition), skipped once the word holds a code: many threads that meet
+// the same condition send one atomic a warp, not one each, to one address.
+__device__ __forceinline__ void latch_warp(uint32_t* err, uint32_t code, uint32_t bad) {
+    if (bad != 0u && int(threadIdx.x & 31) == __ffs(bad) - 1 &&
+        *reinterpret_cast<const volatile uint32_t*>(err) == 0u)
+        atomicCAS(err, 0u, code);
+}
+
 // Nonzero when either fp16 half of w has an all-ones exponent (inf or NaN).
 __device__ __forceinline__ uint32_t f16x2_not_finite(uint32_t w) {
     return uint32_t((w & 0x7c00u) == 0x7c00u) | uint32_t((w & 0x7c000000u) == 0x7c000000u);
 }
+// w with each infinite half replaced by the largest finite value of its sign
+// (+-65504) and each NaN by 0: tensor-core operands stay finite.
+__device__ __forceinline__ uint32_t f16x2_saturate(uint32_t w) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint32_t h = (w >> (16 * k)) & 0xffffu;
+        if ((h & 0x7c00u) == 0x7c00u) {
+            const uint32_t f = (h & 0x03ffu) != 0u ? 0u : ((h & 0x8000u) | 0x7bffu);
+            w = (w & ~(0xffffu << (16 * k))) | (f << (16 * k));
+        }
+    }
+    return w;
+}
 
-// A bounded wait ran out: latch STRATA_ETIMEOUT and record where (the first
-// one only).  `err` points at Ctl::err.
+// A bounded wait ran out: latch STRATA_ETIMEOUT over any code latched
+// before (the waits that give up early look for that code) and record where
+// (the first one only).  `err` points at Ctl::err.
 __device__ __forceinline__ void latch_timeout(uint32_t* err, uint32_t site, uint32_t slot,
                                               uint32_t round, uint32_t item) {
-    atomicCAS(err, 0u, 4u /* STRATA_ETIMEOUT */);
+    atomicExch(err, 4u /* STRATA_ETIMEOUT */);
     uint32_t* w = err + 1;
     if (atomicCAS(&w[6], 0u, 1u) == 0u) {
         w[0] = site;
@@ -195,6 +218,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n)
+                 : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -247,6 +274,14 @@ __device__ __forceinline__ int lds_s32(uint32_t a) {
     int v;
     asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
+}
+
+// Brings [src, src + bytes) into L2 (16-byte aligned, a multiple of 16
+// bytes); no data moves to the SM and nothing waits for it.  L2 is the
+// point of coherence, so a prefetch made before another kernel's writes
+// land never hides them.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // dst, src 16-byte aligned; bytes a multiple of 16

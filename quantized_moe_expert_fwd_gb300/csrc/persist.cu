@@ -367,6 +367,81 @@ __device__ void px_stage_h(const uint64_t* hr, const uint64_t* hs, uint32_t tag,
     }
 }
 
+// Top-K of one token by every consumer thread (the order: larger key first,
+// the lower id among equal keys -- a strict total order, so the K picks are
+// the keys of rank 0 .. K-1), written in ascending id to ids[0..K) with the
+// softmax weights, in the same arithmetic as select_topk_keys.  Lk: the E
+// order-preserving keys; scratch: (E / 32 + 1) * K * 2 + 3 * K words.
+//   1. a key ranked K or later in its group of 32 is ranked K or later
+//      overall: each group keeps its K best as candidates;
+//   2. each candidate's rank among all candidates (four lanes a candidate);
+//   3. the K picks ordered by id, their softmax.
+__device__ void px_select_all(int E, int K, const uint32_t* Lk, uint32_t* scratch, int* ids,
+                              float* w, int ctid, int nthr) {
+    const int lane = ctid & 31, cw = ctid >> 5, nw = nthr >> 5;
+    const int ng = (E + 31) >> 5, nc = ng * K;
+    uint32_t* ck = scratch;
+    int* ci = reinterpret_cast<int*>(ck + nc);
+    uint32_t* sk = reinterpret_cast<uint32_t*>(ci + nc);
+    int* si = reinterpret_cast<int*>(sk + K);
+    float* ex = reinterpret_cast<float*>(si + K);
+    for (int g = cw; g < ng; g += nw) {
+        const int e = g * 32 + lane;
+        const uint32_t k = e < E ? Lk[e] : 0u;     // past E: key 0 and the largest ids
+        int r = 0;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const uint32_t ku = __shfl_sync(0xffffffffu, k, u);
+            r += (ku > k || (ku == k && u < lane)) ? 1 : 0;
+        }
+        if (r < K) {
+            ck[g * K + r] = k;
+            ci[g * K + r] = e;
+        }
+    }
+    px_cbar();
+    constexpr int kSplit = 4;
+    const int per = nthr / kSplit;
+    for (int c0 = 0; c0 < nc; c0 += per) {
+        const int c = c0 + ctid / kSplit;
+        uint32_t k = 0u;
+        int id = 0x7fffffff, r = 0;
+        if (c < nc) {
+            k = ck[c];
+            id = ci[c];
+            for (int d = ctid % kSplit; d < nc; d += kSplit) {
+                const uint32_t kd = ck[d];
+                r += (kd > k || (kd == k && ci[d] < id)) ? 1 : 0;
+            }
+        }
+        r += __shfl_xor_sync(0xffffffffu, r, 1);
+        r += __shfl_xor_sync(0xffffffffu, r, 2);
+        if (c < nc && ctid % kSplit == 0 && r < K) {
+            sk[r] = k;
+            si[r] = id;
+        }
+    }
+    px_cbar();
+    if (cw == 0) {
+        const uint32_t k = lane < K ? sk[lane] : 0u;
+        const int id = lane < K ? si[lane] : 0x7fffffff;
+        int pos = 0;
+        for (int j = 0; j < K; ++j) pos += (__shfl_sync(0xffffffffu, id, j) < id) ? 1 : 0;
+        const float m = __shfl_sync(0xffffffffu, key_logit(k), 0);   // rank 0: the largest
+        float e_k = 0.0f;
+        if (lane < K) {
+            e_k = expf(key_logit(k) - m);
+            ex[pos] = e_k;
+            ids[pos] = id;
+        }
+        __syncwarp();
+        float sum = 0.0f;
+        for (int p = 0; p < K; ++p) sum += ex[p];                      // ascending id
+        if (lane < K) w[pos] = e_k / sum;
+        __syncwarp();
+    }
+}
+
 // Down rows [r0, r1) of this CTA's rows of one unit (length L, packed bytes
 // at sq, scales at ss, shared memory) for each slot s0 .. s0+scount-1 whose
 // h row (fp32, chunk-interleaved, shared memory) is at hb + s * L * 4 bytes:
@@ -441,6 +516,11 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
     const int NC = H >> 5;
     const int R = a.R, o0 = b * R;
     const int nrow = max(0, min(R, H - o0));
+    // down products: a task is one pass of a warp over one unit (RPW rows,
+    // 32 / chunks-per-row); every unit has max(1, passes) tasks, each
+    // arriving once on the unit's empty barrier
+    const int rpw_r = 32 / (I >> 5), rpw_s = 32 / (Is >> 5);
+    const int np_r = max(1, (nrow + rpw_r - 1) / rpw_r), np_s = max(1, (nrow + rpw_s - 1) / rpw_s);
     const int Sg = a.gu_stages, Sd = a.dn_stages;
     const int nR = a.forced_ids ? 1 : E + 1;
     const uint32_t base = smem_u32(px);
@@ -457,7 +537,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         mbar_init(&plan_free, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sd_full[i], 1);
-            mbar_init(&sd_empty[i], 2);               // two warps, a half each
+            mbar_init(&sd_empty[i], np_s);            // one arrival a task
         }
         for (int i = 0; i < Sg; ++i) {
             mbar_init(&g_full[i], 1);
@@ -465,7 +545,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         }
         for (int i = 0; i < Sd; ++i) {
             mbar_init(&d_full[i], 1);
-            mbar_init(&d_empty[i], 2);                // two warps, a half each
+            mbar_init(&d_empty[i], np_r);             // one arrival a task
         }
         mbar_fence_init();
     }
@@ -508,6 +588,12 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         if (lane == 0) {
             issue_r(0);
             issue_sd(0);
+            // the first layer's input (this CTA reads all of it after the
+            // grid dependency resolves) on its way to L2 in the meantime
+            if (a.resid != nullptr)
+                bulk_prefetch_l2(a.resid, uint32_t(T) * H * 4u);
+            else
+                bulk_prefetch_l2(a.x_in, uint32_t(T) * H * 2u);
         }
         RingPos gpos{0, 0}, dpos{0, 0};
         for (int l = 0; l < a.n_layers; ++l) {
@@ -515,12 +601,14 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
             if (!px_wait(&plan_full, l & 1, err)) latch_timeout(err, 60, 0, l, 0);
             px_fence_proxy_async();
             // gate/up stages of this CTA's share, then its down rows of every
-            // touched expert.  A copy into a slot's first round waits for
-            // nothing: the 32 lanes request those in parallel (copy k by lane
-            // k mod 32).  A copy that reuses a slot waits for the slot: lane 0
-            // requests those, in order, while the other lanes wait at the
-            // warp barrier -- so no lane ever waits while another still has a
-            // copy to request that the wait depends on.
+            // touched expert.  The first S of them (S the ring's slots) reuse
+            // slots last filled in an earlier layer, whose consumers are done
+            // (they finished before this layer's plan): lane k requests copy k
+            // at once, its wait on the slot returning at once.  A copy past
+            // the ring reuses a slot of this layer: lane 0 requests those, in
+            // order, while the other lanes wait at the warp barrier -- so no
+            // lane ever waits while another still has a copy to request that
+            // the wait depends on.
             const GRange gr = px_g_range(P, I);
             const uint32_t dqb = uint32_t(nrow) * (I / 2), dsb = uint32_t(nrow) * (I / 16);
             auto issue_g = [&](int slot, int j, int i0, int nb) {
@@ -540,48 +628,82 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                     bulk_g2s(dst + a.d_q, Lr.dn_s + row * (I / 32), dsb, &d_full[slot]);
                 }
             };
-            {
-                RingPos pos = gpos;
-                int k = 0;
-                for (int j = gr.j, i0 = gr.i0, left = gr.n; left > 0; pos.next(Sg), ++k) {
-                    const int nb = min(kPxRowPairs, min(I - i0, left));
-                    if (pos.round == 0) {
-                        if ((k & 31) == lane) issue_g(pos.slot, j, i0, nb);
-                    } else {
-                        __syncwarp();
-                        if (lane == 0) {
+            int nst = 0;                                 // this layer's stages
+            for (int j = gr.j, i0 = gr.i0, left = gr.n; left > 0; ++j, i0 = 0) {
+                const int seg = min(I - i0, left);
+                nst += (seg + kPxRowPairs - 1) / kPxRowPairs;
+                left -= seg;
+            }
+            const int ng0 = min(nst, Sg);
+            for (int k = lane; k < ng0; k += 32) {
+                const int sl = gpos.slot + k;               // < 2 Sg
+                const int slot = sl < Sg ? sl : sl - Sg;
+                const uint32_t round = gpos.round + (sl < Sg ? 0u : 1u);
+                if (round > 0 && !px_wait(&g_empty[slot], (round - 1) & 1, err))
+                    latch_timeout(err, 61, slot, round, l);
+                // stage k: walk the range's expert segments to it
+                int j = gr.j, i0 = gr.i0, left = gr.n, kk = k;
+                for (;;) {
+                    const int seg = min(I - i0, left);
+                    const int ns = (seg + kPxRowPairs - 1) / kPxRowPairs;
+                    if (kk < ns) {
+                        i0 += kk * kPxRowPairs;
+                        issue_g(slot, j, i0, min(kPxRowPairs, seg - kk * kPxRowPairs));
+                        break;
+                    }
+                    kk -= ns;
+                    left -= seg;
+                    ++j;
+                    i0 = 0;
+                }
+            }
+            __syncwarp();
+            if (nst > ng0) {
+                if (lane == 0) {
+                    RingPos pos = gpos;
+                    int k = 0;
+                    for (int j = gr.j, i0 = gr.i0, left = gr.n; left > 0; pos.next(Sg), ++k) {
+                        const int nb = min(kPxRowPairs, min(I - i0, left));
+                        if (k >= ng0) {
                             if (!px_wait(&g_empty[pos.slot], (pos.round - 1) & 1, err))
                                 latch_timeout(err, 61, pos.slot, pos.round, l);
                             issue_g(pos.slot, j, i0, nb);
                         }
-                    }
-                    i0 += nb;
-                    left -= nb;
-                    if (i0 == I) {
-                        ++j;
-                        i0 = 0;
-                    }
-                }
-                gpos = pos;
-            }
-            __syncwarp();
-            {
-                RingPos pos = dpos;
-                for (int j = 0; j < P.n; ++j, pos.next(Sd)) {
-                    if (pos.round == 0) {
-                        if ((j & 31) == lane) issue_d(pos.slot, j);
-                    } else {
-                        __syncwarp();
-                        if (lane == 0) {
-                            if (!px_wait(&d_empty[pos.slot], (pos.round - 1) & 1, err))
-                                latch_timeout(err, 62, pos.slot, pos.round, l);
-                            issue_d(pos.slot, j);
+                        i0 += nb;
+                        left -= nb;
+                        if (i0 == I) {
+                            ++j;
+                            i0 = 0;
                         }
                     }
                 }
-                dpos = pos;
+                __syncwarp();
+            }
+            for (int k = 0; k < nst; ++k) gpos.next(Sg);
+            // the down units: the same split
+            const int nd0 = min(P.n, Sd);
+            for (int j = lane; j < nd0; j += 32) {
+                const int sl = dpos.slot + j;
+                const int slot = sl < Sd ? sl : sl - Sd;
+                const uint32_t round = dpos.round + (sl < Sd ? 0u : 1u);
+                if (round > 0 && !px_wait(&d_empty[slot], (round - 1) & 1, err))
+                    latch_timeout(err, 62, slot, round, l);
+                issue_d(slot, j);
             }
             __syncwarp();
+            if (P.n > nd0) {
+                if (lane == 0) {
+                    RingPos pos = dpos;
+                    for (int j = 0; j < P.n; ++j, pos.next(Sd)) {
+                        if (j < nd0) continue;
+                        if (!px_wait(&d_empty[pos.slot], (pos.round - 1) & 1, err))
+                            latch_timeout(err, 62, pos.slot, pos.round, l);
+                        issue_d(pos.slot, j);
+                    }
+                }
+                __syncwarp();
+            }
+            for (int j = 0; j < P.n; ++j) dpos.next(Sd);
             if (lane == 0) {
                 mbar_arrive(&plan_free);          // P no longer read here
                 // the next layer's routing-independent rows
@@ -743,6 +865,8 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         {
             const uint32_t tg_l = tag(l, 0);
             uint32_t* keys = reinterpret_cast<uint32_t*>(px + a.off_g);
+            // one token: every consumer warp selects; more: a warp a token
+            const bool all_select = T == 1 && a.forced_ids == nullptr;
             for (int t = cw; t < T; t += kPxConsumers) {
                 const uint64_t* lg = a.ll_logits + size_t(t) * (E + 1);
                 uint32_t* Lk = keys + size_t(cw) * (E + 16);
@@ -790,11 +914,15 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                         s_ids[t * K + k] = id;
                         s_w[t * K + k] = __ldg(fw + k);
                     }
-                } else {
+                } else if (!all_select) {
                     select_topk_keys(E, K, Lk, reinterpret_cast<float*>(Lk + E), s_ids + t * K,
                                      s_w + t * K, lane);
                 }
                 if (lane == 0) s_sig[t] = 1.0f / (1.0f + expf(-gl));
+            }
+            if (all_select) {
+                px_cbar();        // the polling warp's keys are in shared memory
+                px_select_all(E, K, keys, keys + (E + 16), s_ids, s_w, ctid, NT);
             }
         }
         px_cbar();
@@ -878,41 +1006,52 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
             px_stage_h(a.ll_h, a.ll_hs, tg_h, TK, I, T, Is, hsm, ctid, NT, lim, err);
             px_cbar();
             const uint32_t hb = sg;
-            // unit j lands in the next slot of the ring; half h of slot s (rows
-            // [0, R/2) or [R/2, R)) is always computed by warp (2 s + h) mod the
-            // warps, so each slot's rounds are waited for in order by the same
-            // two warps
-            const int rh = (nrow + 1) / 2;
-            for (int j = 0; j < n; ++j, dpos.next(Sd)) {
-                const int slot = dpos.slot;
-                for (int hh = 0; hh < 2; ++hh) {
-                    if ((2 * slot + hh) % kPxConsumers != cw) continue;
-                    const uint32_t round = dpos.round;
-                    if (!px_wait(&d_full[slot], round & 1, err))
-                        latch_timeout(err, 76, slot, round, l);
-                    const uint32_t dq = sd0 + uint32_t(slot) * a.d_stage;
-                    const int r0 = hh ? rh : 0, r1 = hh ? nrow : rh;
+            // tasks: first the shared unit's np_s passes, then np_r passes of
+            // each routed unit j (in the ring's order: unit j in the slot j
+            // places after this layer's first).  Warp w takes the contiguous
+            // run [w * ntask / 15, (w + 1) * ntask / 15), at most a few units,
+            // each as one call (its h loaded once, two rows a lane in flight);
+            // it arrives on a unit's empty barrier once per task it took.  A
+            // task's wait only depends on tasks of lower index (the unit's
+            // earlier round in the same slot), and every warp takes its run in
+            // increasing order, so the lowest unfinished task can always run.
+            const int ntask = np_s + n * np_r;
+            const int k1 = (cw + 1) * ntask / kPxConsumers;
+            RingPos up = dpos;                 // the slot of routed unit uj
+            int uj = 0;
+            for (int k = cw * ntask / kPxConsumers; k < k1;) {
+                if (k < np_s) {
+                    const int kend = min(k1, np_s);
+                    const int buf = l & 1;
+                    if (!px_wait(&sd_full[buf], (l >> 1) & 1, err))
+                        latch_timeout(err, 77, buf, l, 0);
+                    const uint32_t dq = base + a.off_sd + uint32_t(buf) * a.sd_bytes;
+                    const int r0 = k * rpw_s, r1 = min(kend * rpw_s, nrow);
+                    if (r1 > r0)
+                        px_down_unit(dq, dq + a.sd_q, Is, r0, r1, lane,
+                                     hb + uint32_t(TK) * uint32_t(I) * 4u, 0, T, nullptr, s_y, TK,
+                                     R);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_n(&sd_empty[buf], uint32_t(kend - k));
+                    k = kend;
+                } else {
+                    const int j = (k - np_s) / np_r, p0 = (k - np_s) - j * np_r;
+                    const int kend = min(k1, np_s + (j + 1) * np_r);
+                    const int p1 = kend - np_s - j * np_r;
+                    for (; uj < j; ++uj) up.next(Sd);
+                    if (!px_wait(&d_full[up.slot], up.round & 1, err))
+                        latch_timeout(err, 76, up.slot, up.round, l);
+                    const uint32_t dq = sd0 + uint32_t(up.slot) * a.d_stage;
+                    const int r0 = p0 * rpw_r, r1 = min(p1 * rpw_r, nrow);
                     if (r1 > r0)
                         px_down_unit(dq, dq + a.d_q, I, r0, r1, lane, hb, P.off[j], P.cnt[j],
                                      P.tok, s_y, 0, R);
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&d_empty[slot]);
+                    if (lane == 0) mbar_arrive_n(&d_empty[up.slot], uint32_t(kend - k));
+                    k = kend;
                 }
             }
-            // the shared expert: the warps the next unit's halves would go to
-            const int nslot = dpos.slot;
-            for (int hh = 0; hh < 2; ++hh) {
-                if ((2 * nslot + hh) % kPxConsumers != cw) continue;
-                const int buf = l & 1;
-                if (!px_wait(&sd_full[buf], (l >> 1) & 1, err)) latch_timeout(err, 77, buf, l, 0);
-                const uint32_t dq = base + a.off_sd + uint32_t(buf) * a.sd_bytes;
-                const int r0 = hh ? rh : 0, r1 = hh ? nrow : rh;
-                if (r1 > r0)
-                    px_down_unit(dq, dq + a.sd_q, Is, r0, r1, lane,
-                                 hb + uint32_t(TK) * uint32_t(I) * 4u, 0, T, nullptr, s_y, TK, R);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sd_empty[buf]);
-            }
+            for (int j = 0; j < n; ++j) dpos.next(Sd);
             px_cbar();
             const bool write_out = a.out != nullptr && (last || a.resid == nullptr);
             for (int i = ctid; i < T * nrow; i += NT) {
@@ -1000,9 +1139,12 @@ bool px_geometry(const strata_moe_dims& d, int T, bool forced, bool resid, int G
     // bucketing's scratch, the RMSNorm's residual and the SwiGLU vectors the
     // down products read.  The down ring: all of a small call's units (and
     // the next one) in flight, within 40 KB and what the gate/up ring leaves.
-    const size_t scratch = size_t(kPxConsumers) * (E + 16) * 4 > size_t(2 * E + 33) * 4
-                               ? size_t(kPxConsumers) * (E + 16) * 4
-                               : size_t(2 * E + 33) * 4;
+    size_t scratch = size_t(kPxConsumers) * (E + 16) * 4 > size_t(2 * E + 33) * 4
+                         ? size_t(kPxConsumers) * (E + 16) * 4
+                         : size_t(2 * E + 33) * 4;
+    // the one-token selection's keys and candidates
+    const size_t sel = (size_t(E + 16) + size_t((E + 31) / 32) * K * 2 + size_t(3) * K) * 4;
+    if (sel > scratch) scratch = sel;
     const size_t budget = kPxSmemBudget;
     const size_t fixed = x_bytes + r_bytes + size_t(2) * g->sd_bytes + y_bytes;
     const size_t g_round = size_t(kPxConsumers) * g->g_stage;

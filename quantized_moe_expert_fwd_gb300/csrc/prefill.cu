@@ -471,12 +471,16 @@ __global__ void k_pf_gather(const uint16_t* x, const int32_t* perm, int T, int K
                              *reinterpret_cast<const uint32_t*>(&h1),
                              *reinterpret_cast<const uint32_t*>(&h2),
                              *reinterpret_cast<const uint32_t*>(&h3));
-            inf_nan |= f16x2_not_finite(out.x) | f16x2_not_finite(out.y) |
-                       f16x2_not_finite(out.z) | f16x2_not_finite(out.w);
+            if ((f16x2_not_finite(out.x) | f16x2_not_finite(out.y) | f16x2_not_finite(out.z) |
+                 f16x2_not_finite(out.w)) != 0u) {
+                inf_nan = 1u;
+                out = make_uint4(f16x2_saturate(out.x), f16x2_saturate(out.y),
+                                 f16x2_saturate(out.z), f16x2_saturate(out.w));
+            }
         }
         reinterpret_cast<uint4*>(xg + size_t(row) * H)[g0 + q * gq] = out;
     }
-    if (inf_nan != 0u) latch(err, STRATA_ERANGE);
+    latch_warp(err, STRATA_ERANGE, __ballot_sync(__activemask(), inf_nan != 0u));
 }
 
 // fp32 -> fp16 in the operand order, 8 elements a thread.
@@ -491,14 +495,17 @@ __global__ void k_pf_pack(const float* src, long long n8, __half* dst, uint32_t*
     const __half2 h1 = __floats2half2_rn(a.y, b.y);
     const __half2 h2 = __floats2half2_rn(a.z, b.z);
     const __half2 h3 = __floats2half2_rn(a.w, b.w);
-    const uint4 out = make_uint4(*reinterpret_cast<const uint32_t*>(&h0),
-                                 *reinterpret_cast<const uint32_t*>(&h1),
-                                 *reinterpret_cast<const uint32_t*>(&h2),
-                                 *reinterpret_cast<const uint32_t*>(&h3));
+    uint4 out = make_uint4(*reinterpret_cast<const uint32_t*>(&h0),
+                           *reinterpret_cast<const uint32_t*>(&h1),
+                           *reinterpret_cast<const uint32_t*>(&h2),
+                           *reinterpret_cast<const uint32_t*>(&h3));
+    const uint32_t bad = f16x2_not_finite(out.x) | f16x2_not_finite(out.y) |
+                         f16x2_not_finite(out.z) | f16x2_not_finite(out.w);
+    if (bad != 0u)
+        out = make_uint4(f16x2_saturate(out.x), f16x2_saturate(out.y), f16x2_saturate(out.z),
+                         f16x2_saturate(out.w));
     reinterpret_cast<uint4*>(dst)[i] = out;
-    if ((f16x2_not_finite(out.x) | f16x2_not_finite(out.y) | f16x2_not_finite(out.z) |
-         f16x2_not_finite(out.w)) != 0u)
-        latch(err, STRATA_ERANGE);
+    latch_warp(err, STRATA_ERANGE, __ballot_sync(__activemask(), bad != 0u));
 }
 
 // out[t] = bf16( sum_k w[t][k] y[inv[t*K+k]] + sig[t] y_sh[t] ), 8 columns

@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
     __shared__ __align__(8) uint64_t mma_done;
     __shared__ uint32_t tmem_base;
     __shared__ int s_ntiles;
+    __shared__ uint32_t s_range;       // an fp16 output left the finite range
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sab_dyn) + 1023) &
                                                ~uintptr_t(1023));
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
         }
         mbar_init(&mma_done, kSabMmaWarps);
         mbar_fence_init();
+        s_range = 0u;
         for (int i = 0; i < kSabXMaps; ++i) tma_prefetch_map(&map_x.m[i]);
         tma_prefetch_map(&map_w);
     }
@@ -479,9 +481,12 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                         const float gt = odd ? other : keep, up = odd ? keep : other;
                         if (j + odd < nv) {
                             const float h = __fdividef(gt, 1.0f + __expf(-gt)) * up;
-                            const __half hh = __float2half_rn(h);
-                            inf_nan |= f16x2_not_finite(__half_as_ushort(hh));
-                            hb[size_t(j) * ld] = hh;
+                            uint32_t hu = __half_as_ushort(__float2half_rn(h));
+                            if (f16x2_not_finite(hu) != 0u) {
+                                inf_nan = 1u;
+                                hu = f16x2_saturate(hu);
+                            }
+                            hb[size_t(j) * ld] = __ushort_as_half(uint16_t(hu));
                             if (hf != nullptr) hf[size_t(j) * ld] = h;
                         }
                     }
@@ -499,13 +504,17 @@ __global__ void __launch_bounds__(kSabThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             if (j < nv) {
-                                const __half yv = __float2half_rn(__uint_as_float(v[j]));
-                                inf_nan |= f16x2_not_finite(__half_as_ushort(yv));
-                                yh[j * ld] = yv;
+                                const float yf = __uint_as_float(v[j]);
+                                uint32_t yu = __half_as_ushort(__float2half_rn(yf));
+                                if (f16x2_not_finite(yu) != 0u) {
+                                    inf_nan = 1u;
+                                    yu = f16x2_saturate(yu);
+                                }
+                                yh[j * ld] = __ushort_as_half(uint16_t(yu));
                             }
                     }
                 }
-                if (inf_nan != 0u) latch(a.err, STRATA_ERANGE);
+                if (inf_nan != 0u) s_range = 1u;       // latched once, at the end
             }
             tc_fence_before();
             mbar_arrive(&acc_empty[dbuf]);
@@ -516,6 +525,7 @@ __global__ void __launch_bounds__(kSabThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (wid == 1) tmem_dealloc(tmem, kSabTmemCols);
+    if (tid == 0 && s_range != 0u) latch(a.err, STRATA_ERANGE);
 }
 
 // ------------------------------------------------------------------ host

