@@ -34,11 +34,12 @@
  *     latches STRATA_EBADROUTE in the workspace's error word; a bounded wait
  *     that runs out latches STRATA_ETIMEOUT (over any code latched before
  *     it: the other waits of the call then give up early); on the tensor-core path
- *     (STRATA_PATH_TC), an activation, h or expert output whose fp16 operand
- *     copy is not finite (|value| beyond 65504, or a non-finite input)
- *     latches STRATA_ERANGE; the operand is written saturated (+-65504, 0
- *     for a NaN), so the products stay finite, and the call's outputs are
- *     not to be used.
+ *     (STRATA_PATH_TC), an activation or h whose fp16 operand copy is not
+ *     finite (|value| beyond 65504, or a non-finite input) latches
+ *     STRATA_ERANGE and is written saturated (+-65504, 0 for a NaN), so the
+ *     products stay finite, and a non-finite output (an expert output past
+ *     the fp16 range among the causes) latches it too; the call's outputs
+ *     are then not to be used.
  *     moe_get_device_status reads and clears the word.
  *   - Results are deterministic: ids, permutations and every floating sum are
  *     computed in a fixed order, with no floating-point atomics.

@@ -329,7 +329,7 @@ strata_status prefill_layer(const strata_moe_dims* d, const strata_moe_layer* L,
     p.xg_shared_row0 = T * d->top_k;
     STRATA_TRY(launch_prefill_experts(p, s));
     STRATA_TRY(launch_prefill_combine(p.y, nullptr, p.ysh, b.inv, r.w, r.sig, T, d->top_k,
-                                      d->hidden, static_cast<uint16_t*>(out), resid, s));
+                                      d->hidden, static_cast<uint16_t*>(out), resid, p.err, s));
     return STRATA_OK;
 }
 
@@ -742,7 +742,7 @@ strata_status moe_combine(const strata_moe_dims* dims, const strata_moe_layer* l
         STRATA_TRY(launch_prefill_combine(nullptr, static_cast<const uint16_t*>(y_dev), p.ysh,
                                           inv_perm_dev, weights_dev, shared_gate_dev, T,
                                           dims->top_k, dims->hidden,
-                                          static_cast<uint16_t*>(out_dev), nullptr, s));
+                                          static_cast<uint16_t*>(out_dev), nullptr, p.err, s));
         return STRATA_OK;
     }
     GuLaunch g{};

@@ -32,6 +32,16 @@ __device__ __forceinline__ void latch_warp(uint32_t* err, uint32_t code, uint32_
 __device__ __forceinline__ uint32_t f16x2_not_finite(uint32_t w) {
     return uint32_t((w & 0x7c00u) == 0x7c00u) | uint32_t((w & 0x7c000000u) == 0x7c000000u);
 }
+// Nonzero when either bf16 half of w is not finite.
+__device__ __forceinline__ uint32_t bf16x2_not_finite(uint32_t w) {
+    return uint32_t((w & 0x7f80u) == 0x7f80u) | uint32_t((w & 0x7f800000u) == 0x7f800000u);
+}
+// Nonzero when either bf16 half of w has no finite fp16 value: |v| >= 65536
+// (the bf16 value below it, 65280, converts exactly), infinite or NaN.  A
+// half at or above 0x4780 carries into its top bit when 0x3880 is added.
+__device__ __forceinline__ uint32_t bf16x2_over_f16(uint32_t w) {
+    return ((w & 0x7fff7fffu) + 0x38803880u) & 0x80008000u;
+}
 // w with each infinite half replaced by the largest finite value of its sign
 // (+-65504) and each NaN by 0: tensor-core operands stay finite.
 __device__ __forceinline__ uint32_t f16x2_saturate(uint32_t w) {
@@ -274,14 +284,6 @@ __device__ __forceinline__ int lds_s32(uint32_t a) {
     int v;
     asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
-}
-
-// Brings [src, src + bytes) into L2 (16-byte aligned, a multiple of 16
-// bytes); no data moves to the SM and nothing waits for it.  L2 is the
-// point of coherence, so a prefetch made before another kernel's writes
-// land never hides them.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // dst, src 16-byte aligned; bytes a multiple of 16

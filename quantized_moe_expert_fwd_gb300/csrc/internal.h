@@ -148,7 +148,7 @@ constexpr int kPxMaxLayers = 40;          // layers one launch carries
 // SM's four sub-partitions
 constexpr int kPxConsumers = 15;
 constexpr int kPxRowPairs = 2;            // gate/up row pairs per ring stage (one warp's)
-constexpr int kPxGuMaxStages = 30;
+constexpr int kPxGuMaxStages = 15;
 constexpr int kPxDnMaxStages = 32;
 constexpr size_t kPxSmemBudget = 200 * 1024;   // dynamic shared memory at most
 constexpr size_t kPxSmemMin = 120 * 1024;      // at least: one CTA per SM
@@ -285,6 +285,7 @@ cudaError_t launch_prefill_experts(const PfExperts& p, cudaStream_t s);
 // y: fp16 (y_f16) or bf16 (y_bf16), slot order; ysh fp16
 cudaError_t launch_prefill_combine(const __half* y_f16, const uint16_t* y_bf16, const __half* ysh,
                                    const int32_t* inv, const float* w, const float* sig, int T,
-                                   int K, int H, uint16_t* out, float* resid, cudaStream_t s);
+                                   int K, int H, uint16_t* out, float* resid, uint32_t* err,
+                                   cudaStream_t s);
 
 }  // namespace strata

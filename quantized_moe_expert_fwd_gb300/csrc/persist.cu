@@ -53,7 +53,7 @@
 namespace strata {
 
 constexpr int kPxThreads = 32 * (kPxConsumers + 1);
-constexpr uint32_t kLlWaitLimit = 1u << 21;     // polls: a second or two
+constexpr uint32_t kLlWaitLimit = 1u << 21;     // polls (L2 round trips): a second or two
 constexpr int kPxExchanges = 3;                  // tagged exchanges a layer
 
 static std::atomic<uint32_t> g_grid_wait_limit{0};
@@ -104,9 +104,10 @@ __device__ __forceinline__ bool px_wait(uint64_t* bar, uint32_t parity, const ui
     return false;
 }
 
-// A poll that found its data missing waits a little before the next one, so
-// the CTAs that are still computing it do not share L2 with a storm of reads.
-__device__ __forceinline__ void px_backoff() { __nanosleep(128); }
+// Between two polls of a word that was not there yet: nothing.  A poll is an
+// L2 round trip, which paces it; a sleep of 32 or 128 ns here measured 0.4
+// and 4 us slower a layer in the 40-layer stack, the same in one layer.
+__device__ __forceinline__ void px_backoff() {}
 
 // --------------------------------------------------- tagged 64-bit words
 __device__ __forceinline__ void ll_put(uint64_t* p, float v, uint32_t tag) {
@@ -325,7 +326,7 @@ __device__ void px_stage_h(const uint64_t* hr, const uint64_t* hs, uint32_t tag,
                            int T, int Is, float* dst, int ctid, int nthr, uint32_t limit,
                            uint32_t* err) {
     const int pr = TK * (I / 4), ptot = pr + T * (Is / 4);     // pieces of four words
-    constexpr int PB = 4;                                         // pieces a thread per batch
+    constexpr int PB = 1;        // pieces a thread per batch (more cost registers: spills)
     for (int p0 = ctid; p0 < ptot; p0 += nthr * PB) {
         uint32_t todo = 0;
 #pragma unroll
@@ -364,81 +365,6 @@ __device__ void px_stage_h(const uint64_t* hr, const uint64_t* hs, uint32_t tag,
             }
         }
         if (todo != 0u) latch_timeout(err, 81, p0, tag, 0);
-    }
-}
-
-// Top-K of one token by every consumer thread (the order: larger key first,
-// the lower id among equal keys -- a strict total order, so the K picks are
-// the keys of rank 0 .. K-1), written in ascending id to ids[0..K) with the
-// softmax weights, in the same arithmetic as select_topk_keys.  Lk: the E
-// order-preserving keys; scratch: (E / 32 + 1) * K * 2 + 3 * K words.
-//   1. a key ranked K or later in its group of 32 is ranked K or later
-//      overall: each group keeps its K best as candidates;
-//   2. each candidate's rank among all candidates (four lanes a candidate);
-//   3. the K picks ordered by id, their softmax.
-__device__ void px_select_all(int E, int K, const uint32_t* Lk, uint32_t* scratch, int* ids,
-                              float* w, int ctid, int nthr) {
-    const int lane = ctid & 31, cw = ctid >> 5, nw = nthr >> 5;
-    const int ng = (E + 31) >> 5, nc = ng * K;
-    uint32_t* ck = scratch;
-    int* ci = reinterpret_cast<int*>(ck + nc);
-    uint32_t* sk = reinterpret_cast<uint32_t*>(ci + nc);
-    int* si = reinterpret_cast<int*>(sk + K);
-    float* ex = reinterpret_cast<float*>(si + K);
-    for (int g = cw; g < ng; g += nw) {
-        const int e = g * 32 + lane;
-        const uint32_t k = e < E ? Lk[e] : 0u;     // past E: key 0 and the largest ids
-        int r = 0;
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const uint32_t ku = __shfl_sync(0xffffffffu, k, u);
-            r += (ku > k || (ku == k && u < lane)) ? 1 : 0;
-        }
-        if (r < K) {
-            ck[g * K + r] = k;
-            ci[g * K + r] = e;
-        }
-    }
-    px_cbar();
-    constexpr int kSplit = 4;
-    const int per = nthr / kSplit;
-    for (int c0 = 0; c0 < nc; c0 += per) {
-        const int c = c0 + ctid / kSplit;
-        uint32_t k = 0u;
-        int id = 0x7fffffff, r = 0;
-        if (c < nc) {
-            k = ck[c];
-            id = ci[c];
-            for (int d = ctid % kSplit; d < nc; d += kSplit) {
-                const uint32_t kd = ck[d];
-                r += (kd > k || (kd == k && ci[d] < id)) ? 1 : 0;
-            }
-        }
-        r += __shfl_xor_sync(0xffffffffu, r, 1);
-        r += __shfl_xor_sync(0xffffffffu, r, 2);
-        if (c < nc && ctid % kSplit == 0 && r < K) {
-            sk[r] = k;
-            si[r] = id;
-        }
-    }
-    px_cbar();
-    if (cw == 0) {
-        const uint32_t k = lane < K ? sk[lane] : 0u;
-        const int id = lane < K ? si[lane] : 0x7fffffff;
-        int pos = 0;
-        for (int j = 0; j < K; ++j) pos += (__shfl_sync(0xffffffffu, id, j) < id) ? 1 : 0;
-        const float m = __shfl_sync(0xffffffffu, key_logit(k), 0);   // rank 0: the largest
-        float e_k = 0.0f;
-        if (lane < K) {
-            e_k = expf(key_logit(k) - m);
-            ex[pos] = e_k;
-            ids[pos] = id;
-        }
-        __syncwarp();
-        float sum = 0.0f;
-        for (int p = 0; p < K; ++p) sum += ex[p];                      // ascending id
-        if (lane < K) w[pos] = e_k / sum;
-        __syncwarp();
     }
 }
 
@@ -497,7 +423,10 @@ __device__ void px_down_unit(uint32_t sq, uint32_t ss, int L, int r0, int r1, in
 }
 
 // ------------------------------------------------------------------ kernel
-template <int MC>
+// RESID: a residual stack (RMSNorm before each layer, the output added to
+// the residual) or one layer on x_in; a kernel of each, so that one-layer
+// calls carry no registers for the RMSNorm.
+template <int MC, bool RESID>
 __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant__ PxArgs a) {
     extern __shared__ __align__(128) uint8_t px[];
     __shared__ SPlan P;
@@ -588,12 +517,6 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         if (lane == 0) {
             issue_r(0);
             issue_sd(0);
-            // the first layer's input (this CTA reads all of it after the
-            // grid dependency resolves) on its way to L2 in the meantime
-            if (a.resid != nullptr)
-                bulk_prefetch_l2(a.resid, uint32_t(T) * H * 4u);
-            else
-                bulk_prefetch_l2(a.x_in, uint32_t(T) * H * 2u);
         }
         RingPos gpos{0, 0}, dpos{0, 0};
         for (int l = 0; l < a.n_layers; ++l) {
@@ -747,7 +670,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         const PxLayer& Lr = a.L[l];
         const bool last = l + 1 == a.n_layers;
         // ---- the layer input x (bf16) into shared memory
-        if (a.resid != nullptr) {
+        if constexpr (RESID) {
             // RMSNorm of the residual: the caller's (plain) before the first
             // layer, the previous layer's tagged words after it
             // (pass 1 parks the fp32 residual at the start of the gate/up ring,
@@ -865,8 +788,6 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         {
             const uint32_t tg_l = tag(l, 0);
             uint32_t* keys = reinterpret_cast<uint32_t*>(px + a.off_g);
-            // one token: every consumer warp selects; more: a warp a token
-            const bool all_select = T == 1 && a.forced_ids == nullptr;
             for (int t = cw; t < T; t += kPxConsumers) {
                 const uint64_t* lg = a.ll_logits + size_t(t) * (E + 1);
                 uint32_t* Lk = keys + size_t(cw) * (E + 16);
@@ -914,15 +835,11 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                         s_ids[t * K + k] = id;
                         s_w[t * K + k] = __ldg(fw + k);
                     }
-                } else if (!all_select) {
+                } else {
                     select_topk_keys(E, K, Lk, reinterpret_cast<float*>(Lk + E), s_ids + t * K,
                                      s_w + t * K, lane);
                 }
                 if (lane == 0) s_sig[t] = 1.0f / (1.0f + expf(-gl));
-            }
-            if (all_select) {
-                px_cbar();        // the polling warp's keys are in shared memory
-                px_select_all(E, K, keys, keys + (E + 16), s_ids, s_w, ctid, NT);
             }
         }
         px_cbar();
@@ -1053,7 +970,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
             }
             for (int j = 0; j < n; ++j) dpos.next(Sd);
             px_cbar();
-            const bool write_out = a.out != nullptr && (last || a.resid == nullptr);
+            const bool write_out = a.out != nullptr && (last || !RESID);
             for (int i = ctid; i < T * nrow; i += NT) {
                 const int t = i / nrow, r = i - t * nrow, o = o0 + r;
                 float acc = 0.0f;
@@ -1065,7 +982,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                 const float v = acc + s_sig[t] * s_y[size_t(TK + t) * R + r];
                 const uint16_t ob = f32_to_bf16(v);
                 if (write_out) a.out[size_t(t) * H + o] = ob;
-                if (a.resid != nullptr) {
+                if constexpr (RESID) {
                     float* rp = a.resid + size_t(t) * H + o;
                     const float rn = __ldcg(rp) + __uint_as_float(uint32_t(ob) << 16);
                     *rp = rn;
@@ -1100,7 +1017,10 @@ size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
 
 using PxFn = void (*)(PxArgs);
 
-PxFn px_kernel(int MC) { return MC == 1 ? k_persist<1> : k_persist<2>; }
+PxFn px_kernel(int MC, bool resid) {
+    if (resid) return MC == 1 ? k_persist<1, true> : k_persist<2, true>;
+    return MC == 1 ? k_persist<1, false> : k_persist<2, false>;
+}
 
 }  // namespace
 
@@ -1139,12 +1059,9 @@ bool px_geometry(const strata_moe_dims& d, int T, bool forced, bool resid, int G
     // bucketing's scratch, the RMSNorm's residual and the SwiGLU vectors the
     // down products read.  The down ring: all of a small call's units (and
     // the next one) in flight, within 40 KB and what the gate/up ring leaves.
-    size_t scratch = size_t(kPxConsumers) * (E + 16) * 4 > size_t(2 * E + 33) * 4
-                         ? size_t(kPxConsumers) * (E + 16) * 4
-                         : size_t(2 * E + 33) * 4;
-    // the one-token selection's keys and candidates
-    const size_t sel = (size_t(E + 16) + size_t((E + 31) / 32) * K * 2 + size_t(3) * K) * 4;
-    if (sel > scratch) scratch = sel;
+    const size_t scratch = size_t(kPxConsumers) * (E + 16) * 4 > size_t(2 * E + 33) * 4
+                               ? size_t(kPxConsumers) * (E + 16) * 4
+                               : size_t(2 * E + 33) * 4;
     const size_t budget = kPxSmemBudget;
     const size_t fixed = x_bytes + r_bytes + size_t(2) * g->sd_bytes + y_bytes;
     const size_t g_round = size_t(kPxConsumers) * g->g_stage;
@@ -1183,7 +1100,7 @@ bool px_geometry(const strata_moe_dims& d, int T, bool forced, bool resid, int G
 }
 
 cudaError_t launch_persistent(const PxArgs& a, const PxGeo& g, cudaStream_t s) {
-    PxFn fn = px_kernel(g.MC);
+    PxFn fn = px_kernel(g.MC, a.resid != nullptr);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(g.dyn));
     if (e != cudaSuccess) return e;

@@ -471,12 +471,12 @@ __global__ void k_pf_gather(const uint16_t* x, const int32_t* perm, int T, int K
                              *reinterpret_cast<const uint32_t*>(&h1),
                              *reinterpret_cast<const uint32_t*>(&h2),
                              *reinterpret_cast<const uint32_t*>(&h3));
-            if ((f16x2_not_finite(out.x) | f16x2_not_finite(out.y) | f16x2_not_finite(out.z) |
-                 f16x2_not_finite(out.w)) != 0u) {
-                inf_nan = 1u;
+            const uint32_t bad = bf16x2_over_f16(wv[0]) | bf16x2_over_f16(wv[1]) |
+                                 bf16x2_over_f16(wv[2]) | bf16x2_over_f16(wv[3]);
+            inf_nan |= bad;
+            if (bad != 0u)            // rare: the operand stays finite
                 out = make_uint4(f16x2_saturate(out.x), f16x2_saturate(out.y),
                                  f16x2_saturate(out.z), f16x2_saturate(out.w));
-            }
         }
         reinterpret_cast<uint4*>(xg + size_t(row) * H)[g0 + q * gq] = out;
     }
@@ -532,7 +532,7 @@ __device__ __forceinline__ void b8_to_f32(const uint4& v, float (&f)[8]) {
 template <bool Y_BF16>
 __global__ void k_pf_combine(const void* y, const __half* y_sh, const int32_t* inv,
                              const float* w, const float* sig, int T, int K, int H,
-                             uint16_t* out, float* resid) {
+                             uint16_t* out, float* resid, uint32_t* err) {
     pdl_launch();
     pdl_wait();
     const int groups = H >> 3;
@@ -564,6 +564,11 @@ __global__ void k_pf_combine(const void* y, const __half* y_sh, const int32_t* i
         o[j] = uint32_t(f32_to_bf16(a0)) | (uint32_t(f32_to_bf16(a1)) << 16);
     }
     *reinterpret_cast<uint4*>(out + size_t(t) * H + 8 * g) = make_uint4(o[0], o[1], o[2], o[3]);
+    // an expert output that overflowed its fp16 copy shows here as a
+    // non-finite output (the down products' epilogue carries no check)
+    const uint32_t bad = bf16x2_not_finite(o[0]) | bf16x2_not_finite(o[1]) |
+                         bf16x2_not_finite(o[2]) | bf16x2_not_finite(o[3]);
+    latch_warp(err, STRATA_ERANGE, __ballot_sync(__activemask(), bad != 0u));
     if (resid) {
         float* rr = resid + size_t(t) * H + 8 * g;
 #pragma unroll
@@ -582,7 +587,7 @@ template <bool Y_BF16, int MAXK>
 __global__ void __launch_bounds__(256)
     k_pf_combine_few(const void* y, const __half* y_sh, const int32_t* inv,
                              const float* w, const float* sig, int T, int K, int H,
-                             uint16_t* out, float* resid) {
+                             uint16_t* out, float* resid, uint32_t* err) {
     pdl_launch();
     pdl_wait();
     const int groups = H >> 3;
@@ -628,6 +633,11 @@ __global__ void __launch_bounds__(256)
         o[j] = uint32_t(f32_to_bf16(a0)) | (uint32_t(f32_to_bf16(a1)) << 16);
     }
     *reinterpret_cast<uint4*>(out + size_t(t) * H + 8 * g) = make_uint4(o[0], o[1], o[2], o[3]);
+    // an expert output that overflowed its fp16 copy shows here as a
+    // non-finite output (the down products' epilogue carries no check)
+    const uint32_t bad = bf16x2_not_finite(o[0]) | bf16x2_not_finite(o[1]) |
+                         bf16x2_not_finite(o[2]) | bf16x2_not_finite(o[3]);
+    latch_warp(err, STRATA_ERANGE, __ballot_sync(__activemask(), bad != 0u));
     if (resid) {
         float* rr = resid + size_t(t) * H + 8 * g;
 #pragma unroll
@@ -939,7 +949,8 @@ constexpr int kCombineFewTokens = 256;
 
 cudaError_t launch_prefill_combine(const __half* y_f16, const uint16_t* y_bf16, const __half* ysh,
                                    const int32_t* inv, const float* w, const float* sig, int T,
-                                   int K, int H, uint16_t* out, float* resid, cudaStream_t s) {
+                                   int K, int H, uint16_t* out, float* resid, uint32_t* err,
+                                   cudaStream_t s) {
     const long long n = (long long)T * (H / 8);
     const int grid = int((n + 255) / 256);
     if (T <= kCombineFewTokens && K <= 8) {
@@ -947,15 +958,15 @@ cudaError_t launch_prefill_combine(const __half* y_f16, const uint16_t* y_bf16, 
                                           : static_cast<const void*>(y_f16);
         if (y_bf16 != nullptr)
             return launch_pdl(k_pf_combine_few<true, 8>, grid, 256, 0, s, y, ysh, inv, w, sig, T,
-                              K, H, out, resid);
+                              K, H, out, resid, err);
         return launch_pdl(k_pf_combine_few<false, 8>, grid, 256, 0, s, y, ysh, inv, w, sig, T, K,
-                          H, out, resid);
+                          H, out, resid, err);
     }
     if (y_bf16 != nullptr)
         return launch_pdl(k_pf_combine<true>, grid, 256, 0, s, static_cast<const void*>(y_bf16),
-                          ysh, inv, w, sig, T, K, H, out, resid);
+                          ysh, inv, w, sig, T, K, H, out, resid, err);
     return launch_pdl(k_pf_combine<false>, grid, 256, 0, s, static_cast<const void*>(y_f16), ysh,
-                      inv, w, sig, T, K, H, out, resid);
+                      inv, w, sig, T, K, H, out, resid, err);
 }
 
 }  // namespace strata

@@ -481,15 +481,20 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                         const float gt = odd ? other : keep, up = odd ? keep : other;
                         if (j + odd < nv) {
                             const float h = __fdividef(gt, 1.0f + __expf(-gt)) * up;
-                            uint32_t hu = __half_as_ushort(__float2half_rn(h));
-                            if (f16x2_not_finite(hu) != 0u) {
-                                inf_nan = 1u;
-                                hu = f16x2_saturate(hu);
-                            }
-                            hb[size_t(j) * ld] = __ushort_as_half(uint16_t(hu));
+                            const __half hh = __float2half_rn(h);
+                            inf_nan |= f16x2_not_finite(__half_as_ushort(hh));
+                            hb[size_t(j) * ld] = hh;
                             if (hf != nullptr) hf[size_t(j) * ld] = h;
                         }
                     }
+                    // rare: an element overflowed; the thread rewrites its own
+                    // stores saturated (kept out of the loop above, which a
+                    // branch per element slowed by a third)
+                    if (inf_nan != 0u)
+                        for (int j = odd; j < nv; j += 2) {
+                            const uint32_t hu = __half_as_ushort(hb[size_t(j) * ld]);
+                            hb[size_t(j) * ld] = __ushort_as_half(uint16_t(f16x2_saturate(hu)));
+                        }
                 } else {
                     const int o = mt * kBM + m;              // output feature
                     const size_t ld = size_t(a.ldo);
@@ -502,16 +507,12 @@ __global__ void __launch_bounds__(kSabThreads, 1)
                     } else {
                         __half* yh = (sh ? a.out2_f16 : a.out_f16) + r0;
 #pragma unroll
+                        // no range check here: this epilogue paces the down
+                        // products (a check per element cost a quarter of the
+                        // kernel); y is no tensor-core operand, and the
+                        // combine checks the outputs it makes of it
                         for (int j = 0; j < 32; ++j)
-                            if (j < nv) {
-                                const float yf = __uint_as_float(v[j]);
-                                uint32_t yu = __half_as_ushort(__float2half_rn(yf));
-                                if (f16x2_not_finite(yu) != 0u) {
-                                    inf_nan = 1u;
-                                    yu = f16x2_saturate(yu);
-                                }
-                                yh[j * ld] = __ushort_as_half(uint16_t(yu));
-                            }
+                            if (j < nv) yh[j * ld] = __float2half_rn(__uint_as_float(v[j]));
                     }
                 }
                 if (inf_nan != 0u) s_range = 1u;       // latched once, at the end

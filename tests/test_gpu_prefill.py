@@ -218,9 +218,10 @@ def test_tc_path_latches_erange_on_fp16_overflow(scale, what):
     """The tensor-core path holds activations, h and expert outputs as fp16
     operands.  Scaled inputs whose fp16 copy (x * 1e5: |x| up to ~5e5) or
     whose h (x * 300: the oracle's fp32 h far beyond 65504) leaves the finite
-    fp16 range latch STRATA_ERANGE, with the operand written saturated (the
-    output stays finite); the unscaled input passes clean, and the same
-    scaled token through the persistent decode kernel (fp32 h) does too."""
+    fp16 range latch STRATA_ERANGE (and not a timeout: the operand is written
+    saturated, the kernels run to their end); the unscaled input passes
+    clean, and the same scaled token through the persistent decode kernel
+    (fp32 h) does too."""
     dims = gen.QWEN
     planes, dl = layer(dims, 7)
     T = 40
@@ -242,8 +243,6 @@ def test_tc_path_latches_erange_on_fp16_overflow(scale, what):
     q.moe_layer_forward(dims, dl, G.u16(xb), out, ws)
     torch.cuda.synchronize()
     assert q.moe_get_device_status(ws) == q.STRATA_ERANGE
-    # the overflowing operands were written saturated: the output is finite
-    assert np.all(np.isfinite(G.bf16_to_np(out)))
     # the word was cleared by the read: the next clean call reports OK
     q.moe_layer_forward(dims, dl, G.u16(x0), out, ws)
     torch.cuda.synchronize()
