@@ -155,9 +155,65 @@ __device__ __forceinline__ float dot_chunk(const uint4& q, const uint64_t* x2) {
     return (a0.x + a0.y) + (a1.x + a1.y);
 }
 
+// d = a * b + c with a, b one bf16 half each of a 32-bit word (HI_A /
+// HI_B: the upper half) and c, d fp32; the product of two bf16 is exact in
+// fp32, so this rounds once, as fmaf on the widened values does.
+template <bool HI_A, bool HI_B>
+__device__ __forceinline__ float fma_bf16(uint32_t a, uint32_t b, float c) {
+    float d;
+    if (!HI_A && !HI_B)
+        asm("{ .reg .b16 a0, a1, b0, b1; mov.b32 {a0, a1}, %1; mov.b32 {b0, b1}, %2;\n"
+            "  fma.rn.f32.bf16 %0, a0, b0, %3; }" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    else if (!HI_A && HI_B)
+        asm("{ .reg .b16 a0, a1, b0, b1; mov.b32 {a0, a1}, %1; mov.b32 {b0, b1}, %2;\n"
+            "  fma.rn.f32.bf16 %0, a0, b1, %3; }" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    else if (HI_A && !HI_B)
+        asm("{ .reg .b16 a0, a1, b0, b1; mov.b32 {a0, a1}, %1; mov.b32 {b0, b1}, %2;\n"
+            "  fma.rn.f32.bf16 %0, a1, b0, %3; }" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    else
+        asm("{ .reg .b16 a0, a1, b0, b1; mov.b32 {a0, a1}, %1; mov.b32 {b0, b1}, %2;\n"
+            "  fma.rn.f32.bf16 %0, a1, b1, %3; }" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+
+// dot_chunk times 128, bit for bit, against bf16 activations left packed:
+// xb[k] holds elements 2k, 2k + 1.  A weight becomes the bf16 128 + u (one
+// mask-and-or makes two), multiplied by x with fp32 accumulation in the
+// same four chains, in the same order, as dot_chunk (elements {0,4},
+// {1,5}, {2,6}, {3,7} of each word); 128 * (1 + u/128) = 128 + u exactly,
+// so each partial sum is 128 times dot_chunk's.
+__device__ __forceinline__ float dot_chunk_bf16(const uint4& q, const uint32_t* xb) {
+    float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, c3 = 0.0f;
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t v = words[w];
+        const uint32_t p04 = (v & 0x000F000Fu) | 0x43004300u;
+        const uint32_t p15 = ((v >> 4) & 0x000F000Fu) | 0x43004300u;
+        const uint32_t p26 = ((v >> 8) & 0x000F000Fu) | 0x43004300u;
+        const uint32_t p37 = ((v >> 12) & 0x000F000Fu) | 0x43004300u;
+        const uint32_t x0 = xb[4 * w], x1 = xb[4 * w + 1], x2 = xb[4 * w + 2], x3 = xb[4 * w + 3];
+        c0 = fma_bf16<false, false>(p04, x0, c0);
+        c0 = fma_bf16<true, false>(p04, x2, c0);
+        c1 = fma_bf16<false, true>(p15, x0, c1);
+        c1 = fma_bf16<true, true>(p15, x2, c1);
+        c2 = fma_bf16<false, false>(p26, x1, c2);
+        c2 = fma_bf16<true, false>(p26, x3, c2);
+        c3 = fma_bf16<false, true>(p37, x1, c3);
+        c3 = fma_bf16<true, true>(p37, x3, c3);
+    }
+    return (c0 + c1) + (c2 + c3);
+}
+
 // Scaled group dot product: scale * sum_j (u_j - 8) x_j.
 __device__ __forceinline__ float group_dot(float A, float X, float scale) {
     return scale * fmaf(128.0f, A, -136.0f * X);
+}
+// The same from dot_chunk_bf16's sum (128 A): -136 X rounded, then one
+// rounding of 128 A plus it, as in group_dot (the explicit roundings keep
+// the compiler from fusing the two into one).
+__device__ __forceinline__ float group_dot128(float A128, float X, float scale) {
+    return scale * __fadd_rn(A128, __fmul_rn(-136.0f, X));
 }
 
 // ------------------------------------------------------------- reductions

@@ -214,10 +214,12 @@ struct RingPos {
 // Activations of token t in shared memory, chunk-interleaved: the 16-byte
 // piece v of 32-element chunk c at piece index v * NC + c.
 
-// One bf16 router row (natural layout, shared memory) against token x.
+// One bf16 router row (natural layout, shared memory) against token x:
+// four fp32 chains (even words' low and high halves, odd words' low and
+// high halves), both operands bf16.
 template <int MC>
 __device__ __forceinline__ float px_router_dot(uint32_t wrow, uint32_t xrow, int NC, int lane) {
-    uint64_t acc0 = 0ull, acc1 = 0ull;
+    float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, c3 = 0.0f;
 #pragma unroll
     for (int m = 0; m < MC; ++m) {
         const int c = lane + 32 * m;
@@ -226,27 +228,24 @@ __device__ __forceinline__ float px_router_dot(uint32_t wrow, uint32_t xrow, int
             for (int v = 0; v < 4; ++v) {
                 const uint4 wu = lds128(wrow + 64u * c + 16u * v);
                 const uint4 xu = lds128(xrow + 16u * (v * NC + c));
-                const uint32_t xw[4] = {xu.x, xu.y, xu.z, xu.w};
-                const uint32_t ww[4] = {wu.x, wu.y, wu.z, wu.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint64_t a = pk(bf16_lo(ww[i]), bf16_hi(ww[i]));
-                    const uint64_t bb = pk(bf16_lo(xw[i]), bf16_hi(xw[i]));
-                    if (i & 1)
-                        acc1 = ffma2(a, bb, acc1);
-                    else
-                        acc0 = ffma2(a, bb, acc0);
-                }
+                c0 = fma_bf16<false, false>(wu.x, xu.x, c0);
+                c1 = fma_bf16<true, true>(wu.x, xu.x, c1);
+                c2 = fma_bf16<false, false>(wu.y, xu.y, c2);
+                c3 = fma_bf16<true, true>(wu.y, xu.y, c3);
+                c0 = fma_bf16<false, false>(wu.z, xu.z, c0);
+                c1 = fma_bf16<true, true>(wu.z, xu.z, c1);
+                c2 = fma_bf16<false, false>(wu.w, xu.w, c2);
+                c3 = fma_bf16<true, true>(wu.w, xu.w, c3);
             }
         }
     }
-    const float2 a0 = upk(acc0), a1 = upk(acc1);
-    return warp_sum((a0.x + a0.y) + (a1.x + a1.y));
+    return warp_sum((c0 + c1) + (c2 + c3));
 }
 
-// Token x from shared memory into the lane's fp32 pairs and chunk sums.
+// Token x from shared memory: the lane's bf16 words of chunks lane and
+// lane + 32 and their fp32 sums.
 template <int MC>
-__device__ __forceinline__ void px_load_x(uint32_t xrow, int NC, int lane, uint64_t (&x2)[MC][16],
+__device__ __forceinline__ void px_load_x(uint32_t xrow, int NC, int lane, uint32_t (&xb)[MC][16],
                                           float (&X)[MC]) {
 #pragma unroll
     for (int m = 0; m < MC; ++m) {
@@ -259,25 +258,24 @@ __device__ __forceinline__ void px_load_x(uint32_t xrow, int NC, int lane, uint6
                 const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float lo = bf16_lo(wv[i]), hi = bf16_hi(wv[i]);
-                    x2[m][4 * v + i] = pk(lo, hi);
-                    sum += lo + hi;
+                    xb[m][4 * v + i] = wv[i];
+                    sum += bf16_lo(wv[i]) + bf16_hi(wv[i]);
                 }
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) x2[m][j] = 0ull;
+            for (int j = 0; j < 16; ++j) xb[m][j] = 0u;
         }
         X[m] = sum;
     }
 }
 
 // Rows r < nrows (<= NR) of length H (packed bytes at q + r * qs, fp16
-// scales at s + r * ss, shared memory) against the token in x2 / X, all at
+// scales at s + r * ss, shared memory) against the token in xb / X, all at
 // once: out[r] = the row's dot product, in every lane.
 template <int MC, int NR>
 __device__ __forceinline__ void px_rows_dot(uint32_t q, uint32_t s, uint32_t qs, uint32_t ss,
-                                            int nrows, const uint64_t (&x2)[MC][16],
+                                            int nrows, const uint32_t (&xb)[MC][16],
                                             const float (&X)[MC], int NC, int lane,
                                             float (&out)[NR]) {
     float acc[NR];
@@ -292,7 +290,7 @@ __device__ __forceinline__ void px_rows_dot(uint32_t q, uint32_t s, uint32_t qs,
                 if (r < nrows) {
                     const uint4 w = lds128(q + uint32_t(r) * qs + 16u * c);
                     const float sc = f16_to_f32(lds_u16(s + uint32_t(r) * ss + 2u * c));
-                    acc[r] += group_dot(dot_chunk(w, x2[m]), X[m], sc);
+                    acc[r] += group_dot128(dot_chunk_bf16(w, xb[m]), X[m], sc);
                 }
             }
         }
@@ -309,11 +307,11 @@ __device__ __forceinline__ void px_rows_dot(uint32_t q, uint32_t s, uint32_t qs,
 template <int MC>
 __device__ __noinline__ float px_pair_silu(uint32_t q, uint32_t s, uint32_t xrow, int NC,
                                            int lane) {
-    uint64_t x2[MC][16];
+    uint32_t xb[MC][16];
     float X[MC];
-    px_load_x<MC>(xrow, NC, lane, x2, X);
+    px_load_x<MC>(xrow, NC, lane, xb, X);
     float gu[2];
-    px_rows_dot<MC, 2>(q, s, uint32_t(NC) * 16u, uint32_t(NC) * 2u, 2, x2, X, NC, lane, gu);
+    px_rows_dot<MC, 2>(q, s, uint32_t(NC) * 16u, uint32_t(NC) * 2u, 2, xb, X, NC, lane, gu);
     return silu_mul(gu[0], gu[1]);
 }
 
