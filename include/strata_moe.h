@@ -204,10 +204,10 @@ STRATA_API strata_status moe_combine(const strata_moe_dims* dims, const strata_m
                           size_t ws_bytes, void* stream);
 
 /* The whole layer: route, permute, experts, shared expert, combine.  Which
- * kernels run is moe_layer_path(dims, T): at decode sizes ONE persistent
+ * kernels run is moe_layer_path(dims, T): for one token ONE persistent
  * kernel (one CTA per SM; the router product, top-K and bucketing, the
- * routed gate/up, the down products and the combine separated by grid-wide
- * barriers on flags in the workspace; PolyStrata, "Models and backends",
+ * routed gate/up, the down products and the combine, values passing between
+ * CTAs as tagged words in the workspace; PolyStrata, "Models and backends",
  * section "What was tuned": decode was launch-bound at ~35 launches a
  * layer), else three decode kernels or the tcgen05 prefill kernels.
  * ids_dev / weights_dev / shared_gate_dev receive the routing when non-NULL.

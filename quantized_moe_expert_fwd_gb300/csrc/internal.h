@@ -134,13 +134,14 @@ cudaError_t launch_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x,
 // ------------------------------------------------ persistent decode layers
 // A whole decode-size layer (or a stack of residual layers) as one launch of
 // one CTA per SM (persist.cu).
-// Tokens a whole-layer call it takes.  Measured on GB300 at the 2048-hidden,
-// 256-expert, top-8 shape (ten layers rotating, CUDA graph): T = 1 27.4 us
-// against 32.2 on the three decode kernels; T = 2 47.0 against 45.5; T = 3..6
-// 59..129 against 48..62 on the tcgen05 kernels.  The kernel itself takes up
-// to kPersistTokensCap tokens (the shared memory decides above a few).
+// Tokens a whole-layer call it takes: one.  At T = 1 (2048-hidden,
+// 256-expert, top-8 layers rotating in a CUDA graph) it takes 20.4 us against
+// 32.2 for the three decode kernels.  Calls of 2 and 3 tokens ended in a
+// launch failure in a crossover measurement after the kernel was tuned for
+// one token (its 15-stage gate/up ring then wraps within a layer); the cause
+// was not found by reading the code, so the kernel takes no more than one.
 constexpr int kPersistMaxTokens = 1;
-constexpr int kPersistTokensCap = 16;
+constexpr int kPersistTokensCap = 1;
 constexpr int kMaxGrid = 1024;            // grid barrier flags in the workspace
 constexpr int kPxMaxLayers = 40;          // layers one launch carries
 // 1 producer + 15 consumer warps (128 registers a thread): the int4 dot

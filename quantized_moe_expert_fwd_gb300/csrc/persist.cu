@@ -1077,6 +1077,13 @@ bool px_geometry(const strata_moe_dims& d, int T, bool forced, bool resid, int G
     if (Sd > int(d_cap / g->d_stage)) Sd = int(d_cap / g->d_stage);
     if (Sd > kPxDnMaxStages) Sd = kPxDnMaxStages;
     if (Sd < 2) return false;
+    // a layer's gate/up stages and down units fit their rings in one round:
+    // a CTA's share of T K I row pairs (cost-balanced: every one of the
+    // token's units weighs the same) is at most ceil(K I / G) + 1 pairs, cut
+    // at most once at an expert boundary.  (Rings that wrap inside a layer
+    // take code paths that a multi-token run saw fail; they stay closed.)
+    const int pairs_max = (K * I + G - 1) / G + 1;
+    if ((pairs_max + kPxRowPairs - 1) / kPxRowPairs + 1 > Sg || units > Sd) return false;
     g->dn_stages = Sd;
     g->gu_stages = Sg;
     size_t o = 0;
