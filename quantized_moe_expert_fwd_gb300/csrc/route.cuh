@@ -312,9 +312,12 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
 // Top-K of one token's logits (larger first, ties to the lower id), written
 // in ascending id to ids[0..K) with renormalised softmax weights w[0..K).
 // One warp.  L: this warp's shared scratch of E words; ex: K floats.
-// A lane keeps the best key of its own logits (ids lane, lane+32, ...); each
-// pick is a warp maximum of the lanes' bests (redux), then the lowest id
-// holding it, after which only the winning lane rescans its own logits.
+// Up to 256 logits and K <= 8: merged sorted lists (select_topk_merge), with
+// no reduction per pick.  Otherwise, and where that cannot decide the K-th
+// pick exactly, a lane keeps the best key of its own logits (ids lane,
+// lane+32, ...); each pick is a warp maximum of the lanes' bests (redux),
+// then the lowest id holding it, after which only the winning lane rescans
+// its own logits.
 __device__ inline void select_topk_keys(int E, int K, uint32_t* Lk, float* ex, int* ids, float* w,
                                         int lane);
 
@@ -332,6 +335,24 @@ __device__ inline void select_topk_warp(const float* lg, int E, int K, float* L,
             if (e0 + 32 * j < E) Lk[e0 + 32 * j] = logit_key(v[j]);
     }
     select_topk_keys(E, K, Lk, ex, ids, w, lane);
+}
+
+// The softmax weights of a selected set, the same arithmetic whichever way
+// the set was found: lane k < K holds pick k (id mye, order-preserving key
+// myk), mk is the largest key of the set.  ids ascending, renormalised.
+__device__ __forceinline__ void topk_weights(int K, uint32_t myk, uint32_t mye, uint32_t mk,
+                                             int rank, float* ex, int* ids, float* w, int lane) {
+    float e_k = 0.0f;
+    if (lane < K) {
+        e_k = expf(key_logit(myk) - key_logit(mk));
+        ex[rank] = e_k;
+        ids[rank] = int(mye);
+    }
+    __syncwarp();
+    float sum = 0.0f;
+    for (int r = 0; r < K; ++r) sum += ex[r];                 // ascending id
+    if (lane < K) w[rank] = e_k / sum;
+    __syncwarp();
 }
 
 // The selection itself on the order-preserving keys Lk[0..E) already in
@@ -377,25 +398,103 @@ __device__ inline void select_topk_reg(int E, int K, const uint32_t* Lk, float* 
             }
         }
     }
-    const float myv = key_logit(myk);
-    const float m = __shfl_sync(0xffffffffu, myv, 0);      // the first pick is the largest
+    const uint32_t mk = __shfl_sync(0xffffffffu, myk, 0);    // the first pick is the largest
     int rank = 0;
     for (int j = 0; j < K; ++j) rank += (__shfl_sync(0xffffffffu, mye, j) < mye) ? 1 : 0;
-    float e_k = 0.0f;
-    if (lane < K) {
-        e_k = expf(myv - m);
-        ex[rank] = e_k;
-        ids[rank] = int(mye);
+    topk_weights(K, myk, mye, mk, rank, ex, ids, w, lane);
+}
+
+// Eight u32 in registers, descending (a bitonic sorting network).
+__device__ __forceinline__ void cas_desc(uint32_t& a, uint32_t& b) {
+    const uint32_t hi = max(a, b), lo = min(a, b);
+    a = hi;
+    b = lo;
+}
+__device__ __forceinline__ void sort8_desc(uint32_t (&a)[8]) {
+#pragma unroll
+    for (int k = 2; k <= 8; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int l = i ^ j;
+                if (l > i) {
+                    if ((i & k) == 0)
+                        cas_desc(a[i], a[l]);
+                    else
+                        cas_desc(a[l], a[i]);
+                }
+            }
+}
+
+// Top-K (K <= 8) of E <= 256 keys without a warp reduction per pick.  A
+// logit's sort word is its key with the low 8 bits replaced by 255 - id:
+// distinct words, ordered by key and, within equal upper bits, by lower id.
+// A lane sorts its eight words; five butterfly rounds merge the lanes'
+// lists (the larger halves of a list against its partner's reversed list
+// hold the top eight of both, then a bitonic merge sorts them), keeping the
+// largest word dropped on the way, so every lane ends with the top eight
+// words and the ninth.  The set equals the exact top-K unless the K-th and
+// (K+1)-th words agree in their upper 24 bits (keys that close, or NaN keys):
+// then the function returns false and the exact selection runs instead.
+__device__ inline bool select_topk_merge(int E, int K, const uint32_t* Lk, float* ex, int* ids,
+                                         float* w, int lane) {
+    __syncwarp();
+    uint32_t t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        t[i] = e < E ? ((Lk[e] & 0xFFFFFF00u) | uint32_t(255 - e)) : 0u;
     }
-    __syncwarp();
-    float sum = 0.0f;
-    for (int r = 0; r < K; ++r) sum += ex[r];                 // ascending id
-    if (lane < K) w[rank] = e_k / sum;
-    __syncwarp();
+    sort8_desc(t);
+    uint32_t d9 = 0u;                          // the largest word dropped so far
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t b[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b[i] = __shfl_xor_sync(0xffffffffu, t[i], d);
+        uint32_t dm = __shfl_xor_sync(0xffffffffu, d9, d);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            dm = max(dm, min(t[i], b[7 - i]));
+            t[i] = max(t[i], b[7 - i]);
+        }
+        d9 = max(d9, dm);
+#pragma unroll
+        for (int j = 4; j > 0; j >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if ((i ^ j) > i) cas_desc(t[i], t[i ^ j]);
+    }
+    uint32_t cK = 0u, nxt = d9, myc = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i == K - 1) cK = t[i];
+        if (i == K) nxt = t[i];
+        if (i == lane) myc = t[i];
+    }
+    const uint32_t up = cK & 0xFFFFFF00u;
+    if (up == 0u || up == (nxt & 0xFFFFFF00u)) return false;     // warp-uniform
+    // the largest key of the set: among the words whose upper bits equal the
+    // first word's (usually the first alone)
+    const uint32_t up0 = t[0] & 0xFFFFFF00u;
+    uint32_t mk = Lk[255u - (t[0] & 255u)];
+#pragma unroll
+    for (int j = 1; j < 8; ++j)
+        if (j < K && (t[j] & 0xFFFFFF00u) == up0) mk = max(mk, Lk[255u - (t[j] & 255u)]);
+    const uint32_t mye = 255u - (myc & 255u);
+    int rank = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (j < K && 255u - (t[j] & 255u) < mye) ++rank;
+    const uint32_t myk = lane < K ? Lk[mye] : 0u;
+    topk_weights(K, myk, mye, mk, rank, ex, ids, w, lane);
+    return true;
 }
 
 __device__ inline void select_topk_keys(int E, int K, uint32_t* Lk, float* ex, int* ids, float* w,
                                         int lane) {
+    if (E <= 256 && K <= 8 && select_topk_merge(E, K, Lk, ex, ids, w, lane)) return;
     if (E <= 32)
         select_topk_reg<1>(E, K, Lk, ex, ids, w, lane);
     else if (E <= 64)
