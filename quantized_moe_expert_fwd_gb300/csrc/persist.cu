@@ -243,10 +243,34 @@ __device__ __forceinline__ float px_router_dot(uint32_t wrow, uint32_t xrow, int
 }
 
 // Token x from shared memory: the lane's bf16 words of chunks lane and
-// lane + 32 and their fp32 sums.
+// lane + 32.
 template <int MC>
-__device__ __forceinline__ void px_load_x(uint32_t xrow, int NC, int lane, uint32_t (&xb)[MC][16],
-                                          float (&X)[MC]) {
+__device__ __forceinline__ void px_load_x(uint32_t xrow, int NC, int lane,
+                                          uint32_t (&xb)[MC][16]) {
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+        const int c = lane + 32 * m;
+        if (c < NC) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint4 u = lds128(xrow + 16u * (v * NC + c));
+                xb[m][4 * v] = u.x;
+                xb[m][4 * v + 1] = u.y;
+                xb[m][4 * v + 2] = u.z;
+                xb[m][4 * v + 3] = u.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xb[m][j] = 0u;
+        }
+    }
+}
+
+// The fp32 sums of the same two chunks (the offset term of every group's
+// dot product): taken once a layer, they serve every row.
+template <int MC>
+__device__ __forceinline__ float2 px_x_sums(uint32_t xrow, int NC, int lane) {
+    float X[2] = {0.0f, 0.0f};
 #pragma unroll
     for (int m = 0; m < MC; ++m) {
         const int c = lane + 32 * m;
@@ -257,17 +281,12 @@ __device__ __forceinline__ void px_load_x(uint32_t xrow, int NC, int lane, uint3
                 const uint4 u = lds128(xrow + 16u * (v * NC + c));
                 const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    xb[m][4 * v + i] = wv[i];
-                    sum += bf16_lo(wv[i]) + bf16_hi(wv[i]);
-                }
+                for (int i = 0; i < 4; ++i) sum += bf16_lo(wv[i]) + bf16_hi(wv[i]);
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) xb[m][j] = 0u;
         }
         X[m] = sum;
     }
+    return make_float2(X[0], X[1]);
 }
 
 // Rows r < nrows (<= NR) of length H (packed bytes at q + r * qs, fp16
@@ -301,15 +320,17 @@ __device__ __forceinline__ void px_rows_dot(uint32_t q, uint32_t s, uint32_t qs,
 
 // silu(gate) * up of one gate/up row pair (packed bytes at q, the up row at
 // q + H/2; fp16 scales at s, the up row's at s + H/16; shared memory) for
-// the token whose activations are at xrow.  Out of line: phase R (the
+// the token whose activations are at xrow, their chunk sums xs.  Out of line: phase R (the
 // shared expert) and phase G (the routed experts) run the same instructions,
 // so the second finds them in the instruction cache.
 template <int MC>
-__device__ __noinline__ float px_pair_silu(uint32_t q, uint32_t s, uint32_t xrow, int NC,
-                                           int lane) {
+__device__ __noinline__ float px_pair_silu(uint32_t q, uint32_t s, uint32_t xrow, float2 xs,
+                                           int NC, int lane) {
     uint32_t xb[MC][16];
+    px_load_x<MC>(xrow, NC, lane, xb);
     float X[MC];
-    px_load_x<MC>(xrow, NC, lane, xb, X);
+    X[0] = xs.x;
+    if constexpr (MC > 1) X[1] = xs.y;
     float gu[2];
     px_rows_dot<MC, 2>(q, s, uint32_t(NC) * 16u, uint32_t(NC) * 2u, 2, xb, X, NC, lane, gu);
     return silu_mul(gu[0], gu[1]);
@@ -750,6 +771,9 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
             }
         }
         px_cbar();
+        // the token's chunk sums, for every gate/up row pair of the layer
+        static_assert(kPersistMaxTokens == 1, "one token's chunk sums a layer");
+        const float2 xsum = px_x_sums<MC>(sx, NC, lane);
 
         // ---- R: router rows and shared gate/up row pairs of this CTA
         if (!px_wait(&r_full, l & 1, err)) latch_timeout(err, 71, 0, l, 0);
@@ -771,7 +795,8 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                     const uint32_t qg = rq + uint32_t(2 * pl) * (H / 2);
                     const uint32_t sgs = rs_ + uint32_t(2 * pl) * (H / 16);
                     for (int t = 0; t < T; ++t) {
-                        const float hv = px_pair_silu<MC>(qg, sgs, sx + uint32_t(t) * H * 2, NC, lane);
+                        const float hv = px_pair_silu<MC>(qg, sgs, sx + uint32_t(t) * H * 2, xsum,
+                                                          NC, lane);
                         if (lane == 0) ll_put(a.ll_hs + size_t(t) * Is + p, hv, tg_s);
                     }
                 }
@@ -901,7 +926,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                     for (int p = 0; p < nb; ++p) {
                         const float hv = px_pair_silu<MC>(sq + uint32_t(p) * H,
                                                           ssc + uint32_t(p) * (H / 8),
-                                                          sx + uint32_t(t) * H * 2, NC, lane);
+                                                          sx + uint32_t(t) * H * 2, xsum, NC, lane);
                         if (lane == 0) ll_put(a.ll_h + size_t(s) * I + ii0 + p, hv, tg_h);
                     }
                 }
