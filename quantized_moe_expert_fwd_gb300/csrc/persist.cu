@@ -691,58 +691,53 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         // ---- the layer input x (bf16) into shared memory
         if constexpr (RESID) {
             // RMSNorm of the residual: the caller's (plain) before the first
-            // layer, the previous layer's tagged words after it
-            // (pass 1 parks the fp32 residual at the start of the gate/up ring,
-            // idle between the layer's down products and its next gate/up)
+            // layer, the previous layer's tagged words after it.  Every
+            // consumer thread gathers eight elements at once (one round trip
+            // for the whole vector), parked as fp32 at the start of the
+            // gate/up ring (idle between the layer's down products and its
+            // next gate/up); then warp t reduces token t in the lane order
+            // of the one-warp norm.
             float* raw = reinterpret_cast<float*>(px + a.off_g);
+            const uint32_t tg = tag(l - 1, 2);
+            for (int g = ctid; g < T * (H / 8); g += NT) {
+                const int t = g / (H / 8), h = (g - t * (H / 8)) * 8;
+                float4 v0, v1;
+                if (l == 0) {
+                    v0 = ldcg_f4(a.resid + size_t(t) * H + h);
+                    v1 = ldcg_f4(a.resid + size_t(t) * H + h + 4);
+                } else {
+                    const uint64_t* lt = a.ll_resid + size_t(t) * H + h;
+                    bool ok = false;
+                    uint64_t w[8];
+                    for (uint32_t it = 0; it < lim && !ok; ++it) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) ll_ld2(lt + 2 * i, w[2 * i], w[2 * i + 1]);
+                        ok = true;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) ok &= ll_has(w[i], tg);
+                        if (!ok && (it & 255u) == 255u &&
+                            ld_relaxed_u32(err) == uint32_t(STRATA_ETIMEOUT))
+                            break;
+                        if (!ok) px_backoff();
+                    }
+                    if (!ok) latch_timeout(err, 83, t, l, h);
+                    v0 = make_float4(ll_val(w[0]), ll_val(w[1]), ll_val(w[2]), ll_val(w[3]));
+                    v1 = make_float4(ll_val(w[4]), ll_val(w[5]), ll_val(w[6]), ll_val(w[7]));
+                }
+                *reinterpret_cast<float4*>(raw + size_t(t) * H + h) = v0;
+                *reinterpret_cast<float4*>(raw + size_t(t) * H + h + 4) = v1;
+            }
+            px_cbar();
             for (int t = cw; t < T; t += kPxConsumers) {
-                const float* rt = a.resid + size_t(t) * H;
-                const uint64_t* lt = a.ll_resid + size_t(t) * H;
-                float* rw = raw + size_t(t) * H;
-                const uint32_t tg = tag(l - 1, 2);
+                const float* rw = raw + size_t(t) * H;
                 float ss = 0.0f;
 #pragma unroll 1
                 for (int h0 = lane * 4; h0 < H; h0 += 128 * 4) {
-                    // up to four groups of four a lane, all requested at once
-                    float4 v[4];
-                    if (l == 0) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            if (h0 + 128 * i < H) v[i] = ldcg_f4(rt + h0 + 128 * i);
-                    } else {
-                        bool ok = false;
-                        for (uint32_t it = 0; it < lim && !ok; ++it) {
-                            uint64_t w[16];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                if (h0 + 128 * i < H) {
-                                    ll_ld2(lt + h0 + 128 * i, w[4 * i], w[4 * i + 1]);
-                                    ll_ld2(lt + h0 + 128 * i + 2, w[4 * i + 2], w[4 * i + 3]);
-                                } else {
-                                    w[4 * i] = w[4 * i + 1] = w[4 * i + 2] = w[4 * i + 3] =
-                                        uint64_t(tg) << 32;
-                                }
-                            }
-                            ok = true;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) ok &= ll_has(w[i], tg);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                v[i] = make_float4(ll_val(w[4 * i]), ll_val(w[4 * i + 1]),
-                                                   ll_val(w[4 * i + 2]), ll_val(w[4 * i + 3]));
-                            if (!ok && (it & 255u) == 255u &&
-                                ld_relaxed_u32(err) == uint32_t(STRATA_ETIMEOUT))
-                                break;
-                            if (!ok) px_backoff();
-                        }
-                        if (!ok) latch_timeout(err, 83, t, l, h0);
-                    }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         if (h0 + 128 * i < H) {
-                            *reinterpret_cast<float4*>(rw + h0 + 128 * i) = v[i];
-                            ss += (v[i].x * v[i].x + v[i].y * v[i].y) +
-                                  (v[i].z * v[i].z + v[i].w * v[i].w);
+                            const float4 v = *reinterpret_cast<const float4*>(rw + h0 + 128 * i);
+                            ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
                         }
                     }
                 }
