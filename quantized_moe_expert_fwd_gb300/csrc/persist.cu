@@ -453,6 +453,8 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
     __shared__ float s_w[kDecodeMaxTokens * kMaxTopK];
     __shared__ int s_inv[kDecodeMaxTokens * kMaxTopK];
     __shared__ float s_sig[kDecodeMaxTokens];
+    __shared__ float s_res[kPersistMaxTokens * 16];     // this CTA's rows of the residual
+    __shared__ float s_den[kPersistMaxTokens];          // the RMSNorm denominators
     __shared__ __align__(8) uint64_t r_full, r_empty, plan_full, plan_free;
     __shared__ __align__(8) uint64_t sd_full[2], sd_empty[2];
     __shared__ __align__(8) uint64_t g_full[kPxGuMaxStages], g_empty[kPxGuMaxStages];
@@ -728,6 +730,11 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                 *reinterpret_cast<float4*>(raw + size_t(t) * H + h + 4) = v1;
             }
             px_cbar();
+            // this CTA's rows of it, for the residual add after the combine
+            for (int i = ctid; i < T * nrow; i += NT) {
+                const int t = i / nrow, r = i - t * nrow;
+                s_res[t * 16 + r] = raw[size_t(t) * H + o0 + r];
+            }
             for (int t = cw; t < T; t += kPxConsumers) {
                 const float* rw = raw + size_t(t) * H;
                 float ss = 0.0f;
@@ -742,20 +749,24 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                     }
                 }
                 ss = warp_sum(ss);
-                const float denom = sqrtf(ss / float(H) + a.eps);
+                if (lane == 0) s_den[t] = sqrtf(ss / float(H) + a.eps);
+            }
+            px_cbar();
+            // the normalised token rows into shared memory (bf16, chunk-interleaved)
+            for (int i = ctid; i < T * (H / 4); i += NT) {
+                const int t = i / (H / 4), h = (i - t * (H / 4)) * 4;
+                const float denom = s_den[t];
+                const float4 v = *reinterpret_cast<const float4*>(raw + size_t(t) * H + h);
+                const uint32_t p0 = uint32_t(f32_to_bf16(v.x / denom)) |
+                                    (uint32_t(f32_to_bf16(v.y / denom)) << 16);
+                const uint32_t p1 = uint32_t(f32_to_bf16(v.z / denom)) |
+                                    (uint32_t(f32_to_bf16(v.w / denom)) << 16);
+                const int c = h >> 5, v8 = (h & 31) >> 3;
                 uint8_t* xt = px + a.off_x + size_t(t) * H * 2;
-                for (int h = lane * 4; h < H; h += 128) {
-                    const float4 v = *reinterpret_cast<const float4*>(rw + h);
-                    const uint32_t p0 = uint32_t(f32_to_bf16(v.x / denom)) |
-                                        (uint32_t(f32_to_bf16(v.y / denom)) << 16);
-                    const uint32_t p1 = uint32_t(f32_to_bf16(v.z / denom)) |
-                                        (uint32_t(f32_to_bf16(v.w / denom)) << 16);
-                    const int c = h >> 5, v8 = (h & 31) >> 3;
-                    *reinterpret_cast<uint2*>(xt + 16 * (v8 * NC + c) + 2 * (h & 7)) =
-                        make_uint2(p0, p1);
-                    if (a.x_out != nullptr && b == 0 && last)
-                        *reinterpret_cast<uint2*>(a.x_out + size_t(t) * H + h) = make_uint2(p0, p1);
-                }
+                *reinterpret_cast<uint2*>(xt + 16 * (v8 * NC + c) + 2 * (h & 7)) =
+                    make_uint2(p0, p1);
+                if (a.x_out != nullptr && b == 0 && last)
+                    *reinterpret_cast<uint2*>(a.x_out + size_t(t) * H + h) = make_uint2(p0, p1);
             }
         } else {
             uint4* xs = reinterpret_cast<uint4*>(px + a.off_x);
@@ -1002,7 +1013,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                 if (write_out) a.out[size_t(t) * H + o] = ob;
                 if constexpr (RESID) {
                     float* rp = a.resid + size_t(t) * H + o;
-                    const float rn = __ldcg(rp) + __uint_as_float(uint32_t(ob) << 16);
+                    const float rn = s_res[t * 16 + r] + __uint_as_float(uint32_t(ob) << 16);
                     *rp = rn;
                     if (!last) ll_put(a.ll_resid + size_t(t) * H + o, rn, tg_r);
                 }
