@@ -1019,8 +1019,10 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                 }
             }
         }
-        // the last layer's routing and bucketing, by CTA 0 off the critical path
-        if (last && b == 0) {
+        // the last layer's routing and bucketing, by the last CTA (the one
+        // with the fewest output rows, done first), so that no CTA with a
+        // full share of the down products ends later for it
+        if (last && b == G - 1) {
             publish_bucket(TK, E, P, s_inv, BucketOut{a.counts, a.offsets, a.perm, a.inv, nullptr},
                            ctid, NT);
             for (int p = ctid; p < TK; p += NT) {
