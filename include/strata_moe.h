@@ -394,6 +394,26 @@ STRATA_API strata_status moe_get_device_status(void* ws_dev, void* stream);
  * into shared memory are always waited for in full. */
 STRATA_API void strata_set_grid_wait_limit(uint32_t polls);
 
+/* Phase timestamps of the persistent kernel (the one-token layer and the
+ * stack, moe_layer_path() == 1), for a library built with phase tracing
+ * (quantized_moe_expert_fwd_gb300.build.build(trace=True), which compiles
+ * with STRATA_PX_TRACE; the default library records none and returns
+ * STRATA_EUNSUPPORTED).  Copies min(bytes, 512 KiB) of the last launch's
+ * record to host memory `host`: uint64 global-timer readings in ns, laid out
+ * [CTA 0..1023][slot 0..3][point 0..15]; slots are the launch's layers 0, 1,
+ * n/2 and n-1 (the first match), points:
+ *   0 CTA initialised (slot 0 only)      1 grid dependency resolved (slot 0)
+ *   2 token row in shared memory         3 router rows and shared pairs done
+ *   4 token 0's logits all seen          5 token 0's top-K and gate done
+ *   6 plan published                     7 the CTA's gate/up stages done
+ *   8 SwiGLU rows staged                 9 down products done
+ *  10 combined                          11 producer: plan seen
+ *  12 producer: gate/up copies issued   13 producer: down copies issued
+ * (unused entries are left as they were).  Synchronises the device.
+ * Returns STRATA_EINVAL for a NULL `host` or zero `bytes`, STRATA_ECUDA when
+ * the copy fails. */
+STRATA_API strata_status strata_px_trace_read(void* host, size_t bytes);
+
 /* Static, human-readable name of a status. */
 STRATA_API const char* strata_status_str(strata_status s);
 

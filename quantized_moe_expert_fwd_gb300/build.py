@@ -19,6 +19,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libstrata_moe.so")
+# the same library with the persistent kernel's phase timestamps recorded
+# (STRATA_PX_TRACE): a separate file, never the one the package loads
+TRACE_BUILD_DIR = os.path.join(HERE, "_build_trace")
+TRACE_LIB_PATH = os.path.join(HERE, "libstrata_moe_trace.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -36,7 +40,7 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stamp() -> str:
+def _stamp(flags) -> str:
     h = hashlib.sha256()
     files = _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
         sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [os.path.join(INCLUDE, "strata_moe.h")]
@@ -44,24 +48,27 @@ def _stamp() -> str:
         h.update(f.encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    h.update(" ".join(flags).encode())
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    stamp_file = os.path.join(BUILD_DIR, "stamp")
-    stamp = _stamp()
-    if not force and os.path.exists(LIB_PATH) and os.path.exists(stamp_file):
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """The library (trace: the phase-traced one at TRACE_LIB_PATH); returns its path."""
+    build_dir, lib_path = (TRACE_BUILD_DIR, TRACE_LIB_PATH) if trace else (BUILD_DIR, LIB_PATH)
+    flags = NVCC_FLAGS + (["-DSTRATA_PX_TRACE=1"] if trace else [])
+    os.makedirs(build_dir, exist_ok=True)
+    stamp_file = os.path.join(build_dir, "stamp")
+    stamp = _stamp(flags)
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read() == stamp:
-                return LIB_PATH
+                return lib_path
     cc = nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [cc, *flags, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -73,15 +80,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB_PATH + f".{os.getpid()}.tmp"
+    tmp = lib_path + f".{os.getpid()}.tmp"
     r = subprocess.run([cc, *ARCH, "-shared", "--cudart", "static", "-o", tmp, *objs],
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":

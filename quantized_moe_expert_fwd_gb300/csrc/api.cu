@@ -1011,6 +1011,13 @@ strata_status moe_layer_bucketing(const strata_moe_dims* dims, int32_t T, const 
 
 void strata_set_grid_wait_limit(uint32_t polls) { set_grid_wait_limit(polls); }
 
+strata_status strata_px_trace_read(void* host, size_t bytes) {
+    if (host == nullptr || bytes == 0) return STRATA_EINVAL;
+    const cudaError_t e = px_trace_copy(host, bytes);
+    if (e == cudaErrorNotSupported) return STRATA_EUNSUPPORTED;
+    return cuda_status(e);
+}
+
 const char* strata_last_cuda_error(void) {
     return t_last_cuda == cudaSuccess ? "no error" : cudaGetErrorName(t_last_cuda);
 }

@@ -199,6 +199,16 @@ struct PxArgs {
 // geometry.
 bool px_geometry(const strata_moe_dims& d, int T, bool forced, bool resid, int G, PxGeo* g);
 cudaError_t launch_persistent(const PxArgs& a, const PxGeo& g, cudaStream_t s);
+
+// Phase timestamps of the persistent kernel, recorded only by a library
+// built with STRATA_PX_TRACE (the default build has none): per CTA, for the
+// last launch's layers 0, 1, n/2 and n-1 (slots 0..3), kPxTracePoints
+// global-timer readings (ns), the points of strata_px_trace_read.
+constexpr int kPxTraceSlots = 4;
+constexpr int kPxTracePoints = 16;
+constexpr size_t kPxTraceBytes = size_t(kMaxGrid) * kPxTraceSlots * kPxTracePoints * 8;
+// Copies the timestamps to host memory; cudaErrorNotSupported without tracing.
+cudaError_t px_trace_copy(void* host, size_t bytes);
 // polls before a grid barrier of the persistent kernel gives up (testing
 // hook, strata_set_grid_wait_limit; 0: the default)
 uint32_t grid_wait_limit();

@@ -65,6 +65,22 @@ uint32_t grid_wait_limit() {
 
 void set_grid_wait_limit(uint32_t polls) { g_grid_wait_limit.store(polls, std::memory_order_relaxed); }
 
+// ------------------------------------------------------------ phase trace
+#ifdef STRATA_PX_TRACE
+__device__ unsigned long long g_px_trace[kMaxGrid * kPxTraceSlots * kPxTracePoints];
+// The global timer at phase point `pt` of layer l (of n) into this CTA's
+// slot for that layer (layers 0, 1, n/2, n-1; others are not recorded).
+__device__ __forceinline__ void px_trace(int l, int n, int pt) {
+    const int slot = l == 0 ? 0 : l == 1 ? 1 : l == n / 2 ? 2 : l == n - 1 ? 3 : -1;
+    if (slot < 0) return;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    g_px_trace[(size_t(blockIdx.x) * kPxTraceSlots + slot) * kPxTracePoints + pt] = t;
+}
+#else
+__device__ __forceinline__ void px_trace(int, int, int) {}
+#endif
+
 // ------------------------------------------------------------ primitives
 __device__ __forceinline__ void px_cbar() {   // the consumer warps only
     asm volatile("bar.sync 1, %0;" ::"r"(kPxConsumers * 32) : "memory");
@@ -500,6 +516,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         mbar_fence_init();
     }
     __syncthreads();
+    if (tid == 32) px_trace(0, a.n_layers, 0);
 
     const RShare rsh = px_r_share(b, G, nR, Is, H);
 
@@ -544,6 +561,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
             const PxLayer& Lr = a.L[l];
             if (!px_wait(&plan_full, l & 1, err)) latch_timeout(err, 60, 0, l, 0);
             px_fence_proxy_async();
+            if (lane == 0) px_trace(l, a.n_layers, 11);
             // gate/up stages of this CTA's share, then its down rows of every
             // touched expert.  The first S of them (S the ring's slots) reuse
             // slots last filled in an earlier layer, whose consumers are done
@@ -624,6 +642,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                 __syncwarp();
             }
             for (int k = 0; k < nst; ++k) gpos.next(Sg);
+            if (lane == 0) px_trace(l, a.n_layers, 12);
             // the down units: the same split
             const int nd0 = min(P.n, Sd);
             for (int j = lane; j < nd0; j += 32) {
@@ -648,6 +667,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                 __syncwarp();
             }
             for (int j = 0; j < P.n; ++j) dpos.next(Sd);
+            if (lane == 0) px_trace(l, a.n_layers, 13);
             if (lane == 0) {
                 mbar_arrive(&plan_free);          // P no longer read here
                 // the next layer's routing-independent rows
@@ -683,6 +703,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
     constexpr int NT = kPxConsumers * 32;
     const uint32_t lim = a.grid_wait_limit;
     pdl_wait();
+    if (ctid == 0) px_trace(0, a.n_layers, 1);
     // the workspace's exchange count: this launch's tags follow it
     const uint32_t tag0 = ld_relaxed_u32(a.flags + b);
     auto tag = [&](int l, int ex) { return tag0 + uint32_t(kPxExchanges * l + ex) + 1u; };
@@ -780,6 +801,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         // the token's chunk sums, for every gate/up row pair of the layer
         static_assert(kPersistMaxTokens == 1, "one token's chunk sums a layer");
         const float2 xsum = px_x_sums<MC>(sx, NC, lane);
+        if (ctid == 0) px_trace(l, a.n_layers, 2);
 
         // ---- R: router rows and shared gate/up row pairs of this CTA
         if (!px_wait(&r_full, l & 1, err)) latch_timeout(err, 71, 0, l, 0);
@@ -809,7 +831,10 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
             }
         }
         px_cbar();
-        if (ctid == 0) mbar_arrive(&r_empty);
+        if (ctid == 0) {
+            px_trace(l, a.n_layers, 3);
+            mbar_arrive(&r_empty);
+        }
 
         // ---- S: selection and bucketing (the same in every CTA)
         if (l > 0 && ctid == 0 && !px_wait(&plan_free, (l - 1) & 1, err))
@@ -854,6 +879,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                     if (!ok) px_backoff();
                 }
                 if (!ok && lane == 0) latch_timeout(err, 80, t, tg_l, 0);
+                if (t == 0 && lane == 0) px_trace(l, a.n_layers, 4);
                 gl = __shfl_sync(0xffffffffu, gl, E & 31);
                 if (a.forced_ids != nullptr) {
                     const int32_t* fi = a.forced_ids + size_t(l) * TK + size_t(t) * K;
@@ -869,6 +895,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                                      s_w + t * K, lane);
                 }
                 if (lane == 0) s_sig[t] = 1.0f / (1.0f + expf(-gl));
+                if (t == 0 && lane == 0) px_trace(l, a.n_layers, 5);
             }
         }
         px_cbar();
@@ -904,7 +931,10 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
         }
         px_fence_proxy_async();
         px_cbar();
-        if (ctid == 0) mbar_arrive(&plan_full);
+        if (ctid == 0) {
+            mbar_arrive(&plan_full);
+            px_trace(l, a.n_layers, 6);
+        }
 
         // ---- G: gate/up + SwiGLU, one warp a stage of this CTA's row pairs
         {
@@ -948,9 +978,11 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
             for (int i = ctid; i < (TK + T) * R; i += NT) s_y[i] = 0.0f;
             // every warp's gate/up stages are computed: the ring holds h now
             px_cbar();
+            if (ctid == 0) px_trace(l, a.n_layers, 7);
             float* hsm = reinterpret_cast<float*>(px + a.off_g);
             px_stage_h(a.ll_h, a.ll_hs, tg_h, TK, I, T, Is, hsm, ctid, NT, lim, err);
             px_cbar();
+            if (ctid == 0) px_trace(l, a.n_layers, 8);
             const uint32_t hb = sg;
             // tasks: first the shared unit's np_s passes, then np_r passes of
             // each routed unit j (in the ring's order: unit j in the slot j
@@ -999,6 +1031,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
             }
             for (int j = 0; j < n; ++j) dpos.next(Sd);
             px_cbar();
+            if (ctid == 0) px_trace(l, a.n_layers, 9);
             const bool write_out = a.out != nullptr && (last || !RESID);
             for (int i = ctid; i < T * nrow; i += NT) {
                 const int t = i / nrow, r = i - t * nrow, o = o0 + r;
@@ -1019,6 +1052,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
                 }
             }
         }
+        if (ctid == 0) px_trace(l, a.n_layers, 10);
         // the last layer's routing and bucketing, by the last CTA (the one
         // with the fewest output rows, done first), so that no CTA with a
         // full share of the down products ends later for it
@@ -1042,6 +1076,17 @@ __global__ void __launch_bounds__(kPxThreads, 1) k_persist(const __grid_constant
 }
 
 // ------------------------------------------------------------------ launch
+cudaError_t px_trace_copy(void* host, size_t bytes) {
+#ifdef STRATA_PX_TRACE
+    if (bytes > kPxTraceBytes) bytes = kPxTraceBytes;
+    return cudaMemcpyFromSymbol(host, g_px_trace, bytes);
+#else
+    (void)host;
+    (void)bytes;
+    return cudaErrorNotSupported;
+#endif
+}
+
 namespace {
 
 size_t align128(size_t x) { return (x + 127) & ~size_t(127); }

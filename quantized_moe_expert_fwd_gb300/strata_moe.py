@@ -46,8 +46,21 @@ class LayerPtrs(ctypes.Structure):
     _fields_ = [(n + "_dev", ctypes.c_void_p) for n in _LAYER_FIELDS]
 
 
+_path_override = None
+
+
 def lib_path() -> str:
-    return _build.LIB_PATH
+    return _path_override or _build.LIB_PATH
+
+
+def use_library(path: str) -> None:
+    """Load `path` instead of libstrata_moe.so (the phase-traced build of the
+    same sources); only before the first call loads a library."""
+    global _path_override
+    with _lock:
+        if _lib is not None and path != lib_path():
+            raise RuntimeError("a library is already loaded in this process")
+        _path_override = path
 
 
 def load() -> ctypes.CDLL:
@@ -56,7 +69,7 @@ def load() -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
+        path = lib_path()
         if not os.path.exists(path):
             raise RuntimeError(f"{path} is missing: run quantized_moe_expert_fwd_gb300.build.build()"
                                " (the CUDA library is required; there is no fallback)")
@@ -88,6 +101,7 @@ def load() -> ctypes.CDLL:
             "moe_layer_bucketing": (I32, [D, I32, P, SZ, P, P, P, P, P]),
             "moe_get_device_status": (I32, [P, P]),
             "strata_set_grid_wait_limit": (None, [ctypes.c_uint32]),
+            "strata_px_trace_read": (I32, [P, SZ]),
             "strata_status_str": (ctypes.c_char_p, [I32]),
             "strata_last_cuda_error": (ctypes.c_char_p, []),
         }
@@ -107,7 +121,7 @@ EXPORTED = ("moe_workspace_bytes", "moe_decode_max_tokens", "moe_layer_decode_ma
             "moe_block_forward", "moe_stack_forward", "moe_decode_route", "moe_decode_gate_up",
             "moe_decode_down_combine", "moe_layer_forward_static", "moe_layer_profile",
             "moe_layer_path", "moe_layer_bucketing", "moe_get_device_status",
-            "strata_set_grid_wait_limit",
+            "strata_set_grid_wait_limit", "strata_px_trace_read",
             "strata_status_str", "strata_last_cuda_error")
 
 
@@ -370,6 +384,15 @@ def moe_layer_bucketing(dims, T: int, ws, counts, offsets, perm, inv, stream=Non
     _check("moe_layer_bucketing", load().moe_layer_bucketing(
         ctypes.byref(d), int(T), _ptr(ws), ws.numel(), _ptr(counts), _ptr(offsets), _ptr(perm),
         _ptr(inv), _stream(stream)))
+
+
+def strata_px_trace_read(nbytes: int = 1024 * 4 * 16 * 8):
+    """The persistent kernel's phase timestamps of its last launch, as a
+    numpy uint64 array [CTA][slot][point] (a library built with
+    build.build(trace=True) only; points and slots as in strata_moe.h)."""
+    buf = np.zeros(nbytes // 8, dtype=np.uint64)
+    _check("strata_px_trace_read", load().strata_px_trace_read(buf.ctypes.data, buf.nbytes))
+    return buf.reshape(-1, 4, 16)
 
 
 def strata_set_grid_wait_limit(polls: int) -> None:
