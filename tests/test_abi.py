@@ -133,3 +133,12 @@ def test_pack_round_trip_and_interleave():
     assert np.all(gs[0::2] == 0x3800) and np.all(gs[1::2] == 0x4000)
     with pytest.raises(ValueError):
         pack.pack_int4([[8, 0]])
+
+
+def test_phase_trace_needs_the_traced_build(lib):
+    """The default library records no phase stamps: a read returns
+    STRATA_EUNSUPPORTED (no device call), a NULL buffer STRATA_EINVAL."""
+    buf = (ctypes.c_uint64 * 64)()
+    assert lib.strata_px_trace_read(ctypes.c_void_p(0), 512) == q.STRATA_EINVAL
+    assert lib.strata_px_trace_read(buf, 0) == q.STRATA_EINVAL
+    assert lib.strata_px_trace_read(buf, ctypes.sizeof(buf)) == q.STRATA_EUNSUPPORTED
