@@ -274,8 +274,9 @@ __global__ void __launch_bounds__(1024) k_pf_scan(PfScanLaunch a) {
     const int b_hi = act ? int((long long)(part + 1) * nb / P) : 0;
     constexpr int CH = 16;                // counts loaded CH blocks at a time
     int sum = 0;
+    int c1[CH];                           // kept for the second pass when one chunk is all
     for (int b0 = b_lo; b0 < b_hi; b0 += CH) {
-        int c[CH];
+        int* c = c1;
 #pragma unroll
         for (int j = 0; j < CH; ++j)
             c[j] = (b0 + j < b_hi) ? __ldcg(a.cnt_blk + size_t(b0 + j) * E + e) : 0;
@@ -308,7 +309,8 @@ __global__ void __launch_bounds__(1024) k_pf_scan(PfScanLaunch a) {
             int c[CH];
 #pragma unroll
             for (int j = 0; j < CH; ++j)
-                c[j] = (b0 + j < b_hi) ? __ldcg(a.cnt_blk + size_t(b0 + j) * E + e) : 0;
+                c[j] = (b_hi - b_lo <= CH) ? c1[j]
+                       : (b0 + j < b_hi) ? __ldcg(a.cnt_blk + size_t(b0 + j) * E + e) : 0;
 #pragma unroll
             for (int j = 0; j < CH; ++j)
                 if (b0 + j < b_hi) {
