@@ -135,7 +135,7 @@ cudaError_t launch_rmsnorm(const float* r, int T, int H, float eps, uint16_t* x,
 // A whole decode-size layer (or a stack of residual layers) as one launch of
 // one CTA per SM (persist.cu).
 // Tokens a whole-layer call it takes: one.  At T = 1 (2048-hidden,
-// 256-expert, top-8 layers rotating in a CUDA graph) it takes 20.4 us against
+// 256-expert, top-8 layers rotating in a CUDA graph) it takes 19.4 us against
 // 32.2 for the three decode kernels.  Calls of 2 and 3 tokens ended in a
 // launch failure in a crossover measurement after the kernel was tuned for
 // one token (its 15-stage gate/up ring then wraps within a layer); the cause
